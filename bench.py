@@ -1,0 +1,463 @@
+#!/usr/bin/env python3
+"""Benchmark of the tcgen05 GEMM library (one JSON line on stdout, rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-suite]
+
+A step is one GEMM C <- alpha*A*B + beta*C of the chosen workload (default: the
+2048^3 fp16 -> fp32 workload) with operands already resident in HBM.  Between
+timed steps L2 is flushed by writing a buffer larger than L2, and only the GEMM
+launch is inside each step's CUDA-event pair (on the stream the kernel runs on).
+Value = whole-job TFLOP/s (2MNK per step, logical FLOPs) over all ranks.
+
+Besides value and ms_per_step the line carries: the roofline of the GEMM kernel
+(achieved TFLOP/s or GB/s against the measured peak), the end-to-end rate through
+the host-buffer entry point gemm_host (pinned host operands, copies included),
+the CPU oracle timed on the host cores on a bounded sample, SM clocks sampled
+during the timed region, and a "suite" with the other workloads (4096^3 bf16,
+8192^3 bf16 beta, 128x8192x8192 skinny, 512^3).
+
+--impl reference times the CPU oracle (the plain FP64 triple loop) on the same
+workload, one bounded row sample per step, on the host cores.
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica
+of the workload (the GEMM does not shard across GPUs here: replicas only),
+a barrier and synchronize bracket the timed region, the time is the max over
+ranks, and value = sum of the ranks' FLOPs / that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+WORKLOAD_BY_NAME = {w["name"]: k for k, w in si.WORKLOADS.items()}
+DEFAULT_WORKLOAD = si.WORKLOADS[2]["name"]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20    # > 129 MB L2
+CSRC = os.path.join(ROOT, "dense_tensor_core_tcgen05_gb300", "csrc")
+
+
+# ------------------------------------------------------------------ helpers
+
+def gemm_flops(M, N, K):
+    """Logical FLOPs, 2MNK (one multiply and one add per inner-loop step)."""
+    return 2 * M * N * K
+
+
+def algorithmic_bytes(w):
+    """Compulsory HBM bytes of one GEMM: each input read once, C written once
+    (and read once when beta != 0)."""
+    isz = 2
+    osz = 4 if w["out_dtype"] == "f32" else 2
+    b = w["M"] * w["K"] * isz + w["K"] * w["N"] * isz + w["M"] * w["N"] * osz
+    if w["beta"] != 0.0:
+        b += w["M"] * w["N"] * osz
+    return b
+
+
+def panel_intensity(bm, bn, item_bytes):
+    """FLOP per byte of operand loads for a BM x BN output tile: 2*BM*BN/(s*(BM+BN))."""
+    return 2 * bm * bn / (item_bytes * (bm + bn))
+
+
+def roofline_bound(w, peak_tflops, hbm_gbs):
+    """'tensor' when the tensor-core roof is lower than HBM bandwidth x intensity."""
+    intensity = gemm_flops(w["M"], w["N"], w["K"]) / algorithmic_bytes(w)
+    return "tensor" if peak_tflops * 1e12 <= hbm_gbs * 1e9 * intensity else "hbm"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload_name):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on the
+    current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload_name)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = [s for s in sm if s > 0.5 * (max(mx) if mx else 1)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def upload(bits, fmt, device):
+    import torch
+    b = np.ascontiguousarray(bits)
+    if fmt == "f32":
+        return torch.from_numpy(b.view(np.int32).copy()).view(torch.float32).to(device)
+    dt = torch.float16 if fmt == "f16" else torch.bfloat16
+    return torch.from_numpy(b.view(np.int16).copy()).view(dt).to(device)
+
+
+def make_device_problem(cfg, device):
+    import torch
+    w = si.workload_operands(cfg)
+    a = upload(w["A"], w["in_dtype"], device)
+    b = upload(w["B"], w["in_dtype"], device)
+    odt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w["out_dtype"]]
+    if w["C"] is not None:
+        c0 = upload(w["C"], w["out_dtype"], device)
+    else:
+        c0 = None
+    c = torch.empty(w["M"], w["N"], dtype=odt, device=device)
+    return w, a, b, c, c0
+
+
+def time_gemm(g, w, a, b, c, c0, steps, warmup, stream, flush):
+    """Per-step CUDA-event times (ms) of the GEMM launch alone, L2 flushed before
+    each step outside the event pair.  C is reset from c0 before each step when
+    beta != 0 (outside the event pair) so every step computes the same result."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    st = torch.cuda.Stream(stream) if False else stream
+    with torch.cuda.stream(st):
+        for i in range(warmup + steps):
+            if c0 is not None:
+                c.copy_(c0)
+            flush.zero_()
+            if i >= warmup:
+                evs[i - warmup][0].record(st)
+            g.matmul(a, b, c, alpha=w["alpha"], beta=w["beta"], a_col=w["a_col"],
+                     b_col=w["b_col"], stream=st.cuda_stream)
+            if i >= warmup:
+                evs[i - warmup][1].record(st)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def time_e2e(g, w, steps, warmup, device):
+    """End-to-end through gemm_host: pinned host A, B (C when beta != 0) in,
+    device GEMM, host C out; CUDA events around the whole enqueued sequence."""
+    import torch
+    hA = torch.from_numpy(w["A"].view(np.int16).copy()).pin_memory()
+    hB = torch.from_numpy(w["B"].view(np.int16).copy()).pin_memory()
+    osz = 4 if w["out_dtype"] == "f32" else 2
+    cnp = np.zeros((w["M"], w["N"]), dtype=np.uint32 if osz == 4 else np.uint16)
+    if w["C"] is not None:
+        cnp[:] = w["C"]
+    hC = torch.from_numpy(cnp.view(np.int32 if osz == 4 else np.int16)).pin_memory()
+    dA = torch.empty(hA.numel(), dtype=torch.int16, device=device)
+    dB = torch.empty(hB.numel(), dtype=torch.int16, device=device)
+    dC = torch.empty(hC.numel() * osz // 2, dtype=torch.int16, device=device)
+    din = g.GEMM_F16 if w["in_dtype"] == "f16" else g.GEMM_BF16
+    dout = {"f32": g.GEMM_F32, "bf16": g.GEMM_BF16, "f16": g.GEMM_F16}[w["out_dtype"]]
+    layout = (g.GEMM_A_COL if w["a_col"] else 0) | (g.GEMM_B_COL if w["b_col"] else 0)
+    lda = w["A"].shape[1]
+    ldb = w["B"].shape[1]
+    st = torch.cuda.current_stream(device)
+    times = []
+    for i in range(warmup + steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        s = g.gemm_host(w["M"], w["N"], w["K"], w["alpha"], hA.data_ptr(), lda, hB.data_ptr(),
+                        ldb, w["beta"], hC.data_ptr(), w["N"], din, dout, layout,
+                        dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), st.cuda_stream)
+        if s != g.GEMM_OK:
+            raise g.GemmError(s, "gemm_host")
+        e1.record(st)
+        st.synchronize()
+        if i >= warmup:
+            times.append(e0.elapsed_time(e1))
+    h2d = w["A"].nbytes + w["B"].nbytes + (cnp.nbytes if w["beta"] != 0.0 else 0)
+    return times, h2d, cnp.nbytes
+
+
+def cpu_baseline(w, target_s=12.0):
+    """The oracle, as it stands, on the host cores over a bounded row sample."""
+    import oracle
+    t0 = time.perf_counter()
+    rows = list(range(min(8, w["M"])))
+    oracle.gemm(w["A"], w["B"], M=w["M"], N=w["N"], K=w["K"], in_dtype=w["in_dtype"],
+                out_dtype=w["out_dtype"], a_col=w["a_col"], b_col=w["b_col"], alpha=w["alpha"],
+                beta=w["beta"], C=w["C"], rows=rows)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    nrows = int(min(w["M"], max(8, len(rows) * target_s / dt)))
+    rows = list(range(nrows))
+    t0 = time.perf_counter()
+    oracle.gemm(w["A"], w["B"], M=w["M"], N=w["N"], K=w["K"], in_dtype=w["in_dtype"],
+                out_dtype=w["out_dtype"], a_col=w["a_col"], b_col=w["b_col"], alpha=w["alpha"],
+                beta=w["beta"], C=w["C"], rows=rows)
+    dt = time.perf_counter() - t0
+    flops = gemm_flops(nrows, w["N"], w["K"])
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"rows 0..{nrows - 1} of the {w['M']}x{w['N']}x{w['K']} problem "
+                      f"({flops / 1e9:.1f} GFLOP, {dt:.1f} s, binary64 accumulation)"}
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    import dense_tensor_core_tcgen05_gb300 as g
+    cfg = WORKLOAD_BY_NAME[args.workload]
+    peaks, peak_src = load_peaks()
+    torch.cuda.set_device(device)
+    w, a, b, c, c0 = make_device_problem(cfg, device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    st = torch.cuda.current_stream(device)
+    # correctness launch on a NaN-poisoned output before timing
+    c.fill_(float("nan"))
+    if c0 is not None:
+        c.copy_(c0)
+    g.matmul(a, b, c, alpha=w["alpha"], beta=w["beta"], a_col=w["a_col"], b_col=w["b_col"])
+    s, site = g.gemm_sync_status(st.cuda_stream)
+    if s != g.GEMM_OK or not bool(torch.isfinite(c).all()):
+        raise RuntimeError(f"correctness launch failed: status {s} site {site}")
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    t_wall0 = time.perf_counter()
+    times = time_gemm(g, w, a, b, c, c0, args.steps, args.warmup, st, flush)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop() if sampler else None
+
+    step_ms = sum(times) / len(times)
+    flops = gemm_flops(w["M"], w["N"], w["K"])
+    if world > 1:
+        tt = torch.tensor([step_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(tt.item())
+    value = world * flops / (step_ms * 1e-3) / 1e12
+
+    # roofline of the GEMM kernel (the only kernel of a step)
+    peak_t = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    bound = roofline_bound(w, peak_t, hbm)
+    kernel_ms = step_ms
+    if bound == "tensor":
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                "frac": achieved / peak_t}
+    else:
+        achieved = algorithmic_bytes(w) / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm}
+    roof["peak_source"] = f"{peak_src} ({'bf16_tflops burst' if bound == 'tensor' else 'hbm_gbs'})"
+    roof["traffic"] = load_traffic(w["name"])
+    roof["algorithmic_bytes"] = algorithmic_bytes(w)
+
+    out = {"metric": "GEMM TFLOP/s (2MNK/s) and % of dense FP16/BF16 tensor peak on 1 GB300",
+           "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": w["in_dtype"] + "->f32acc->" + w["out_dtype"],
+           "data": "synthetic (seeded splitmix64, see seeded_inputs)",
+           "config": {"workload": w["name"], "M": w["M"], "N": w["N"], "K": w["K"],
+                      "in_dtype": w["in_dtype"], "out_dtype": w["out_dtype"],
+                      "layout": ("A col" if w["a_col"] else "A row") + ", " +
+                                ("B col" if w["b_col"] else "B row"),
+                      "alpha": w["alpha"], "beta": w["beta"],
+                      "l2": "flushed between timed steps (512 MiB write, outside the events)",
+                      "parallelism": f"replicas x{world}"},
+           "median_ms": statistics.median(times), "min_ms": min(times),
+           "wall_s_timed_region": t_wall,
+           "roofline": roof, "clocks": clocks, "gpu_launches": args.steps * world}
+
+    if rank == 0:
+        # end-to-end through the host-buffer entry point
+        e2e_steps = max(3, min(args.steps, 10))
+        et, h2d, d2h = time_e2e(g, w, e2e_steps, 2, device)
+        e_ms = sum(et) / len(et)
+        out["e2e"] = {"value": flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "entry_point": "gemm_host (pinned host operands)"}
+        if not args.no_suite:
+            out["suite"] = run_suite(g, args, device, peaks, cfg)
+        if not args.no_cpu:
+            out["cpu_baseline"] = cpu_baseline(w)
+        out["kernel_hash"] = kernel_source_hash()
+    return out
+
+
+def run_suite(g, args, device, peaks, skip_cfg):
+    """The other workloads, timed the same way (20 steps, 5 warmups each)."""
+    import torch
+    res = {}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    for cfg in sorted(si.WORKLOADS):
+        if cfg == skip_cfg:
+            continue
+        w, a, b, c, c0 = make_device_problem(cfg, device)
+        times = time_gemm(g, w, a, b, c, c0, 20, 5, torch.cuda.current_stream(device), flush)
+        ms = statistics.median(times)
+        flops = gemm_flops(w["M"], w["N"], w["K"])
+        peak_t = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        bound = roofline_bound(w, peak_t, hbm)
+        tf = flops / (ms * 1e-3) / 1e12
+        gbs = algorithmic_bytes(w) / (ms * 1e-3) / 1e9
+        res[w["name"]] = {"median_ms": ms, "tflops": tf, "gbs_algorithmic": gbs, "bound": bound,
+                          "frac": tf / peak_t if bound == "tensor" else gbs / hbm}
+        del a, b, c, c0
+        torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The CPU oracle on the host cores: each step computes a bounded row sample
+    of the same workload (FP64 accumulation)."""
+    import oracle
+    cfg = WORKLOAD_BY_NAME[args.workload]
+    w = si.workload_operands(cfg)
+    rows_per_step = 32 if w["M"] >= 32 else w["M"]
+    run = lambda r0: oracle.gemm(w["A"], w["B"], M=w["M"], N=w["N"], K=w["K"],  # noqa: E731
+                                 in_dtype=w["in_dtype"], out_dtype=w["out_dtype"],
+                                 a_col=w["a_col"], b_col=w["b_col"], alpha=w["alpha"],
+                                 beta=w["beta"], C=w["C"],
+                                 rows=[(r0 + i) % w["M"] for i in range(rows_per_step)])
+    for i in range(args.warmup):
+        run(i * rows_per_step)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        run((args.warmup + i) * rows_per_step)
+        times.append(time.perf_counter() - t0)
+    step_s = sum(times) / len(times)
+    flops = gemm_flops(rows_per_step, w["N"], w["K"])
+    value = flops / step_s / 1e12
+    sample = (f"{rows_per_step} rows of the {w['M']}x{w['N']}x{w['K']} problem per step "
+              f"({flops / 1e9:.2f} GFLOP), binary64 accumulation")
+    return {"impl": "reference", "metric": "GEMM TFLOP/s (2MNK/s) and % of dense FP16/BF16 tensor peak on 1 GB300",
+            "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded splitmix64, see seeded_inputs)",
+            "config": {"workload": w["name"], "M": w["M"], "N": w["N"], "K": w["K"]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_BY_NAME))
+    ap.add_argument("--no-suite", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    from dense_tensor_core_tcgen05_gb300 import build as b
+    if rank == 0 or world == 1:
+        b.build()
+    if world > 1:
+        torch.distributed.barrier()
+    out = run_ours(args, rank, world, torch.device("cuda", local))
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

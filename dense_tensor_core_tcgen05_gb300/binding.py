@@ -1,0 +1,199 @@
+"""ctypes binding of libgemm_tcgen05.so (the C ABI of include/gemm_tcgen05.h).
+
+Argument marshalling only: every step of the GEMM runs in the library's CUDA
+kernels.  There is no fallback: if the shared library is missing, importing
+this module raises.  PyTorch is used (by ``matmul``) only to hand over device
+pointers and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgemm_tcgen05.so")
+
+GEMM_F16, GEMM_BF16, GEMM_F32 = 0, 1, 2
+GEMM_A_ROW, GEMM_A_COL, GEMM_B_ROW, GEMM_B_COL = 0, 1, 0, 2
+GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ARCH, GEMM_ERR_CUDA, \
+    GEMM_ERR_TIMEOUT = range(6)
+
+# Symbols declared in include/gemm_tcgen05.h.
+EXPORTS = ("gemm", "gemm_ex", "gemm_host", "gemm_status_string", "gemm_sync_status",
+           "gemm_debug_set", "gemm_plan", "gemm_tile_coord", "gemm_encode_idesc",
+           "gemm_encode_sdesc", "gemm_version")
+
+
+class gemm_config_t(ctypes.Structure):
+    _fields_ = [("bn", ctypes.c_int32), ("group_m", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class gemm_plan_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "bm", "bn", "bk", "stages", "m_tiles", "n_tiles", "k_blocks", "num_tiles",
+        "grid", "group_m", "threads", "smem_bytes", "tmem_cols", "a_mn", "b_mn",
+        "epi_chunk_cols")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built: run dense_tensor_core_tcgen05_gb300.build.build() "
+                          "(the GEMM has no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64, f32, vp, ci, i32 = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_int32
+    gemm_args = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ci, ci, ci, vp]
+    lib.gemm.argtypes = gemm_args
+    lib.gemm.restype = ci
+    lib.gemm_ex.argtypes = gemm_args + [ctypes.POINTER(gemm_config_t)]
+    lib.gemm_ex.restype = ci
+    lib.gemm_host.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ci, ci, ci,
+                              vp, vp, vp, vp]
+    lib.gemm_host.restype = ci
+    lib.gemm_status_string.argtypes = [ci]
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_sync_status.argtypes = [vp, ctypes.POINTER(ci)]
+    lib.gemm_sync_status.restype = ci
+    lib.gemm_debug_set.argtypes = [ctypes.c_uint64, i32]
+    lib.gemm_debug_set.restype = None
+    lib.gemm_plan.argtypes = [i64, i64, i64, ci, ci, ci, i32, ctypes.POINTER(gemm_config_t),
+                              ctypes.POINTER(gemm_plan_t)]
+    lib.gemm_plan.restype = ci
+    lib.gemm_tile_coord.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.gemm_tile_coord.restype = None
+    lib.gemm_encode_idesc.argtypes = [ci, ci, ci, ci, ci]
+    lib.gemm_encode_idesc.restype = ctypes.c_uint32
+    lib.gemm_encode_sdesc.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
+    lib.gemm_encode_sdesc.restype = ctypes.c_uint64
+    lib.gemm_version.argtypes = []
+    lib.gemm_version.restype = i32
+    return lib
+
+
+_lib = _load()
+
+
+def library():
+    """The loaded ctypes.CDLL."""
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.gemm_status_string(int(status)).decode()
+
+
+def _cfg(cfg):
+    if cfg is None:
+        return None
+    if isinstance(cfg, gemm_config_t):
+        return ctypes.byref(cfg)
+    return ctypes.byref(gemm_config_t(int(cfg.get("bn", 0)), int(cfg.get("group_m", 0)),
+                                      int(cfg.get("grid", 0)), 0))
+
+
+def gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout, stream):
+    """Raw C-ABI call; pointers and stream as integers.  Returns the status code."""
+    return _lib.gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
+                     stream)
+
+
+def gemm_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout, stream,
+            cfg=None):
+    return _lib.gemm_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
+                        stream, _cfg(cfg))
+
+
+def gemm_host(M, N, K, alpha, hA, lda, hB, ldb, beta, hC, ldc, in_dtype, out_dtype, layout,
+              dA, dB, dC, stream):
+    return _lib.gemm_host(M, N, K, alpha, hA, lda, hB, ldb, beta, hC, ldc, in_dtype, out_dtype,
+                          layout, dA, dB, dC, stream)
+
+
+def gemm_sync_status(stream=0):
+    site = ctypes.c_int(0)
+    s = _lib.gemm_sync_status(stream, ctypes.byref(site))
+    return s, site.value
+
+
+def gemm_debug_set(wait_timeout_ns=0, inject_skip=0):
+    _lib.gemm_debug_set(int(wait_timeout_ns), int(inject_skip))
+
+
+def gemm_plan(M, N, K, in_dtype, out_dtype, layout, num_sms, cfg=None):
+    p = gemm_plan_t()
+    s = _lib.gemm_plan(M, N, K, in_dtype, out_dtype, layout, num_sms, _cfg(cfg), ctypes.byref(p))
+    return s, p
+
+
+def gemm_tile_coord(t, m_tiles, n_tiles, group_m):
+    m, n = ctypes.c_int32(0), ctypes.c_int32(0)
+    _lib.gemm_tile_coord(t, m_tiles, n_tiles, group_m, ctypes.byref(m), ctypes.byref(n))
+    return m.value, n.value
+
+
+def gemm_encode_idesc(in_dtype, a_mn, b_mn, m, n):
+    return _lib.gemm_encode_idesc(in_dtype, a_mn, b_mn, m, n)
+
+
+def gemm_encode_sdesc(addr, lbo, sbo):
+    return _lib.gemm_encode_sdesc(addr, lbo, sbo)
+
+
+def gemm_version():
+    return _lib.gemm_version()
+
+
+# ------------------------------------------------------------ torch helpers
+
+def _torch_dtype_code(dt):
+    import torch
+    if dt == torch.float16:
+        return GEMM_F16
+    if dt == torch.bfloat16:
+        return GEMM_BF16
+    if dt == torch.float32:
+        return GEMM_F32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _ld(t):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("operands must be 2-D with unit stride along the last dimension")
+    return t.stride(0) if t.size(0) > 1 else max(t.stride(0), t.size(1))
+
+
+def matmul(a, b, c, alpha=1.0, beta=0.0, a_col=False, b_col=False, stream=None, cfg=None):
+    """C <- alpha * A * B + beta * C on CUDA tensors (in place in ``c``).
+
+    ``a`` is the stored A: [M, K] (a_col False) or [K, M] (a_col True, i.e. A
+    column-major).  ``b`` is the stored B: [K, N] or [N, K] (b_col True).
+    ``c`` is [M, N] with unit column stride; its dtype is the output format.
+    Runs on ``stream`` (default: torch's current stream).  Raises GemmError.
+    """
+    import torch
+    if not (a.is_cuda and b.is_cuda and c.is_cuda):
+        raise ValueError("a, b and c must be CUDA tensors (there is no CPU path)")
+    if a.dtype != b.dtype:
+        raise TypeError("A and B must share a dtype")
+    M, K = (a.shape[1], a.shape[0]) if a_col else (a.shape[0], a.shape[1])
+    N, Kb = (b.shape[0], b.shape[1]) if b_col else (b.shape[1], b.shape[0])
+    if Kb != K or tuple(c.shape) != (M, N):
+        raise ValueError(f"shape mismatch: A {tuple(a.shape)}, B {tuple(b.shape)}, C {tuple(c.shape)}")
+    if stream is None:
+        stream = torch.cuda.current_stream(c.device).cuda_stream
+    layout = (GEMM_A_COL if a_col else 0) | (GEMM_B_COL if b_col else 0)
+    s = gemm_ex(M, N, K, float(alpha), a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), float(beta),
+                c.data_ptr(), _ld(c), _torch_dtype_code(a.dtype), _torch_dtype_code(c.dtype),
+                layout, int(stream), cfg)
+    if s != GEMM_OK:
+        raise GemmError(s, "gemm")
+    return c

@@ -1,0 +1,398 @@
+// Host side of the C ABI declared in include/gemm_tcgen05.h: argument checks,
+// launch planning, TMA tensor-map encoding and kernel launch.
+//
+// The tensor map is the host-built copy descriptor of the lecture "The
+// Asynchronous Kernel: Tensor Cores & TMA" (linearly.space), section "One thread
+// orders the groceries": element type, base pointer, matrix shape, row pitch,
+// tile shape and the 128B swizzle the tile gets on arrival ("The XOR that unties
+// the banks").  cuTensorMapEncodeTiled is reached through the runtime's driver
+// entry-point query, so the library does not link libcuda.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_common.h"
+#include "gemm_kernel.cuh"
+#include "gemm_launch.h"
+#include "gemm_tcgen05.h"
+
+using namespace gemm_tc;
+
+// Wait-timeout status word of every GEMM kernel launched on a device.
+__device__ int g_gemm_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+
+struct DeviceInfo {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  int cc_major = 0, cc_minor = 0, num_sms = 0;
+  int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+std::atomic<uint64_t> g_timeout_ns{0};
+std::atomic<int32_t> g_inject_skip{0};
+
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+const DeviceInfo* device_info(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceInfo& d = g_dev[dev];
+  std::call_once(d.once, [&d, dev]() {
+    cudaDeviceProp p;
+    d.err = cudaGetDeviceProperties(&p, dev);
+    if (d.err != cudaSuccess) return;
+    d.cc_major = p.major;
+    d.cc_minor = p.minor;
+    d.num_sms = p.multiProcessorCount;
+    d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_gemm_status_word);
+  });
+  return &d;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+int out_size(int out_dtype) { return out_dtype == GEMM_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks on sizes, formats and layout only (no pointers): shared by gemm() and
+// gemm_plan().  *quick is set when M == 0 or N == 0 (nothing to do).
+gemm_status_t check_shape(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int layout,
+                          bool* quick) {
+  *quick = false;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (layout & ~(GEMM_A_COL | GEMM_B_COL)) return GEMM_ERR_INVALID_ARG;
+  if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16) return GEMM_ERR_UNSUPPORTED;
+  if (out_dtype != GEMM_F32 && out_dtype != GEMM_BF16 && out_dtype != GEMM_F16)
+    return GEMM_ERR_UNSUPPORTED;
+  // tile indices and TMA coordinates are 32-bit signed on the device
+  if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+    return GEMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) *quick = true;
+  return GEMM_OK;
+}
+
+// Full argument check of gemm(); pointers may be device or host (gemm_host).
+gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, const void* C, int64_t ldc, int in_dtype,
+                         int out_dtype, int layout, bool* quick) {
+  gemm_status_t s = check_shape(M, N, K, in_dtype, out_dtype, layout, quick);
+  if (s != GEMM_OK || *quick) return s;
+  const bool a_col = (layout & GEMM_A_COL) != 0, b_col = (layout & GEMM_B_COL) != 0;
+  if (ldc < N) return GEMM_ERR_INVALID_ARG;
+  if (C == nullptr) return GEMM_ERR_INVALID_ARG;
+  const int osz = out_size(out_dtype);
+  // byte extents must fit comfortably in 63 bits and TMA strides below 2^40 bytes
+  if (ldc > (int64_t(1) << 36) || M > (int64_t(1) << 62) / (ldc * osz + 1))
+    return GEMM_ERR_INVALID_ARG;
+  if (!aligned16(C) || (ldc * osz) % 16 != 0) return GEMM_ERR_UNSUPPORTED;
+  if (K > 0) {
+    const int64_t lda_min = a_col ? M : K, ldb_min = b_col ? K : N;
+    if (lda < lda_min || ldb < ldb_min) return GEMM_ERR_INVALID_ARG;
+    if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (lda > (int64_t(1) << 36) || ldb > (int64_t(1) << 36)) return GEMM_ERR_INVALID_ARG;
+    const int64_t a_rows = a_col ? K : M, b_rows = b_col ? N : K;
+    if (a_rows > (int64_t(1) << 62) / (lda * 2 + 1) || b_rows > (int64_t(1) << 62) / (ldb * 2 + 1))
+      return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0)
+      return GEMM_ERR_UNSUPPORTED;
+  }
+  return GEMM_OK;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Tile-width choice: the width whose wave-quantised cost, waves * (bn + 64), is
+// lowest (a wave = one tile per SM; "+64" stands for the per-k-block A traffic
+// every tile pays whatever its width).  Ties go to the wider tile.
+int choose_bn(int64_t M, int64_t N, int num_sms) {
+  const int widths[3] = {256, 128, 64};
+  int best = 256;
+  int64_t best_cost = -1;
+  for (int w : widths) {
+    const int64_t tiles = ceil_div(M, BM) * ceil_div(N, w);
+    const int64_t waves = ceil_div(tiles, num_sms);
+    const int64_t cost = waves * (w + 64);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = w;
+    }
+  }
+  return best;
+}
+
+gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layout, int num_sms,
+                        const gemm_config_t* cfg, gemm_plan_t* p) {
+  if (num_sms <= 0) return GEMM_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  int bn = (cfg && cfg->bn) ? cfg->bn : choose_bn(M, N, num_sms);
+  if (bn != 64 && bn != 128 && bn != 256) return GEMM_ERR_INVALID_ARG;
+  p->bm = BM;
+  p->bn = bn;
+  p->bk = BK;
+  p->stages = stages_for_bn(bn);
+  const int64_t mt = ceil_div(M, BM), nt = ceil_div(N, bn), kb = ceil_div(K, BK);
+  if (mt * nt >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
+  p->m_tiles = static_cast<int32_t>(mt);
+  p->n_tiles = static_cast<int32_t>(nt);
+  p->k_blocks = static_cast<int32_t>(kb);
+  p->num_tiles = static_cast<int32_t>(mt * nt);
+  int gm = (cfg && cfg->group_m) ? cfg->group_m : (bn == 256 ? 16 : 8);
+  if (gm < 0) return GEMM_ERR_INVALID_ARG;
+  if (gm > p->m_tiles) gm = p->m_tiles > 0 ? p->m_tiles : 1;
+  p->group_m = gm;
+  int grid = (cfg && cfg->grid) ? cfg->grid : num_sms;
+  if (grid < 0) return GEMM_ERR_INVALID_ARG;
+  if (grid > p->num_tiles) grid = p->num_tiles;
+  p->grid = grid;
+  p->threads = NUM_THREADS;
+  p->smem_bytes = smem_alloc_bytes(bn);
+  p->tmem_cols = 2 * bn;
+  p->a_mn = (layout & GEMM_A_COL) ? 1 : 0;
+  p->b_mn = (layout & GEMM_B_COL) ? 0 : 1;
+  p->epi_chunk_cols = out_dtype == GEMM_F32 ? 32 : 64;
+  return GEMM_OK;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+CUtensorMapDataType tma_dtype(int dt) {
+  switch (dt) {
+    case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  }
+}
+
+template <int OUT>
+gemm_status_t launch_scale(void* C, int64_t ldc, int64_t M, int64_t N, float beta, int num_sms,
+                           cudaStream_t stream) {
+  const int64_t total = M * N;
+  int64_t blocks = ceil_div(total, 256);
+  if (blocks > int64_t(num_sms) * 8) blocks = int64_t(num_sms) * 8;
+  scale_c_kernel<OUT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      C, ldc, static_cast<int>(M), static_cast<int>(N), beta);
+  return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                       const void* B, int64_t ldb, float beta, void* C, int64_t ldc, int in_dtype,
+                       int out_dtype, int layout, void* stream_v, const gemm_config_t* cfg) {
+  bool quick = false;
+  gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, layout, &quick);
+  if (s != GEMM_OK || quick) return s;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+  const DeviceInfo* di = device_info(dev);
+  if (!di || di->err != cudaSuccess) return GEMM_ERR_CUDA;
+  if (di->cc_major != 10 || di->cc_minor != 3) return GEMM_ERR_ARCH;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+
+  if (K == 0) {
+    switch (out_dtype) {
+      case GEMM_F32: return launch_scale<OUT_F32>(C, ldc, M, N, beta, di->num_sms, stream);
+      case GEMM_BF16: return launch_scale<OUT_BF16>(C, ldc, M, N, beta, di->num_sms, stream);
+      default: return launch_scale<OUT_F16>(C, ldc, M, N, beta, di->num_sms, stream);
+    }
+  }
+
+  gemm_plan_t p;
+  s = make_plan(M, N, K, out_dtype, layout, di->num_sms, cfg, &p);
+  if (s != GEMM_OK) return s;
+
+  CUtensorMap ta, tb, tc;
+  const bool a_col = (layout & GEMM_A_COL) != 0, b_col = (layout & GEMM_B_COL) != 0;
+  const CUtensorMapDataType din = tma_dtype(in_dtype);
+  bool ok = a_col ? encode_2d(&ta, din, A, M, K, lda * 2, ATOM_MN, BK)
+                  : encode_2d(&ta, din, A, K, M, lda * 2, BK, BM);
+  ok = ok && (b_col ? encode_2d(&tb, din, B, K, N, ldb * 2, BK, p.bn)
+                    : encode_2d(&tb, din, B, N, K, ldb * 2, ATOM_MN, BK));
+  ok = ok && encode_2d(&tc, tma_dtype(out_dtype), C, N, M, ldc * out_size(out_dtype),
+                       p.epi_chunk_cols, EPI_ROWS);
+  if (!ok) return GEMM_ERR_CUDA;
+
+  KernelArgs ka;
+  std::memset(&ka, 0, sizeof(ka));
+  ka.M = static_cast<int>(M);
+  ka.N = static_cast<int>(N);
+  ka.K = static_cast<int>(K);
+  ka.m_tiles = p.m_tiles;
+  ka.n_tiles = p.n_tiles;
+  ka.k_blocks = p.k_blocks;
+  ka.num_tiles = p.num_tiles;
+  ka.group_m = p.group_m;
+  ka.alpha = alpha;
+  ka.beta = beta;
+  ka.idesc = make_idesc_f16(in_dtype == GEMM_BF16 ? 1 : 0, p.a_mn, p.b_mn, BM, p.bn);
+  ka.a_mn = p.a_mn;
+  ka.b_mn = p.b_mn;
+  ka.read_c = beta != 0.0f ? 1 : 0;
+  ka.status = di->status;
+  const uint64_t tmo = g_timeout_ns.load(std::memory_order_relaxed);
+  ka.timeout_ns = tmo ? tmo : kDefaultTimeoutNs;
+  ka.inject_skip = g_inject_skip.load(std::memory_order_relaxed);
+
+  cudaError_t e;
+  switch (out_dtype) {
+    case GEMM_F32: e = launch_gemm_f32(p.bn, ta, tb, tc, ka, p.grid, stream, dev); break;
+    case GEMM_BF16: e = launch_gemm_bf16(p.bn, ta, tb, tc, ka, p.grid, stream, dev); break;
+    default: e = launch_gemm_f16(p.bn, ta, tb, tc, ka, p.grid, stream, dev); break;
+  }
+  return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace gemm_tc {
+int smem_alloc_bytes(int bn) {
+  switch (bn) {
+    case 64: return SmemLayout<64, stages_for_bn(64)>::ALLOC;
+    case 128: return SmemLayout<128, stages_for_bn(128)>::ALLOC;
+    case 256: return SmemLayout<256, stages_for_bn(256)>::ALLOC;
+    default: return 0;
+  }
+}
+}  // namespace gemm_tc
+
+extern "C" {
+
+gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                   const void* B, int64_t ldb, float beta, void* C, int64_t ldc, int in_dtype,
+                   int out_dtype, int layout, void* stream) {
+  return run_gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
+                  stream, nullptr);
+}
+
+gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, float beta, void* C, int64_t ldc, int in_dtype,
+                      int out_dtype, int layout, void* stream, const gemm_config_t* cfg) {
+  return run_gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
+                  stream, cfg);
+}
+
+gemm_status_t gemm_host(int64_t M, int64_t N, int64_t K, float alpha, const void* hA, int64_t lda,
+                        const void* hB, int64_t ldb, float beta, void* hC, int64_t ldc,
+                        int in_dtype, int out_dtype, int layout, void* dA, void* dB, void* dC,
+                        void* stream_v) {
+  bool quick = false;
+  gemm_status_t s =
+      check_args(M, N, K, hA, lda, hB, ldb, hC, ldc, in_dtype, out_dtype, layout, &quick);
+  if (s != GEMM_OK || quick) return s;
+  s = check_args(M, N, K, dA, lda, dB, ldb, dC, ldc, in_dtype, out_dtype, layout, &quick);
+  if (s != GEMM_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+  const bool a_col = (layout & GEMM_A_COL) != 0, b_col = (layout & GEMM_B_COL) != 0;
+  const size_t osz = static_cast<size_t>(out_size(out_dtype));
+  if (K > 0) {
+    const int64_t a_rows = a_col ? K : M, a_cols = a_col ? M : K;
+    const int64_t b_rows = b_col ? N : K, b_cols = b_col ? K : N;
+    if (cudaMemcpy2DAsync(dA, lda * 2, hA, lda * 2, a_cols * 2, a_rows, cudaMemcpyHostToDevice,
+                          st) != cudaSuccess ||
+        cudaMemcpy2DAsync(dB, ldb * 2, hB, ldb * 2, b_cols * 2, b_rows, cudaMemcpyHostToDevice,
+                          st) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+  }
+  if (beta != 0.0f &&
+      cudaMemcpy2DAsync(dC, ldc * osz, hC, ldc * osz, N * osz, M, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess)
+    return GEMM_ERR_CUDA;
+  s = run_gemm(M, N, K, alpha, dA, lda, dB, ldb, beta, dC, ldc, in_dtype, out_dtype, layout,
+               stream_v, nullptr);
+  if (s != GEMM_OK) return s;
+  if (cudaMemcpy2DAsync(hC, ldc * osz, dC, ldc * osz, N * osz, M, cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return GEMM_ERR_CUDA;
+  return GEMM_OK;
+}
+
+const char* gemm_status_string(gemm_status_t status) {
+  switch (status) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported argument (dtype, alignment or stride)";
+    case GEMM_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
+    case GEMM_ERR_CUDA: return "CUDA runtime or driver error";
+    case GEMM_ERR_TIMEOUT: return "a kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+gemm_status_t gemm_sync_status(void* stream, int* site) {
+  if (site) *site = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GEMM_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gemm_status_word, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (v == 0) return GEMM_OK;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_gemm_status_word, &zero, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (site) *site = v;
+  return GEMM_ERR_TIMEOUT;
+}
+
+void gemm_debug_set(uint64_t wait_timeout_ns, int32_t inject_skip) {
+  g_timeout_ns.store(wait_timeout_ns, std::memory_order_relaxed);
+  g_inject_skip.store(inject_skip > 0 ? inject_skip : 0, std::memory_order_relaxed);
+}
+
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int layout,
+                        int32_t num_sms, const gemm_config_t* cfg, gemm_plan_t* plan) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  bool quick = false;
+  gemm_status_t s = check_shape(M, N, K, in_dtype, out_dtype, layout, &quick);
+  if (s != GEMM_OK) return s;
+  return make_plan(M, N, K, out_dtype, layout, num_sms, cfg, plan);
+}
+
+void gemm_tile_coord(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_m, int32_t* m_blk,
+                     int32_t* n_blk) {
+  int m = 0, n = 0;
+  tile_coord(t, m_tiles, n_tiles, group_m, &m, &n);
+  *m_blk = m;
+  *n_blk = n;
+}
+
+uint32_t gemm_encode_idesc(int in_dtype, int a_mn, int b_mn, int m, int n) {
+  return make_idesc_f16(in_dtype == GEMM_BF16 ? 1 : 0, a_mn, b_mn, m, n);
+}
+
+uint64_t gemm_encode_sdesc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return make_sdesc_sw128(smem_addr, lbo_bytes, sbo_bytes);
+}
+
+int32_t gemm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// Pieces shared by the host planner and the device kernel: tile geometry, the
+// grouped tile order, and the tcgen05 descriptor encoders.  Plain integer code,
+// callable on both sides (host tests exercise it without a GPU).
+#pragma once
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define GEMM_HD __host__ __device__ __forceinline__
+#else
+#define GEMM_HD inline
+#endif
+
+namespace gemm_tc {
+
+constexpr int BM = 128;      // output rows per CTA tile = MMA M: one TMEM lane per row
+constexpr int BK = 64;       // K per pipeline stage: 64 x 16-bit = one 128-byte swizzle row
+constexpr int UMMA_K = 16;   // K of one tcgen05.mma of kind::f16
+constexpr int SW = 128;      // swizzle width in bytes (TMA and MMA agree on the 128B pattern)
+constexpr int ATOM_MN = 64;  // 16-bit elements across one swizzle row (MN-major operands)
+
+// ---------------------------------------------------------------- tile order
+//
+// Grouped ("walk a few rows of the tile grid at a time") order from the lecture
+// "The Asynchronous Kernel: Tensor Cores & TMA" (linearly.space), section
+// "Scheduling is geometry", and the Ada GEMM page's CTA-rasterisation table
+// (kd.iw.mk): tiles are taken group_m tile-rows at a time, column by column
+// inside the group, so the tiles in flight share few A and B panels in L2.
+GEMM_HD void tile_coord(int t, int m_tiles, int n_tiles, int group_m, int* m_blk, int* n_blk) {
+  const int group_size = group_m * n_tiles;
+  const int g = t / group_size;
+  const int first_m = g * group_m;
+  const int rows_in_group = (m_tiles - first_m) < group_m ? (m_tiles - first_m) : group_m;
+  const int r = t - g * group_size;
+  *m_blk = first_m + r % rows_in_group;
+  *n_blk = r / rows_in_group;
+}
+
+// -------------------------------------------------------- tcgen05 descriptors
+//
+// Instruction descriptor of tcgen05.mma kind::f16 (32 bits, public PTX ISA):
+//   [4,6) D format (1 = f32)   [7,10) A format   [10,13) B format (0 = f16, 1 = bf16)
+//   [15] A major   [16] B major (0 = K-major, 1 = MN-major)
+//   [17,23) N >> 3   [24,29) M >> 4     (everything else 0: dense, no negate)
+GEMM_HD uint32_t make_idesc_f16(int in_is_bf16, int a_mn, int b_mn, int m, int n) {
+  return (1u << 4) | ((uint32_t)in_is_bf16 << 7) | ((uint32_t)in_is_bf16 << 10) |
+         ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor (64 bits, public PTX ISA):
+//   [0,14) start address >> 4   [16,30) leading byte offset >> 4
+//   [32,46) stride byte offset >> 4   [46,48) = 1 (descriptor version)
+//   [49,52) base offset (0: atoms are 1024-byte aligned)   [61,64) swizzle (2 = 128B)
+//
+// Canonical 128B-swizzled layouts (units: 16-bit elements):
+//  * K-major: rows of 64 K-elements (128 B), 8-row core groups 1024 B apart
+//    -> SBO = 1024, LBO unused (encoded 1).  Advancing K by 16 inside the row
+//    adds 32 bytes to the start address (the swizzle is applied on address bits).
+//  * MN-major: 64 MN-elements per 128-byte row, one row per K index, 8-row core
+//    groups 1024 B apart along K (SBO) and 64-element MN atoms LBO bytes apart.
+GEMM_HD uint64_t make_sdesc_sw128(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Kernel arguments (plain data, built on the host).
+struct KernelArgs {
+  int M, N, K;
+  int m_tiles, n_tiles, k_blocks, num_tiles, group_m;
+  float alpha, beta;
+  uint32_t idesc;        // tcgen05 instruction descriptor (formats, majors, M, N)
+  int a_mn, b_mn;        // 1: operand is MN-major in memory (A column-major / B row-major)
+  int read_c;            // beta != 0
+  int* status;           // device status word (0 = ok)
+  unsigned long long timeout_ns;
+  int inject_skip;       // debug: the producer leaves ring iteration (inject_skip - 1) unarmed
+};
+
+}  // namespace gemm_tc

@@ -1,0 +1,462 @@
+// Persistent tcgen05 GEMM kernel for sm_103a:  C <- alpha * A * B + beta * C.
+//
+// One CTA per SM, 6 warps with fixed roles ("warp specialisation", the
+// producer/consumer split of the lecture "The Asynchronous Kernel: Tensor Cores &
+// TMA", section "The factory"), re-expressed for the fifth-generation tensor core:
+//
+//   warp 0, one lane   TMA producer: for every k-block of every tile it waits for
+//                      a free ring slot (empty[s]), arms full[s] with the slot's
+//                      byte count and issues the A and B tile copies.
+//   warp 1             allocates Tensor Memory; one lane issues tcgen05.mma
+//                      (4 per k-block, K = 16 each) into one of two TMEM
+//                      accumulators and releases each slot with tcgen05.commit,
+//                      i.e. only after the MMAs reading it have *completed*
+//                      (the leetllm page's "releasing a stage at instruction
+//                      issue is unsafe").
+//   warps 2..5         epilogue: TMEM -> registers (tcgen05.ld, each warp its
+//                      own 32-lane quarter) -> alpha*acc + beta*C in fp32 ->
+//                      output cast -> 128B-swizzled shared memory -> TMA store.
+//                      The accumulator is handed back right after the last
+//                      TMEM read, so the epilogue of tile i overlaps the
+//                      mainloop of tile i+1 (the "ping-pong" of the lecture).
+//
+// Every wait is bounded (nanosecond timer); on expiry the waiter records an
+// error code in the status word, raises a CTA-wide abort flag, the roles drain
+// their own asynchronous work, TMEM is freed and the kernel returns.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "gemm_common.h"
+#include "ptx.cuh"
+
+namespace gemm_tc {
+
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARP0 = 2;
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_ROWS = 32;     // rows per epilogue warp = its TMEM lane quarter
+constexpr int EPI_BUFS = 2;      // staging buffers per epilogue warp
+
+enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_F16 = 2 };
+
+// Where a bounded wait gave up (written to the status word, first error wins).
+enum WaitSite {
+  SITE_PRODUCER_EMPTY = 1,
+  SITE_MMA_TMEM_EMPTY = 2,
+  SITE_MMA_FULL = 3,
+  SITE_EPI_TMEM_FULL = 4,
+  SITE_EPI_C_LOAD = 5,
+  SITE_DRAIN = 6,
+};
+
+template <int BN, int STAGES>
+struct SmemLayout {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int EPI_BUF_BYTES = EPI_ROWS * SW;
+  static constexpr int off_a = 0;
+  static constexpr int off_b = STAGES * A_BYTES;
+  static constexpr int off_epi = off_b + STAGES * B_BYTES;
+  static constexpr int off_bar = off_epi + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
+  // full[STAGES], empty[STAGES], tfull[2], tempty[2], cload[EPI_WARPS*EPI_BUFS], drain
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 1;
+  static constexpr int off_tmem = off_bar + NUM_BARS * 8;
+  static constexpr int off_flag = off_tmem + 8;
+  static constexpr int BYTES = off_flag + 8;
+  static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
+  static constexpr int TMEM_COLS = 2 * BN;    // two fp32 accumulators of BN columns
+  static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                "TMEM allocation must be a power of two in [32, 512]");
+  static_assert(ALLOC <= 232448, "exceeds the 227 KB per-block shared memory limit");
+};
+
+__device__ __forceinline__ void record_error(int* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+// Bounded wait by one thread.  Returns false on timeout or when another role
+// has raised the abort flag.
+__device__ __forceinline__ bool wait_one(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         const KernelArgs& a, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > a.timeout_ns) {
+        record_error(a.status, site);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait by a whole warp, with a warp-uniform result: it succeeds once
+// every lane has observed the phase (a phase cannot advance again before this
+// warp acts on it), and lane 0 alone decides to give up.
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          const KernelArgs& a, int site) {
+  const int lane = threadIdx.x & 31;
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    const bool done = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    if ((i & 15) == 15) {
+      int give_up = 0;
+      if (lane == 0) {
+        const uint64_t now = globaltimer_ns();
+        if (t0 == 0) t0 = now;
+        if (*abort_flag) {
+          give_up = 1;
+        } else if (now - t0 > a.timeout_ns) {
+          record_error(a.status, site);
+          *abort_flag = 1;
+          give_up = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+    }
+  }
+}
+
+// Wait used only while draining after an abort: ignores the abort flag.
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity, const KernelArgs& a) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > a.timeout_ns) {
+      record_error(a.status, SITE_DRAIN);
+      return;
+    }
+  }
+}
+
+template <int OUT>
+struct OutTraits;
+template <>
+struct OutTraits<OUT_F32> {
+  static constexpr int CHUNK_COLS = 32;  // 32 x 4 B = one 128-byte row per chunk
+};
+template <>
+struct OutTraits<OUT_BF16> {
+  static constexpr int CHUNK_COLS = 64;  // 64 x 2 B
+};
+template <>
+struct OutTraits<OUT_F16> {
+  static constexpr int CHUNK_COLS = 64;
+};
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int out_kind) {
+  if (out_kind == OUT_BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack2(uint32_t w, int out_kind) {
+  if (out_kind == OUT_BF16) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
+    return __bfloat1622float2(h);
+  }
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  return __half22float2(h);
+}
+
+template <int BN, int STAGES, int OUT>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const KernelArgs args) {
+  using L = SmemLayout<BN, STAGES>;
+  constexpr int CHUNK = OutTraits<OUT>::CHUNK_COLS;
+  constexpr int CHUNKS = BN / CHUNK;
+  static_assert(BN % CHUNK == 0, "tile width must be a whole number of epilogue chunks");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N in [16,256], N%16==0");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* cload = tempty + 2;
+  uint64_t* drain = cload + EPI_WARPS * EPI_BUFS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_tmem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_flag);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint32_t producer_iters = 0;  // ring iterations armed (producer thread only)
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], EPI_WARPS);
+    }
+    for (int i = 0; i < EPI_WARPS * EPI_BUFS; ++i) mbar_init(&cload[i], 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coord(t, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
+        for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!wait_one(&empty[s], ph ^ 1, abort_flag, args, SITE_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          if (args.inject_skip != 0 && it + 1 == static_cast<uint32_t>(args.inject_skip)) continue;
+          mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
+          uint8_t* sa = smem + L::off_a + s * L::A_BYTES;
+          uint8_t* sb = smem + L::off_b + s * L::B_BYTES;
+          const int k0 = kb * BK;
+          if (!args.a_mn) {
+            tma_load_2d(sa, &tmA, k0, mb * BM, &full[s]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / ATOM_MN; ++j)
+              tma_load_2d(sa + j * (BK * SW), &tmA, mb * BM + j * ATOM_MN, k0, &full[s]);
+          }
+          if (!args.b_mn) {
+            tma_load_2d(sb, &tmB, k0, nb * BN, &full[s]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / ATOM_MN; ++j)
+              tma_load_2d(sb + j * (BK * SW), &tmB, nb * BN + j * ATOM_MN, k0, &full[s]);
+          }
+        }
+      }
+      producer_iters = it;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------ MMA issuer
+      uint32_t it = 0, tl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x, ++tl) {
+        const int buf = tl & 1;
+        const uint32_t aph = (tl >> 1) & 1;
+        if (!wait_one(&tempty[buf], aph ^ 1, abort_flag, args, SITE_MMA_TMEM_EMPTY)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!wait_one(&full[s], ph, abort_flag, args, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + L::off_a + s * L::A_BYTES);
+          const uint32_t sb = smem_u32(smem + L::off_b + s * L::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // K-major: +32 B per K16 step inside the swizzled row.
+            // MN-major: +16 rows of 128 B per K16 step; MN atoms are BK*128 B apart.
+            const uint64_t da = args.a_mn ? make_sdesc_sw128(sa + kk * (UMMA_K * SW), BK * SW, 8 * SW)
+                                          : make_sdesc_sw128(sa + kk * (UMMA_K * 2), 16, 8 * SW);
+            const uint64_t db = args.b_mn ? make_sdesc_sw128(sb + kk * (UMMA_K * SW), BK * SW, 8 * SW)
+                                          : make_sdesc_sw128(sb + kk * (UMMA_K * 2), 16, 8 * SW);
+            umma_f16(d_tmem, da, db, args.idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        umma_commit(&tfull[buf]);
+      }
+    }
+  } else {
+    // -------------------------------------------------------- epilogue
+    const int ew = warp - EPI_WARP0;     // 0..3
+    const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
+    uint8_t* stage0 = smem + L::off_epi + ew * EPI_BUFS * L::EPI_BUF_BYTES;
+    uint32_t tl = 0, chunk_ctr = 0;
+    int pending_cload = -1;              // staging buffer with a C load in flight (abort drain)
+    uint32_t pending_phase = 0;
+    bool ok = true;
+    const int r = lane;                  // this thread's row inside the warp's 32-row block
+    for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x, ++tl) {
+      int mb, nb;
+      tile_coord(t, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
+      const int buf = tl & 1;
+      const uint32_t aph = (tl >> 1) & 1;
+      if (!wait_warp(&tfull[buf], aph, abort_flag, args, SITE_EPI_TMEM_FULL)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(buf * BN);
+      const int row0 = mb * BM + quarter * 32;
+#pragma unroll 1
+      for (int c = 0; c < CHUNKS; ++c, ++chunk_ctr) {
+        const int sbuf = chunk_ctr & 1;
+        uint8_t* stg = stage0 + sbuf * L::EPI_BUF_BYTES;
+        const int col0 = nb * BN + c * CHUNK;
+        // the buffer was last read by the store issued two chunks ago
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        if (args.read_c) {
+          uint64_t* cb = &cload[ew * EPI_BUFS + sbuf];
+          const uint32_t cph = (chunk_ctr >> 1) & 1;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(cb, L::EPI_BUF_BYTES);
+            tma_load_2d(stg, &tmC, col0, row0, cb);
+          }
+          pending_cload = sbuf;
+          pending_phase = cph;
+          if (!wait_warp(cb, cph, abort_flag, args, SITE_EPI_C_LOAD)) {
+            ok = false;
+            break;
+          }
+          pending_cload = -1;
+        }
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(t_row, v0, c * CHUNK);
+        if (CHUNK == 64) tmem_ld_32x32b_x32(t_row, v1, c * CHUNK + 32);
+        tmem_ld_wait();
+        if (c == CHUNKS - 1) {
+          // accumulator fully read: hand it back to the MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[buf]);
+        }
+        uint8_t* rowp = stg + r * SW;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {   // 16-byte pieces of the 128-byte row
+          uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
+          uint4 o;
+          if (OUT == OUT_F32) {
+            const uint32_t* src = v0 + 4 * j;
+            float x[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = args.alpha * __uint_as_float(src[e]);
+            if (args.read_c) {
+              const uint4 ci = *p;
+              x[0] = fmaf(args.beta, __uint_as_float(ci.x), x[0]);
+              x[1] = fmaf(args.beta, __uint_as_float(ci.y), x[1]);
+              x[2] = fmaf(args.beta, __uint_as_float(ci.z), x[2]);
+              x[3] = fmaf(args.beta, __uint_as_float(ci.w), x[3]);
+            }
+            o = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                           __float_as_uint(x[3]));
+          } else {
+            const uint32_t* src = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = args.alpha * __uint_as_float(src[e]);
+            if (args.read_c) {
+              const uint4 ci = *p;
+              const uint32_t cw[4] = {ci.x, ci.y, ci.z, ci.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack2(cw[e], OUT);
+                x[2 * e] = fmaf(args.beta, f.x, x[2 * e]);
+                x[2 * e + 1] = fmaf(args.beta, f.y, x[2 * e + 1]);
+              }
+            }
+            o = make_uint4(pack2(x[0], x[1], OUT), pack2(x[2], x[3], OUT), pack2(x[4], x[5], OUT),
+                           pack2(x[6], x[7], OUT));
+          }
+          *p = o;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, stg, col0, row0);
+          bulk_commit_group();
+        }
+      }
+    }
+    if (!ok && pending_cload >= 0 && lane == 0)
+      wait_drain(&cload[ew * EPI_BUFS + pending_cload], pending_phase, args);
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // Some role gave up.  Before TMEM is freed and the CTA exits, every
+    // asynchronous operation this CTA started must have finished:
+    if (warp == 0 && lane == 0) {
+      // the copies of the last STAGES ring iterations (older slots were
+      // consumed and re-armed), except an iteration deliberately left unarmed
+      const uint32_t it = producer_iters;
+      const uint32_t lo = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0;
+      for (uint32_t j = lo; j < it; ++j) {
+        if (args.inject_skip != 0 && j + 1 == static_cast<uint32_t>(args.inject_skip)) continue;
+        wait_drain(&full[j % STAGES], (j / STAGES) & 1, args);
+      }
+    }
+    if (warp == 1 && lane == 0) {
+      // every MMA already issued (a commit with nothing pending arrives at once)
+      umma_commit(drain);
+      wait_drain(drain, 0, args);
+    }
+  }
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// C <- beta * C (or 0 when beta == 0, without reading C): the K == 0 case.
+template <int OUT>
+__global__ void scale_c_kernel(void* C, long long ldc, int M, int N, float beta) {
+  const long long total = static_cast<long long>(M) * N;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / N, c = i % N;
+    const long long o = r * ldc + c;
+    if (OUT == OUT_F32) {
+      float* p = static_cast<float*>(C) + o;
+      *p = (beta == 0.0f) ? 0.0f : beta * *p;
+    } else if (OUT == OUT_BF16) {
+      __nv_bfloat16* p = static_cast<__nv_bfloat16*>(C) + o;
+      *p = (beta == 0.0f) ? __float2bfloat16_rn(0.0f) : __float2bfloat16_rn(beta * __bfloat162float(*p));
+    } else {
+      __half* p = static_cast<__half*>(C) + o;
+      *p = (beta == 0.0f) ? __float2half_rn(0.0f) : __float2half_rn(beta * __half2float(*p));
+    }
+  }
+}
+
+}  // namespace gemm_tc

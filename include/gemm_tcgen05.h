@@ -1,0 +1,176 @@
+/*
+ * gemm_tcgen05.h -- C ABI of a dense GEMM library for NVIDIA GB300 (sm_103a).
+ *
+ *     C <- alpha * A * B + beta * C
+ *
+ * A is M x K, B is K x N, C is M x N; inputs fp16 or bf16, products accumulated
+ * in fp32 by the fifth-generation tensor core (tcgen05, accumulator in Tensor
+ * Memory), output fp32, bf16 or fp16.  The operation is the GEMM of "GEMM From
+ * Naive CUDA to Tensor Cores" (leetllm.com/learn/gemm-naive-cuda-tensor-cores),
+ * opening section: shapes [M,K] x [K,N] = [M,N], C <- alpha*AB + beta*C, and
+ * with beta = 0 the old output is not read.  FLOPs are counted as 2*M*N*K
+ * (same page, "Compute one output before launching a warp").
+ *
+ * Conventions for every entry point:
+ *  - Pointers named A, B, C are DEVICE pointers of the current CUDA device,
+ *    owned by the caller; the library never frees or retains them.  A and B are
+ *    only read.  C is read (only when beta != 0) and written in place.
+ *  - All work is enqueued on `stream` (a cudaStream_t passed as void*, NULL =
+ *    legacy default stream) and the call returns without synchronising.  A fault
+ *    inside the kernel surfaces at the caller's next synchronisation, and a
+ *    timed-out internal wait through gemm_sync_status().
+ *  - Sizes and leading dimensions are in ELEMENTS; leading dimensions are the
+ *    distance between consecutive rows of the stored (row-major) array.
+ *  - Thread safety: calls from several host threads are safe; the debug knobs
+ *    (gemm_debug_set) are process-wide.
+ *  - Status codes are returned; nothing is printed and nothing aborts.
+ */
+#ifndef GEMM_TCGEN05_H
+#define GEMM_TCGEN05_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element formats. */
+typedef enum {
+  GEMM_F16 = 0,  /* IEEE binary16 */
+  GEMM_BF16 = 1, /* bfloat16 (8-bit exponent, 7-bit mantissa) */
+  GEMM_F32 = 2   /* IEEE binary32 (output only) */
+} gemm_dtype_t;
+
+/* Storage order of A and B (bit mask, OR one A flag with one B flag).  C is
+ * always row-major [M, N] with ldc >= N.  "Layout is part of the type" (leetllm
+ * page, section of that name): the flags say how memory is read; they never
+ * transpose data.
+ *   GEMM_A_ROW  A stored [M, K] row-major, lda >= K   (K-major)
+ *   GEMM_A_COL  A stored [K, M] row-major (A column-major), lda >= M (M-major)
+ *   GEMM_B_ROW  B stored [K, N] row-major, ldb >= N   (N-major)
+ *   GEMM_B_COL  B stored [N, K] row-major (B column-major), ldb >= K (K-major;
+ *               the A-row/B-col pairing is the "TN" layout of the Ada GEMM page,
+ *               kd.iw.mk, that makes both operand copies identical) */
+enum { GEMM_A_ROW = 0, GEMM_A_COL = 1, GEMM_B_ROW = 0, GEMM_B_COL = 2 };
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1, /* negative size, ld below its minimum, NULL operand
+                               that would be read or written, size overflow */
+  GEMM_ERR_UNSUPPORTED = 2, /* dtype not supported, pointer not 16-byte aligned,
+                               ld * element size not a multiple of 16 bytes
+                               (the tensor-copy engine's stride rule), a
+                               dimension >= 2^31 */
+  GEMM_ERR_ARCH = 3,        /* current device is not compute capability 10.3 */
+  GEMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (no device,
+                               launch failure, tensor-map encoding failure) */
+  GEMM_ERR_TIMEOUT = 5      /* a kernel wait gave up (see gemm_sync_status) */
+} gemm_status_t;
+
+/*
+ * gemm -- C <- alpha * A * B + beta * C on the current device.
+ *
+ * in_dtype  : GEMM_F16 or GEMM_BF16 (A and B share it).
+ * out_dtype : GEMM_F32, GEMM_BF16 or GEMM_F16 (C in and C out share it).
+ * layout    : GEMM_A_ROW|GEMM_A_COL combined with GEMM_B_ROW|GEMM_B_COL.
+ * Requirements: A, B, C 16-byte aligned; lda*2, ldb*2 and ldc*sizeof(out)
+ * multiples of 16 bytes.  Any M, N, K >= 0 (ragged edges are handled by the
+ * copy engine's zero fill on loads and clipping on stores).
+ * Quick returns: M == 0 or N == 0 -> GEMM_OK, nothing touched.  K == 0 ->
+ * C <- beta * C (C is not read when beta == 0), A and B not read.
+ * beta == 0: C is never read, so NaN/Inf already in C do not propagate.
+ * Deterministic: the same call on the same device gives bitwise-identical C.
+ * Accuracy: products are exact, sums are fp32 (order differs from a serial loop);
+ * the result is alpha*acc + beta*C evaluated in fp32, then rounded to nearest even.
+ */
+gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                   const void* B, int64_t ldb, float beta, void* C, int64_t ldc, int in_dtype,
+                   int out_dtype, int layout, void* stream);
+
+/* Tile-configuration override for sweeps.  Zero fields mean "choose
+ * automatically".  bn: output columns per CTA tile (64, 128 or 256; rows are
+ * always 128).  group_m: tile-rows per group of the grouped tile order (>= 1).
+ * grid: number of persistent CTAs (<= number of tiles). */
+typedef struct {
+  int32_t bn;
+  int32_t group_m;
+  int32_t grid;
+  int32_t reserved;
+} gemm_config_t;
+
+/* gemm with an explicit configuration (cfg may be NULL = gemm()).  Same
+ * contract and errors as gemm(); an invalid cfg field gives
+ * GEMM_ERR_INVALID_ARG. */
+gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, float beta, void* C, int64_t ldc, int in_dtype,
+                      int out_dtype, int layout, void* stream, const gemm_config_t* cfg);
+
+/*
+ * gemm_host -- the same GEMM on HOST operands (end-to-end path).
+ *
+ * hA, hB, hC are host pointers (pinned memory gives asynchronous copies);
+ * dA, dB, dC are caller-owned device buffers of at least the same extents
+ * (rows * ld elements of each stored array), used as staging.  On `stream`
+ * the call enqueues: copy hA -> dA and hB -> dB, copy hC -> dC when beta != 0,
+ * the GEMM on the device buffers, and copy dC -> hC.  It returns without
+ * synchronising; hC holds the result after the caller synchronises `stream`.
+ * Same argument rules and errors as gemm() (pointer checks apply to both sets).
+ */
+gemm_status_t gemm_host(int64_t M, int64_t N, int64_t K, float alpha, const void* hA, int64_t lda,
+                        const void* hB, int64_t ldb, float beta, void* hC, int64_t ldc,
+                        int in_dtype, int out_dtype, int layout, void* dA, void* dB, void* dC,
+                        void* stream);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* gemm_status_string(gemm_status_t status);
+
+/*
+ * gemm_sync_status -- synchronise `stream`, then report whether any GEMM kernel
+ * on the current device gave up a wait since the last call.  Returns GEMM_OK,
+ * GEMM_ERR_TIMEOUT (and stores the internal wait-site code, 1..6, in *site when
+ * site != NULL; the word is then cleared), or GEMM_ERR_CUDA if the
+ * synchronisation itself failed.  Meant for tests and benchmarks.
+ */
+gemm_status_t gemm_sync_status(void* stream, int* site);
+
+/*
+ * gemm_debug_set -- process-wide debug knobs, for tests only.
+ * wait_timeout_ns: limit of every kernel wait (0 restores the default, 2 s).
+ * inject_skip: when > 0, the copy producer of every CTA leaves its ring
+ * iteration number (inject_skip - 1) unarmed, so the consumer's wait must run
+ * out and the kernel must report GEMM_ERR_TIMEOUT and exit cleanly; 0 = off.
+ */
+void gemm_debug_set(uint64_t wait_timeout_ns, int32_t inject_skip);
+
+/* The launch plan gemm() would use, computed on the host only (no CUDA call):
+ * num_sms is the SM count to plan for.  Returns the same argument errors as
+ * gemm() for the size/dtype/layout arguments. */
+typedef struct {
+  int32_t bm, bn, bk, stages;
+  int32_t m_tiles, n_tiles, k_blocks, num_tiles;
+  int32_t grid, group_m, threads, smem_bytes;
+  int32_t tmem_cols, a_mn, b_mn, epi_chunk_cols;
+} gemm_plan_t;
+
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int layout,
+                        int32_t num_sms, const gemm_config_t* cfg, gemm_plan_t* plan);
+
+/* The grouped tile order (host copy of the device scheduler): tile index t ->
+ * (m_blk, n_blk).  Covers every tile of an m_tiles x n_tiles grid exactly once
+ * for t in [0, m_tiles * n_tiles). */
+void gemm_tile_coord(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_m,
+                     int32_t* m_blk, int32_t* n_blk);
+
+/* The tcgen05 descriptor encoders, exposed for host checks.  idesc: kind::f16
+ * instruction descriptor; sdesc: 128B-swizzled shared-memory descriptor. */
+uint32_t gemm_encode_idesc(int in_dtype, int a_mn, int b_mn, int m, int n);
+uint64_t gemm_encode_sdesc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int32_t gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_TCGEN05_H */

@@ -1,0 +1,200 @@
+"""Host-side checks of the C-ABI library that need no GPU: the shared library
+loads and exports every symbol the header declares, argument validation returns
+the documented codes before touching CUDA, a valid call without a device fails
+loudly (no CPU fallback), and the planner / tile order / descriptor encoders."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def g():
+    from dense_tensor_core_tcgen05_gb300 import build as b
+    b.build()
+    import dense_tensor_core_tcgen05_gb300 as g
+    return g
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "gemm_tcgen05.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_0-9]+)\s*\(", text)) -
+                  {"if", "sizeof", "defined"})
+
+
+def test_header_declares_what_binding_exports(g):
+    assert _header_functions() == sorted(g.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(g):
+    out = subprocess.run(["nm", "-D", "--defined-only", g.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in _header_functions():
+        assert name in syms, name
+    lib = ctypes.CDLL(g.LIB_PATH)
+    for name in _header_functions():
+        assert getattr(lib, name) is not None
+
+
+def test_header_compiles_as_c():
+    src = '#include "gemm_tcgen05.h"\nint main(void){gemm_plan_t p; (void)p; return 0;}\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-x", "c", "-", "-fsyntax-only"], input=src, text=True,
+                       capture_output=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings(g):
+    for s in range(6):
+        assert g.status_string(s)
+    assert g.status_string(99) == "unknown status"
+    assert g.gemm_version() >= 100
+
+
+ALIGNED = 1 << 20   # a fake 16-byte-aligned "pointer": validation never dereferences
+
+
+@pytest.mark.parametrize("args,expected", [
+    # M, N, K, lda, ldb, ldc, in, out, layout, A, B, C
+    ((-1, 8, 8, 8, 8, 8, 0, 2, 0, ALIGNED, ALIGNED, ALIGNED), 1),
+    ((8, -1, 8, 8, 8, 8, 0, 2, 0, ALIGNED, ALIGNED, ALIGNED), 1),
+    ((8, 8, -1, 8, 8, 8, 0, 2, 0, ALIGNED, ALIGNED, ALIGNED), 1),
+    ((8, 8, 8, 8, 8, 8, 2, 2, 0, ALIGNED, ALIGNED, ALIGNED), 2),      # fp32 inputs
+    ((8, 8, 8, 8, 8, 8, 7, 2, 0, ALIGNED, ALIGNED, ALIGNED), 2),      # bad in dtype
+    ((8, 8, 8, 8, 8, 8, 0, 5, 0, ALIGNED, ALIGNED, ALIGNED), 2),      # bad out dtype
+    ((8, 8, 8, 8, 8, 8, 0, 2, 4, ALIGNED, ALIGNED, ALIGNED), 1),      # bad layout bits
+    ((8, 16, 8, 8, 8, 8, 0, 2, 0, ALIGNED, ALIGNED, ALIGNED), 1),     # ldc < N
+    ((8, 8, 16, 8, 8, 8, 0, 2, 0, ALIGNED, ALIGNED, ALIGNED), 1),     # lda < K (A row)
+    ((16, 8, 8, 8, 8, 8, 0, 2, 1, ALIGNED, ALIGNED, ALIGNED), 1),     # lda < M (A col)
+    ((8, 16, 8, 8, 8, 16, 0, 2, 0, ALIGNED, ALIGNED, ALIGNED), 1),    # ldb < N (B row)
+    ((8, 8, 16, 16, 8, 8, 0, 2, 2, ALIGNED, ALIGNED, ALIGNED), 1),    # ldb < K (B col)
+    ((8, 8, 8, 8, 8, 8, 0, 2, 0, 0, ALIGNED, ALIGNED), 1),            # NULL A
+    ((8, 8, 8, 8, 8, 8, 0, 2, 0, ALIGNED, ALIGNED, 0), 1),            # NULL C
+    ((8, 8, 8, 8, 8, 8, 0, 2, 0, ALIGNED + 2, ALIGNED, ALIGNED), 2),  # misaligned A
+    ((8, 8, 8, 8, 8, 8, 0, 2, 0, ALIGNED, ALIGNED, ALIGNED + 8), 2),  # misaligned C
+    ((8, 8, 12, 12, 8, 8, 0, 2, 0, ALIGNED, ALIGNED, ALIGNED), 2),    # lda*2 not /16
+    ((8, 6, 8, 8, 6, 6, 0, 2, 0, ALIGNED, ALIGNED, ALIGNED), 2),      # ldc*4 not /16
+    ((1 << 31, 8, 8, 8, 8, 8, 0, 2, 0, ALIGNED, ALIGNED, ALIGNED), 2),  # M >= 2^31
+    ((0, 8, 8, 8, 8, 8, 0, 2, 0, 0, 0, 0), 0),                         # M == 0: no-op
+    ((8, 0, 8, 8, 8, 8, 0, 2, 0, 0, 0, 0), 0),                         # N == 0: no-op
+])
+def test_argument_validation_codes(g, args, expected):
+    M, N, K, lda, ldb, ldc, din, dout, layout, A, B, C = args
+    assert g.gemm(M, N, K, 1.0, A, lda, B, ldb, 0.0, C, ldc, din, dout, layout, 0) == expected
+
+
+def test_k_zero_does_not_need_a_or_b(g):
+    # valid K == 0 call: passes validation with NULL A/B and then needs a device
+    s = g.gemm(8, 8, 0, 1.0, 0, 0, 0, 0, 0.5, ALIGNED, 8, 0, 2, 0, 0)
+    assert s in (g.GEMM_ERR_CUDA, g.GEMM_ERR_ARCH, g.GEMM_OK)
+
+
+def test_no_cpu_fallback_without_device(g):
+    """A well-formed call on a machine without a usable GB300 must fail with a CUDA
+    or architecture error: the library has no CPU path."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    s = g.gemm(128, 128, 128, 1.0, ALIGNED, 128, ALIGNED, 128, 0.0, ALIGNED, 128, 0, 2, 0, 0)
+    assert s == g.GEMM_ERR_CUDA
+    with pytest.raises(ValueError):
+        g.matmul(torch.ones(4, 4, dtype=torch.float16), torch.ones(4, 4, dtype=torch.float16),
+                 torch.ones(4, 4))
+
+
+@pytest.mark.parametrize("shape,layout,expect", [
+    ((2048, 2048, 2048, 0, 2), 0, dict(bn=256, num_tiles=128, grid=128, k_blocks=32, b_mn=1)),
+    ((4096, 4096, 4096, 1, 1), 0, dict(bn=256, num_tiles=512, grid=152, k_blocks=64)),
+    ((8192, 8192, 8192, 1, 2), 2, dict(bn=256, num_tiles=2048, grid=152, b_mn=0)),
+    ((128, 8192, 8192, 1, 1), 2, dict(bn=64, num_tiles=128, grid=128, k_blocks=128)),
+    ((512, 512, 512, 0, 2), 0, dict(bn=64, num_tiles=32, grid=32)),
+    ((257, 263, 251, 1, 2), 3, dict(m_tiles=3, k_blocks=4, a_mn=1, b_mn=0)),
+])
+def test_plan(g, shape, layout, expect):
+    M, N, K, din, dout = shape
+    s, p = g.gemm_plan(M, N, K, din, dout, layout, 152)
+    assert s == 0
+    d = p.as_dict()
+    for k, v in expect.items():
+        assert d[k] == v, (k, d)
+    assert d["smem_bytes"] <= 232448
+    assert d["tmem_cols"] in (128, 256, 512)
+    assert d["stages"] * (128 * 64 * 2 + d["bn"] * 64 * 2) <= 192 * 1024
+
+
+def test_plan_overrides_and_errors(g):
+    s, p = g.gemm_plan(1024, 1024, 1024, 0, 2, 0, 152, {"bn": 128, "group_m": 3, "grid": 10})
+    assert s == 0 and (p.bn, p.group_m, p.grid) == (128, 3, 10)
+    s, _ = g.gemm_plan(1024, 1024, 1024, 0, 2, 0, 152, {"bn": 96})
+    assert s == g.GEMM_ERR_INVALID_ARG
+    s, _ = g.gemm_plan(1024, 1024, 1024, 0, 2, 0, 0)
+    assert s == g.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("mt,nt,gm", [(1, 1, 1), (32, 16, 8), (32, 16, 16), (5, 7, 3),
+                                      (13, 4, 16), (64, 32, 16), (1, 128, 1), (3, 1, 2)])
+def test_tile_order_covers_every_tile_once(g, mt, nt, gm):
+    seen = np.zeros((mt, nt), np.int32)
+    for t in range(mt * nt):
+        m, n = g.gemm_tile_coord(t, mt, nt, gm)
+        assert 0 <= m < mt and 0 <= n < nt
+        seen[m, n] += 1
+    assert np.all(seen == 1)
+
+
+def _avg_panels(order, window):
+    counts = []
+    for i in range(0, len(order) - window + 1, window):
+        w = order[i:i + window]
+        counts.append(len({m for m, _ in w}) + len({n for _, n in w}))
+    return sum(counts) / len(counts)
+
+
+def test_grouped_order_panel_counts_from_lecture(g):
+    """"Scheduling is geometry" (linearly.space lecture 26.5): eight tiles in flight
+    in one row of the tile grid need 1 + 8 = 9 operand panels; the same eight tiles
+    as a 4 x 2 block need 4 + 2 = 6.  The grouped order with group_m = 4 visits
+    exactly such 4 x 2 blocks."""
+    mt, nt = 32, 16
+    row_major = [(t // nt, t % nt) for t in range(mt * nt)]
+    grouped = [g.gemm_tile_coord(t, mt, nt, 4) for t in range(mt * nt)]
+    assert _avg_panels(row_major, 8) == 9
+    assert _avg_panels(grouped, 8) == 6
+    # a 64-tile wave: row-major spans 4 rows x 16 columns (20 panels), group_m = 8
+    # gives 8 x 8 blocks (16 panels)
+    grouped8 = [g.gemm_tile_coord(t, mt, nt, 8) for t in range(mt * nt)]
+    assert _avg_panels(row_major, 64) == 20
+    assert _avg_panels(grouped8, 64) == 16
+
+
+def test_instruction_descriptor_fields(g):
+    d = g.gemm_encode_idesc(1, 0, 1, 128, 256)
+    assert (d >> 4) & 3 == 1          # D = f32
+    assert (d >> 7) & 7 == 1          # A = bf16
+    assert (d >> 10) & 7 == 1         # B = bf16
+    assert (d >> 15) & 1 == 0         # A K-major
+    assert (d >> 16) & 1 == 1         # B MN-major
+    assert (d >> 17) & 0x3F == 256 >> 3
+    assert (d >> 24) & 0x1F == 128 >> 4
+    assert d & 0b1111 == 0 and (d >> 13) & 3 == 0 and (d >> 23) & 1 == 0 and d >> 29 == 0
+    d16 = g.gemm_encode_idesc(0, 1, 0, 128, 64)
+    assert (d16 >> 7) & 0x3F == 0 and (d16 >> 15) & 3 == 1 and (d16 >> 17) & 0x3F == 8
+
+
+def test_smem_descriptor_fields(g):
+    d = g.gemm_encode_sdesc(0x10400, 16, 1024)
+    assert d & 0x3FFF == 0x10400 >> 4
+    assert (d >> 16) & 0x3FFF == 1
+    assert (d >> 32) & 0x3FFF == 64
+    assert (d >> 46) & 3 == 1
+    assert (d >> 49) & 7 == 0
+    assert (d >> 61) & 7 == 2
+    d2 = g.gemm_encode_sdesc(0x3FFF0, 8192, 1024)
+    assert d2 & 0x3FFF == 0x3FFF and (d2 >> 16) & 0x3FFF == 512
