@@ -265,6 +265,9 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   const uint64_t tmo = g_timeout_ns.load(std::memory_order_relaxed);
   ka.timeout_ns = tmo ? tmo : kDefaultTimeoutNs;
   ka.inject_skip = g_inject_skip.load(std::memory_order_relaxed);
+  ka.c_ptr = C;
+  ka.ldc = ldc;
+  ka.n_ragged = ((N * out_size(out_dtype)) % 16) != 0 ? 1 : 0;
 
   cudaError_t e;
   switch (out_dtype) {

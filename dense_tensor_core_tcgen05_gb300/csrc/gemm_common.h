@@ -74,6 +74,9 @@ struct KernelArgs {
   int* status;           // device status word (0 = ok)
   unsigned long long timeout_ns;
   int inject_skip;       // debug: the producer leaves ring iteration (inject_skip - 1) unarmed
+  void* c_ptr;           // C base (for the ragged right edge, written with plain stores)
+  long long ldc;         // C leading dimension in elements
+  int n_ragged;          // 1 when N * sizeof(out) is not a multiple of 16 bytes
 };
 
 }  // namespace gemm_tc

@@ -347,6 +347,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           pending_cload = -1;
         }
+        // A chunk that crosses the right edge of C when N * sizeof(out) is not a
+        // multiple of 16 bytes is written with predicated plain stores: the
+        // tensor store writes whole 16-byte pieces and would touch the columns
+        // just past N.  Chunks entirely right of N are not stored at all.
+        const bool ragged = args.n_ragged && (col0 + CHUNK > args.N);
+        const bool skip_store = col0 >= args.N || row0 >= args.M;
         uint32_t v0[32], v1[32];
         tmem_ld_32x32b_x32(t_row, v0, c * CHUNK);
         if (CHUNK == 64) tmem_ld_32x32b_x32(t_row, v1, c * CHUNK + 32);
@@ -394,14 +400,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             o = make_uint4(pack2(x[0], x[1], OUT), pack2(x[2], x[3], OUT), pack2(x[4], x[5], OUT),
                            pack2(x[6], x[7], OUT));
           }
-          *p = o;
+          if (!ragged) {
+            *p = o;
+          } else if (!skip_store && row0 + r < args.M) {
+            const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+            if (OUT == OUT_F32) {
+              float* dst = static_cast<float*>(args.c_ptr) +
+                           static_cast<long long>(row0 + r) * args.ldc + col0 + 4 * j;
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (col0 + 4 * j + e < args.N) dst[e] = __uint_as_float(ow[e]);
+            } else {
+              uint16_t* dst = static_cast<uint16_t*>(args.c_ptr) +
+                              static_cast<long long>(row0 + r) * args.ldc + col0 + 8 * j;
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (col0 + 8 * j + e < args.N)
+                  dst[e] = static_cast<uint16_t>(ow[e >> 1] >> (16 * (e & 1)));
+            }
+          }
         }
-        fence_proxy_async_smem();
+        if (!ragged && !skip_store) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tma_store_2d(&tmC, stg, col0, row0);
+        }
+        // exactly one bulk group per chunk (empty when nothing was stored), so
+        // "at most one group still reading" above always means "the other buffer"
+        if (lane == 0) bulk_commit_group();
         __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmC, stg, col0, row0);
-          bulk_commit_group();
-        }
       }
     }
     if (!ok && pending_cload >= 0 && lane == 0)
