@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -123,55 +124,80 @@ gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Tile-width choice: the width whose wave-quantised cost, waves * (bn + 64), is
-// lowest (a wave = one tile per SM; "+64" stands for the per-k-block A traffic
-// every tile pays whatever its width).  Ties go to the wider tile.
-int choose_bn(int64_t M, int64_t N, int num_sms) {
-  const int widths[3] = {256, 128, 64};
-  int best = 256;
+// Work-unit choice.  Per k-block a CTA's tensor core needs 2*W cycles for a
+// 128 x W tile, while its shared memory must receive (128 + W') * 128 bytes
+// (W' = B columns it loads: W, or W/2 for a CTA pair); measured on GB300 the
+// delivery is ~64 B per SM clock, so a k-block costs max(2W, bytes/64) cycles.
+// A launch costs waves * k-block cost (a wave = one unit per SM, or per SM pair),
+// so the choice weighs tile efficiency against wave quantisation.  Pairs need
+// more than 128 rows.  Ties go to the earlier candidate (wider, pair first).
+void choose_unit(int64_t M, int64_t N, int num_sms, int* bn_out, bool* pair_out) {
+  struct Cand { int bn; bool pair; };
+  const Cand cands[5] = {{256, true}, {128, true}, {256, false}, {128, false}, {64, false}};
   int64_t best_cost = -1;
-  for (int w : widths) {
-    const int64_t tiles = ceil_div(M, BM) * ceil_div(N, w);
-    const int64_t waves = ceil_div(tiles, num_sms);
-    const int64_t cost = waves * (w + 64);
+  *bn_out = 256;
+  *pair_out = false;
+  for (const Cand& c : cands) {
+    if (c.pair && (M <= BM || num_sms < 2)) continue;
+    const int64_t rows = c.pair ? 2 * BM : BM;
+    const int64_t units = ceil_div(M, rows) * ceil_div(N, c.bn);
+    const int64_t slots = c.pair ? num_sms / 2 : num_sms;
+    const int64_t waves = ceil_div(units, slots);
+    const int64_t bytes = int64_t(BM + b_cols_per_cta(c.bn, c.pair)) * BK * 2;
+    const int64_t per_kblock = std::max<int64_t>(2 * c.bn, bytes / 64);
+    const int64_t cost = waves * per_kblock;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
-      best = w;
+      *bn_out = c.bn;
+      *pair_out = c.pair;
     }
   }
-  return best;
 }
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layout, int num_sms,
                         const gemm_config_t* cfg, gemm_plan_t* p) {
   if (num_sms <= 0) return GEMM_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
-  int bn = (cfg && cfg->bn) ? cfg->bn : choose_bn(M, N, num_sms);
-  if (bn != 64 && bn != 128 && bn != 256) return GEMM_ERR_INVALID_ARG;
-  p->bm = BM;
+  int bn = 0;
+  bool pair = false;
+  choose_unit(M, N, num_sms, &bn, &pair);
+  if (cfg && cfg->cta_group) {
+    if (cfg->cta_group != 1 && cfg->cta_group != 2) return GEMM_ERR_INVALID_ARG;
+    pair = cfg->cta_group == 2;
+    if (!cfg->bn) bn = 256;
+  }
+  if (cfg && cfg->bn) bn = cfg->bn;
+  if (pair ? (bn != 128 && bn != 256) : (bn != 64 && bn != 128 && bn != 256))
+    return GEMM_ERR_INVALID_ARG;
+  const int rows = pair ? 2 * BM : BM;
+  p->bm = rows;
   p->bn = bn;
   p->bk = BK;
-  p->stages = stages_for_bn(bn);
-  const int64_t mt = ceil_div(M, BM), nt = ceil_div(N, bn), kb = ceil_div(K, BK);
-  if (mt * nt >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
+  p->stages = stages_for(bn, pair);
+  const int64_t mt = ceil_div(M, rows), nt = ceil_div(N, bn), kb = ceil_div(K, BK);
+  if (mt * nt >= (int64_t(1) << 30)) return GEMM_ERR_UNSUPPORTED;
   p->m_tiles = static_cast<int32_t>(mt);
   p->n_tiles = static_cast<int32_t>(nt);
   p->k_blocks = static_cast<int32_t>(kb);
   p->num_tiles = static_cast<int32_t>(mt * nt);
   int gm = (cfg && cfg->group_m) ? cfg->group_m : (bn == 256 ? 16 : 8);
+  if (pair && !(cfg && cfg->group_m)) gm = 8;
   if (gm < 0) return GEMM_ERR_INVALID_ARG;
   if (gm > p->m_tiles) gm = p->m_tiles > 0 ? p->m_tiles : 1;
   p->group_m = gm;
-  int grid = (cfg && cfg->grid) ? cfg->grid : num_sms;
+  const int per_unit = pair ? 2 : 1;
+  int grid = (cfg && cfg->grid) ? cfg->grid : (pair ? (num_sms / 2) * 2 : num_sms);
   if (grid < 0) return GEMM_ERR_INVALID_ARG;
-  if (grid > p->num_tiles) grid = p->num_tiles;
+  if (grid > p->num_tiles * per_unit) grid = p->num_tiles * per_unit;
+  if (pair) grid = std::max(2, grid & ~1);
   p->grid = grid;
   p->threads = NUM_THREADS;
-  p->smem_bytes = smem_alloc_bytes(bn);
+  p->smem_bytes = smem_alloc_bytes(bn, pair);
   p->tmem_cols = 2 * bn;
   p->a_mn = (layout & GEMM_A_COL) ? 1 : 0;
   p->b_mn = (layout & GEMM_B_COL) ? 0 : 1;
   p->epi_chunk_cols = out_dtype == GEMM_F32 ? 32 : 64;
+  p->cta_group = pair ? 2 : 1;
   return GEMM_OK;
 }
 
@@ -239,7 +265,8 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   const CUtensorMapDataType din = tma_dtype(in_dtype);
   bool ok = a_col ? encode_2d(&ta, din, A, M, K, lda * 2, ATOM_MN, BK)
                   : encode_2d(&ta, din, A, K, M, lda * 2, BK, BM);
-  ok = ok && (b_col ? encode_2d(&tb, din, B, K, N, ldb * 2, BK, p.bn)
+  const bool pair = p.cta_group == 2;
+  ok = ok && (b_col ? encode_2d(&tb, din, B, K, N, ldb * 2, BK, b_cols_per_cta(p.bn, pair))
                     : encode_2d(&tb, din, B, N, K, ldb * 2, ATOM_MN, BK));
   ok = ok && encode_2d(&tc, tma_dtype(out_dtype), C, N, M, ldc * out_size(out_dtype),
                        p.epi_chunk_cols, EPI_ROWS);
@@ -257,7 +284,7 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.group_m = p.group_m;
   ka.alpha = alpha;
   ka.beta = beta;
-  ka.idesc = make_idesc_f16(in_dtype == GEMM_BF16 ? 1 : 0, p.a_mn, p.b_mn, BM, p.bn);
+  ka.idesc = make_idesc_f16(in_dtype == GEMM_BF16 ? 1 : 0, p.a_mn, p.b_mn, p.bm, p.bn);
   ka.a_mn = p.a_mn;
   ka.b_mn = p.b_mn;
   ka.read_c = beta != 0.0f ? 1 : 0;
@@ -271,9 +298,9 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
 
   cudaError_t e;
   switch (out_dtype) {
-    case GEMM_F32: e = launch_gemm_f32(p.bn, ta, tb, tc, ka, p.grid, stream, dev); break;
-    case GEMM_BF16: e = launch_gemm_bf16(p.bn, ta, tb, tc, ka, p.grid, stream, dev); break;
-    default: e = launch_gemm_f16(p.bn, ta, tb, tc, ka, p.grid, stream, dev); break;
+    case GEMM_F32: e = launch_gemm_f32(p.bn, pair, ta, tb, tc, ka, p.grid, stream, dev); break;
+    case GEMM_BF16: e = launch_gemm_bf16(p.bn, pair, ta, tb, tc, ka, p.grid, stream, dev); break;
+    default: e = launch_gemm_f16(p.bn, pair, ta, tb, tc, ka, p.grid, stream, dev); break;
   }
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -281,11 +308,18 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
 }  // namespace
 
 namespace gemm_tc {
-int smem_alloc_bytes(int bn) {
+int smem_alloc_bytes(int bn, bool pair) {
+  if (pair) {
+    switch (bn) {
+      case 128: return SmemLayout<128, stages_for(128, true), true>::ALLOC;
+      case 256: return SmemLayout<256, stages_for(256, true), true>::ALLOC;
+      default: return 0;
+    }
+  }
   switch (bn) {
-    case 64: return SmemLayout<64, stages_for_bn(64)>::ALLOC;
-    case 128: return SmemLayout<128, stages_for_bn(128)>::ALLOC;
-    case 256: return SmemLayout<256, stages_for_bn(256)>::ALLOC;
+    case 64: return SmemLayout<64, stages_for(64, false), false>::ALLOC;
+    case 128: return SmemLayout<128, stages_for(128, false), false>::ALLOC;
+    case 256: return SmemLayout<256, stages_for(256, false), false>::ALLOC;
     default: return 0;
   }
 }

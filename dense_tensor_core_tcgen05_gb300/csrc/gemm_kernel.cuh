@@ -52,10 +52,14 @@ enum WaitSite {
   SITE_DRAIN = 6,
 };
 
-template <int BN, int STAGES>
+// Shared-memory map of one CTA.  In pair mode (two CTAs computing a 256-row
+// tile with one cta_group::2 MMA) each CTA holds its own 128 rows of A and half
+// of the tile's B columns.
+template <int BN, int STAGES, bool PAIR>
 struct SmemLayout {
+  static constexpr int B_COLS = PAIR ? BN / 2 : BN;   // B columns (N) held by this CTA
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = B_COLS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_BUF_BYTES = EPI_ROWS * SW;
   static constexpr int off_a = 0;
@@ -72,6 +76,7 @@ struct SmemLayout {
   static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                 "TMEM allocation must be a power of two in [32, 512]");
   static_assert(ALLOC <= 232448, "exceeds the 227 KB per-block shared memory limit");
+  static_assert(B_COLS % ATOM_MN == 0, "B half-tiles are whole 64-column swizzle atoms");
 };
 
 __device__ __forceinline__ void record_error(int* status, int code) {
@@ -79,13 +84,14 @@ __device__ __forceinline__ void record_error(int* status, int code) {
 }
 
 // Bounded wait by one thread.  Returns false on timeout or when another role
-// has raised the abort flag.
+// has raised the abort flag.  CLUSTER: acquire at cluster scope (pair mode).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_one(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                          const KernelArgs& a, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     if ((i & 15) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > a.timeout_ns) {
@@ -100,12 +106,13 @@ __device__ __forceinline__ bool wait_one(uint64_t* bar, uint32_t parity, volatil
 // Bounded wait by a whole warp, with a warp-uniform result: it succeeds once
 // every lane has observed the phase (a phase cannot advance again before this
 // warp acts on it), and lane 0 alone decides to give up.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           const KernelArgs& a, int site) {
   const int lane = threadIdx.x & 31;
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
-    const bool done = mbar_try_wait(bar, parity);
+    const bool done = mbar_try_wait<CLUSTER>(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
     if ((i & 15) == 15) {
       int give_up = 0;
@@ -126,9 +133,10 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volati
 }
 
 // Wait used only while draining after an abort: ignores the abort flag.
+template <bool CLUSTER = false>
 __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity, const KernelArgs& a) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait<CLUSTER>(bar, parity)) {
     if (globaltimer_ns() - t0 > a.timeout_ns) {
       record_error(a.status, SITE_DRAIN);
       return;
@@ -169,16 +177,17 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, int out_kind) {
   return __half22float2(h);
 }
 
-template <int BN, int STAGES, int OUT>
+template <int BN, int STAGES, int OUT, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const KernelArgs args) {
-  using L = SmemLayout<BN, STAGES>;
+  using L = SmemLayout<BN, STAGES, PAIR>;
   constexpr int CHUNK = OutTraits<OUT>::CHUNK_COLS;
   constexpr int CHUNKS = BN / CHUNK;
+  constexpr int TILE_M = PAIR ? 2 * BM : BM;       // rows of one work unit
   static_assert(BN % CHUNK == 0, "tile width must be a whole number of epilogue chunks");
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N in [16,256], N%16==0");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be in [16,256], N%16==0");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -195,6 +204,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Pair mode: the even CTA of the cluster (rank 0) issues the MMAs and owns the
+  // "full" and "tmem empty" barriers both CTAs signal; each CTA computes rows
+  // [rank * 128, rank * 128 + 128) of the 256-row unit.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+  const bool leader = rank == 0;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   uint32_t producer_iters = 0;  // ring iterations armed (producer thread only)
 
   if (threadIdx.x == 0) {
@@ -204,7 +220,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], EPI_WARPS);
+      mbar_init(&tempty[b], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
     for (int i = 0; i < EPI_WARPS * EPI_BUFS; ++i) mbar_init(&cload[i], 1);
     mbar_init(drain, 1);
@@ -215,11 +231,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefetch_tensormap(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, L::TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, L::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -228,48 +252,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------ TMA producer
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x) {
+      for (int t = unit0; ok && t < args.num_tiles; t += unit_stride) {
         int mb, nb;
         tile_coord(t, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
+        const int a_row = mb * TILE_M + static_cast<int>(rank) * BM;
+        const int b_col = nb * BN + static_cast<int>(rank) * L::B_COLS;
         for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_one(&empty[s], ph ^ 1, abort_flag, args, SITE_PRODUCER_EMPTY)) {
+          if (!wait_one<PAIR>(&empty[s], ph ^ 1, abort_flag, args, SITE_PRODUCER_EMPTY)) {
             ok = false;
             break;
           }
           if (args.inject_skip != 0 && it + 1 == static_cast<uint32_t>(args.inject_skip)) continue;
-          mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
+          // the leader's full[s] counts the bytes of both CTAs of a pair
+          if (leader) mbar_arrive_expect_tx(&full[s], (PAIR ? 2 : 1) * L::STAGE_BYTES);
           uint8_t* sa = smem + L::off_a + s * L::A_BYTES;
           uint8_t* sb = smem + L::off_b + s * L::B_BYTES;
           const int k0 = kb * BK;
+          const uint32_t bar_c = PAIR ? map_to_rank(&full[s], 0) : 0;
+          auto load = [&](void* dst, const CUtensorMap* m, int x, int y) {
+            if (PAIR)
+              tma_load_2d_pair(dst, m, x, y, bar_c);
+            else
+              tma_load_2d(dst, m, x, y, &full[s]);
+          };
           if (!args.a_mn) {
-            tma_load_2d(sa, &tmA, k0, mb * BM, &full[s]);
+            load(sa, &tmA, k0, a_row);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / ATOM_MN; ++j)
-              tma_load_2d(sa + j * (BK * SW), &tmA, mb * BM + j * ATOM_MN, k0, &full[s]);
+            for (int j = 0; j < BM / ATOM_MN; ++j) load(sa + j * (BK * SW), &tmA, a_row + j * ATOM_MN, k0);
           }
           if (!args.b_mn) {
-            tma_load_2d(sb, &tmB, k0, nb * BN, &full[s]);
+            load(sb, &tmB, k0, b_col);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / ATOM_MN; ++j)
-              tma_load_2d(sb + j * (BK * SW), &tmB, nb * BN + j * ATOM_MN, k0, &full[s]);
+            for (int j = 0; j < L::B_COLS / ATOM_MN; ++j)
+              load(sb + j * (BK * SW), &tmB, b_col + j * ATOM_MN, k0);
           }
         }
       }
       producer_iters = it;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ------------------------------------------------------ MMA issuer
       uint32_t it = 0, tl = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x, ++tl) {
+      for (int t = unit0; ok && t < args.num_tiles; t += unit_stride, ++tl) {
         const int buf = tl & 1;
         const uint32_t aph = (tl >> 1) & 1;
-        if (!wait_one(&tempty[buf], aph ^ 1, abort_flag, args, SITE_MMA_TMEM_EMPTY)) {
+        if (!wait_one<PAIR>(&tempty[buf], aph ^ 1, abort_flag, args, SITE_MMA_TMEM_EMPTY)) {
           ok = false;
           break;
         }
@@ -278,7 +311,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_one(&full[s], ph, abort_flag, args, SITE_MMA_FULL)) {
+          if (!wait_one<PAIR>(&full[s], ph, abort_flag, args, SITE_MMA_FULL)) {
             ok = false;
             break;
           }
@@ -293,12 +326,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                           : make_sdesc_sw128(sa + kk * (UMMA_K * 2), 16, 8 * SW);
             const uint64_t db = args.b_mn ? make_sdesc_sw128(sb + kk * (UMMA_K * SW), BK * SW, 8 * SW)
                                           : make_sdesc_sw128(sb + kk * (UMMA_K * 2), 16, 8 * SW);
-            umma_f16(d_tmem, da, db, args.idesc, (kb | kk) != 0 ? 1u : 0u);
+            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+            if (PAIR)
+              umma_f16_pair(d_tmem, da, db, args.idesc, acc);
+            else
+              umma_f16(d_tmem, da, db, args.idesc, acc);
           }
-          umma_commit(&empty[s]);
+          if (PAIR)
+            umma_commit_pair_multicast(&empty[s], 0x3);   // free slot s in both CTAs
+          else
+            umma_commit(&empty[s]);
         }
         if (!ok) break;
-        umma_commit(&tfull[buf]);
+        if (PAIR)
+          umma_commit_pair_multicast(&tfull[buf], 0x3);   // accumulator ready in both CTAs
+        else
+          umma_commit(&tfull[buf]);
       }
     }
   } else {
@@ -311,19 +354,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t pending_phase = 0;
     bool ok = true;
     const int r = lane;                  // this thread's row inside the warp's 32-row block
-    for (int t = blockIdx.x; ok && t < args.num_tiles; t += gridDim.x, ++tl) {
+    for (int t = unit0; ok && t < args.num_tiles; t += unit_stride, ++tl) {
       int mb, nb;
       tile_coord(t, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
       const int buf = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
-      if (!wait_warp(&tfull[buf], aph, abort_flag, args, SITE_EPI_TMEM_FULL)) {
+      if (!wait_warp<PAIR>(&tfull[buf], aph, abort_flag, args, SITE_EPI_TMEM_FULL)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
-      const int row0 = mb * BM + quarter * 32;
+      const int row0 = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32;
 #pragma unroll 1
       for (int c = 0; c < CHUNKS; ++c, ++chunk_ctr) {
         const int sbuf = chunk_ctr & 1;
@@ -341,7 +384,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           pending_cload = sbuf;
           pending_phase = cph;
-          if (!wait_warp(cb, cph, abort_flag, args, SITE_EPI_C_LOAD)) {
+          if (!wait_warp<PAIR>(cb, cph, abort_flag, args, SITE_EPI_C_LOAD)) {
             ok = false;
             break;
           }
@@ -361,7 +404,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // accumulator fully read: hand it back to the MMA issuer
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[buf]);
+          if (lane == 0) {
+            if (leader)
+              mbar_arrive(&tempty[buf]);
+            else
+              mbar_arrive_cluster(map_to_rank(&tempty[buf], 0));
+          }
         }
         uint8_t* rowp = stg + r * SW;
 #pragma unroll
@@ -432,7 +480,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     if (!ok && pending_cload >= 0 && lane == 0)
-      wait_drain(&cload[ew * EPI_BUFS + pending_cload], pending_phase, args);
+      wait_drain<PAIR>(&cload[ew * EPI_BUFS + pending_cload], pending_phase, args);
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
   }
@@ -443,25 +491,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Some role gave up.  Before TMEM is freed and the CTA exits, every
     // asynchronous operation this CTA started must have finished:
     if (warp == 0 && lane == 0) {
-      // the copies of the last STAGES ring iterations (older slots were
-      // consumed and re-armed), except an iteration deliberately left unarmed
-      const uint32_t it = producer_iters;
-      const uint32_t lo = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0;
-      for (uint32_t j = lo; j < it; ++j) {
-        if (args.inject_skip != 0 && j + 1 == static_cast<uint32_t>(args.inject_skip)) continue;
-        wait_drain(&full[j % STAGES], (j / STAGES) & 1, args);
+      if (leader) {
+        // the copies of the last STAGES ring iterations (older slots were
+        // consumed and re-armed), except an iteration deliberately left unarmed;
+        // in pair mode these phases also count the peer's copies
+        const uint32_t it = producer_iters;
+        const uint32_t lo = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0;
+        for (uint32_t j = lo; j < it; ++j) {
+          if (args.inject_skip != 0 && j + 1 == static_cast<uint32_t>(args.inject_skip)) continue;
+          wait_drain<PAIR>(&full[j % STAGES], (j / STAGES) & 1, args);
+        }
+      } else {
+        // the odd CTA's copies complete on the leader's barrier, which it cannot
+        // wait on: give copies in flight a bounded grace period to land
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
       }
     }
-    if (warp == 1 && lane == 0) {
+    if (warp == 1 && lane == 0 && leader) {
       // every MMA already issued (a commit with nothing pending arrives at once)
-      umma_commit(drain);
-      wait_drain(drain, 0, args);
+      if (PAIR)
+        umma_commit_pair_multicast(drain, 0x1);
+      else
+        umma_commit(drain);
+      wait_drain<PAIR>(drain, 0, args);
     }
+  }
+  if (PAIR) {
+    // neither CTA may free TMEM or exit while its peer can still signal its
+    // barriers or read its shared memory
+    tc_fence_before();
+    cluster_sync();
   }
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, L::TMEM_COLS);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
 }
 

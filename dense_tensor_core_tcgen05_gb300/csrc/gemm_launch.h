@@ -8,21 +8,29 @@
 
 namespace gemm_tc {
 
-// Pipeline depth for a tile width: as many ring slots as fit in 192 KB of
-// shared memory (the rest holds the epilogue staging buffers and barriers).
-constexpr int stages_for_bn(int bn) { return (192 * 1024) / (BM * BK * 2 + bn * BK * 2); }
+// B columns one CTA holds: the whole tile width, or half of it in pair mode.
+constexpr int b_cols_per_cta(int bn, bool pair) { return pair ? bn / 2 : bn; }
+
+// Pipeline depth: as many ring slots as fit in 192 KB of shared memory (the rest
+// holds the epilogue staging buffers and barriers).
+constexpr int stages_for(int bn, bool pair) {
+  return (192 * 1024) / (BM * BK * 2 + b_cols_per_cta(bn, pair) * BK * 2);
+}
 
 // Dynamic shared memory bytes of an instance (layout + alignment slack).
-int smem_alloc_bytes(int bn);
+int smem_alloc_bytes(int bn, bool pair);
 
-// Launch the instance for tile width `bn` (64, 128 or 256).  `dev` indexes the
-// per-device "attribute already set" cache.  Returns the launch status.
-cudaError_t launch_gemm_f32(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                            const KernelArgs& args, int grid, cudaStream_t stream, int dev);
-cudaError_t launch_gemm_bf16(int bn, const CUtensorMap& a, const CUtensorMap& b,
+// Launch the instance (tile width bn, single CTA or CTA pair).  `grid` is the
+// number of CTAs (even in pair mode); pair launches are capped at the number of
+// co-resident 2-CTA clusters.  `dev` indexes the per-device attribute cache.
+cudaError_t launch_gemm_f32(int bn, bool pair, const CUtensorMap& a, const CUtensorMap& b,
+                            const CUtensorMap& c, const KernelArgs& args, int grid,
+                            cudaStream_t stream, int dev);
+cudaError_t launch_gemm_bf16(int bn, bool pair, const CUtensorMap& a, const CUtensorMap& b,
                              const CUtensorMap& c, const KernelArgs& args, int grid,
                              cudaStream_t stream, int dev);
-cudaError_t launch_gemm_f16(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                            const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_f16(int bn, bool pair, const CUtensorMap& a, const CUtensorMap& b,
+                            const CUtensorMap& c, const KernelArgs& args, int grid,
+                            cudaStream_t stream, int dev);
 
 }  // namespace gemm_tc

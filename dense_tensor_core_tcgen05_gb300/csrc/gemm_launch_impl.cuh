@@ -8,31 +8,65 @@ namespace gemm_tc {
 namespace {
 constexpr int kMaxDevices = 64;
 
-template <int BN>
-cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                      const KernelArgs& args, int grid, cudaStream_t stream, int dev) {
-  constexpr int ST = stages_for_bn(BN);
-  using L = SmemLayout<BN, ST>;
-  auto kern = gemm_tcgen05_kernel<BN, ST, GEMM_OUT_KIND>;
+template <int BN, bool PAIR>
+cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const KernelArgs& args, int grid, cudaStream_t stream, int dev) {
+  constexpr int ST = stages_for(BN, PAIR);
+  using L = SmemLayout<BN, ST, PAIR>;
+  auto kern = gemm_tcgen05_kernel<BN, ST, GEMM_OUT_KIND, PAIR>;
   static volatile bool attr_set[kMaxDevices] = {};
+  static volatile int max_clusters[kMaxDevices] = {};
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  kern<<<grid, NUM_THREADS, L::ALLOC, stream>>>(a, b, c, args);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.stream = stream;
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_clusters[dev] == 0) {
+      cfg.gridDim = dim3(2, 1, 1);
+      int n = 0;
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n <= 0) return cudaErrorInvalidConfiguration;
+      max_clusters[dev] = n;
+    }
+    if (grid > 2 * max_clusters[dev]) grid = 2 * max_clusters[dev];
+    grid &= ~1;
+    if (grid < 2) return cudaErrorInvalidConfiguration;
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t GEMM_LAUNCH_NAME(int bn, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t GEMM_LAUNCH_NAME(int bn, bool pair, const CUtensorMap& a, const CUtensorMap& b,
                              const CUtensorMap& c, const KernelArgs& args, int grid,
                              cudaStream_t stream, int dev) {
+  if (pair) {
+    switch (bn) {
+      case 128: return launch_inst<128, true>(a, b, c, args, grid, stream, dev);
+      case 256: return launch_inst<256, true>(a, b, c, args, grid, stream, dev);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (bn) {
-    case 64: return launch_bn<64>(a, b, c, args, grid, stream, dev);
-    case 128: return launch_bn<128>(a, b, c, args, grid, stream, dev);
-    case 256: return launch_bn<256>(a, b, c, args, grid, stream, dev);
+    case 64: return launch_inst<64, false>(a, b, c, args, grid, stream, dev);
+    case 128: return launch_inst<128, false>(a, b, c, args, grid, stream, dev);
+    case 256: return launch_inst<256, false>(a, b, c, args, grid, stream, dev);
     default: return cudaErrorInvalidValue;
   }
 }

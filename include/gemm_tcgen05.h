@@ -88,14 +88,20 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
                    int out_dtype, int layout, void* stream);
 
 /* Tile-configuration override for sweeps.  Zero fields mean "choose
- * automatically".  bn: output columns per CTA tile (64, 128 or 256; rows are
- * always 128).  group_m: tile-rows per group of the grouped tile order (>= 1).
- * grid: number of persistent CTAs (<= number of tiles). */
+ * automatically".
+ *   bn        output columns per tile: 64, 128 or 256 for single-CTA tiles
+ *             (128 rows); 128 or 256 for CTA-pair tiles (256 rows).
+ *   group_m   tile-rows per group of the grouped tile order (>= 1).
+ *   grid      number of persistent CTAs (clamped to the work available; even in
+ *             pair mode).
+ *   cta_group 1: one CTA per tile (tcgen05 cta_group::1); 2: a cluster of two
+ *             CTAs per 256-row tile, one MMA spanning both SMs (cta_group::2),
+ *             each SM loading its own half of A and of B. */
 typedef struct {
   int32_t bn;
   int32_t group_m;
   int32_t grid;
-  int32_t reserved;
+  int32_t cta_group;
 } gemm_config_t;
 
 /* gemm with an explicit configuration (cfg may be NULL = gemm()).  Same
@@ -146,10 +152,11 @@ void gemm_debug_set(uint64_t wait_timeout_ns, int32_t inject_skip);
  * num_sms is the SM count to plan for.  Returns the same argument errors as
  * gemm() for the size/dtype/layout arguments. */
 typedef struct {
-  int32_t bm, bn, bk, stages;
+  int32_t bm, bn, bk, stages;             /* bm: rows per tile (128, or 256 for a pair) */
   int32_t m_tiles, n_tiles, k_blocks, num_tiles;
   int32_t grid, group_m, threads, smem_bytes;
   int32_t tmem_cols, a_mn, b_mn, epi_chunk_cols;
+  int32_t cta_group, reserved;
 } gemm_plan_t;
 
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int layout,

@@ -36,25 +36,30 @@ def _lib():
 # wrong shared-memory descriptor, swizzle, TMEM lane/column map or operand major
 # shows up as a misplaced value (checked by exact equality).
 
+MODES = [{"cta_group": 1}, {"cta_group": 2}]
+
+
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
 @pytest.mark.parametrize("in_dtype", ["f16", "bf16"])
-def test_probe_identity_left(a_col, b_col, in_dtype):
-    M, N, K = 128, 256, 128
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_probe_identity_left(a_col, b_col, in_dtype, cta_group):
+    M, N, K = 128 * cta_group, 256, 256
     eye = si.to_bits(np.eye(M, K, dtype=np.float32), in_dtype)
     A = np.ascontiguousarray(eye.T) if a_col else eye
     Bv = si.normal(77, K * N, 1.0).reshape(K, N)
     Bl = si.to_bits(Bv, in_dtype)
     B = np.ascontiguousarray(Bl.T) if b_col else Bl
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype=in_dtype, out_dtype="f32",
-                         a_col=a_col, b_col=b_col, cfg={"bn": 256})
+                         a_col=a_col, b_col=b_col, cfg={"bn": 256, "cta_group": cta_group})
     np.testing.assert_array_equal(oracle.decode(out, "f32"), oracle.decode(Bl, in_dtype)[:M])
 
 
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
-@pytest.mark.parametrize("bn", [64, 128, 256])
-def test_probe_permutations(a_col, b_col, bn):
-    """A = P (row permutation), B = Q^T-like column permutation of unique values."""
-    M, N, K = 128, bn, 64
+@pytest.mark.parametrize("bn,cta_group", [(64, 1), (128, 1), (256, 1), (128, 2), (256, 2)])
+def test_probe_permutations(a_col, b_col, bn, cta_group):
+    """A = P (rows pick unique-valued rows of B): every output is one exact product,
+    so a misplaced operand row/column or accumulator lane/column is caught."""
+    M, N, K = 128 * cta_group, bn, 64
     rng = np.random.default_rng(bn + 7 * a_col + 13 * b_col)
     P = np.zeros((M, K), np.float32)
     rows = rng.integers(0, K, size=M)
@@ -65,7 +70,7 @@ def test_probe_permutations(a_col, b_col, bn):
     A = np.ascontiguousarray(Al.T) if a_col else Al
     B = np.ascontiguousarray(Bl.T) if b_col else Bl
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="f16", out_dtype="f32",
-                         a_col=a_col, b_col=b_col, cfg={"bn": bn})
+                         a_col=a_col, b_col=b_col, cfg={"bn": bn, "cta_group": cta_group})
     np.testing.assert_array_equal(oracle.decode(out, "f32"), Bv[rows])
 
 
@@ -92,6 +97,13 @@ def _check_w(w, out, rows=None, exact=False):
 def test_workload_integer_bit_exact_full(cfg):
     w = _workload(cfg, integer=True)
     out, _ = _run_w(w)
+    _check_w(w, out, exact=True)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_workload2_integer_bit_exact_each_mode(mode):
+    w = _workload(2, integer=True)
+    out, _ = _run_w(w, cfg=mode)
     _check_w(w, out, exact=True)
 
 
@@ -137,12 +149,13 @@ ODD_SHAPES = [(257, 263, 251), (31, 29, 37), (17, 65, 19), (73, 61, 67), (1, 1, 
 
 @pytest.mark.parametrize("shape", ODD_SHAPES)
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
-def test_odd_shapes_integer_exact(shape, a_col, b_col):
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_odd_shapes_integer_exact(shape, a_col, b_col, cta_group):
     M, N, K = shape
     A, B = operands(M, N, K, "bf16", a_col, b_col, dist="int", seed=M + N + K, pad=True)
     ldc = pad8(N) + 8
     out, full = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
-                            a_col=a_col, b_col=b_col, ldc=ldc)
+                            a_col=a_col, b_col=b_col, ldc=ldc, cfg={"cta_group": cta_group})
     check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
                          a_col=a_col, b_col=b_col, exact=True)
     # guard columns of C (beyond N) untouched: still the NaN poison
@@ -151,24 +164,27 @@ def test_odd_shapes_integer_exact(shape, a_col, b_col):
 
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("in_dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("bn", [64, 128, 256])
-def test_formats_and_tile_widths(out_dtype, in_dtype, bn):
+@pytest.mark.parametrize("bn,cta_group", [(64, 1), (128, 1), (256, 1), (128, 2), (256, 2)])
+def test_formats_and_tile_widths(out_dtype, in_dtype, bn, cta_group):
     M, N, K = 300, 520, 333
     A, B = operands(M, N, K, in_dtype, False, False, dist="uniform", seed=bn, pad=True)
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype=in_dtype, out_dtype=out_dtype,
-                         a_col=False, b_col=False, cfg={"bn": bn}, ldc=pad8(N))
+                         a_col=False, b_col=False, cfg={"bn": bn, "cta_group": cta_group},
+                         ldc=pad8(N))
     check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype=in_dtype, out_dtype=out_dtype,
                          a_col=False, b_col=False)
 
 
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("alpha,beta", [(1.0, 0.5), (-2.0, 1.0), (0.5, -1.0)])
-def test_alpha_beta(out_dtype, alpha, beta):
-    M, N, K = 256, 384, 192
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_alpha_beta(out_dtype, alpha, beta, cta_group):
+    M, N, K = 512, 384, 192
     A, B = operands(M, N, K, "bf16", False, True, dist="int", seed=3)
     C = si.matrix("int", 3003, M, N, out_dtype)
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype=out_dtype,
-                         a_col=False, b_col=True, alpha=alpha, beta=beta, C=C)
+                         a_col=False, b_col=True, alpha=alpha, beta=beta, C=C,
+                         cfg={"cta_group": cta_group})
     # integer inputs and power-of-two alpha/beta keep alpha*acc + beta*c exact in
     # fp32, so both sides round the same exact value once: bit-exact for every format
     check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype=out_dtype,
@@ -234,14 +250,17 @@ def test_deterministic_bitwise():
     np.testing.assert_array_equal(o1, o2)
 
 
-@pytest.mark.parametrize("grid,group_m", [(1, 1), (7, 3), (152, 16), (300, 2)])
-def test_persistent_grid_and_group_override(grid, group_m):
-    """Every CTA count (one CTA doing every tile, fewer CTAs than tiles) and tile
-    order gives the same exact result."""
+@pytest.mark.parametrize("grid,group_m,cta_group", [(1, 1, 1), (7, 3, 1), (152, 16, 1),
+                                                    (300, 2, 1), (2, 1, 2), (6, 3, 2),
+                                                    (152, 8, 2)])
+def test_persistent_grid_and_group_override(grid, group_m, cta_group):
+    """Every CTA count (one CTA or one pair doing every tile, fewer CTAs than
+    tiles) and tile order gives the same exact result."""
     M, N, K = 640, 768, 320
     A, B = operands(M, N, K, "bf16", False, True, dist="int", seed=grid)
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32", a_col=False,
-                         b_col=True, cfg={"bn": 128, "grid": grid, "group_m": group_m})
+                         b_col=True, cfg={"bn": 128, "grid": grid, "group_m": group_m,
+                                          "cta_group": cta_group})
     check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
                          a_col=False, b_col=True, exact=True)
 
@@ -283,25 +302,26 @@ def test_device_checks_on_gpu(_lib):
 
 # ------------------------------------------------------------ bounded waits
 
-def test_wait_timeout_is_reported_and_context_survives(_lib):
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_wait_timeout_is_reported_and_context_survives(_lib, cta_group):
     """The producer leaves one ring slot unarmed (host-set debug flag): the MMA
     issuer's wait must run out, the kernel must record the timeout and return,
     and the device must stay usable."""
     g = _lib
-    M, N, K = 256, 256, 512
+    M, N, K = 512, 256, 512
     A, B = operands(M, N, K, "bf16", False, False, dist="int", seed=5)
     try:
         g.gemm_debug_set(50_000_000, 3)   # 50 ms limit; skip ring iteration 2
         dA = to_device(A, "bf16")
         dB = to_device(B, "bf16")
         c = torch.zeros(M, N, device="cuda", dtype=torch.float32)
-        g.matmul(dA, dB, c)
+        g.matmul(dA, dB, c, cfg={"cta_group": cta_group})
         s, site = g.gemm_sync_status(torch.cuda.current_stream().cuda_stream)
         assert s == g.GEMM_ERR_TIMEOUT
         assert site in (2, 3, 4, 1)
     finally:
         g.gemm_debug_set(0, 0)
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32", a_col=False,
-                         b_col=False)
+                         b_col=False, cfg={"cta_group": cta_group})
     check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
                          a_col=False, b_col=False, exact=True)

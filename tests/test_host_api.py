@@ -110,12 +110,15 @@ def test_no_cpu_fallback_without_device(g):
 
 
 @pytest.mark.parametrize("shape,layout,expect", [
-    ((2048, 2048, 2048, 0, 2), 0, dict(bn=256, num_tiles=128, grid=128, k_blocks=32, b_mn=1)),
-    ((4096, 4096, 4096, 1, 1), 0, dict(bn=256, num_tiles=512, grid=152, k_blocks=64)),
-    ((8192, 8192, 8192, 1, 2), 2, dict(bn=256, num_tiles=2048, grid=152, b_mn=0)),
-    ((128, 8192, 8192, 1, 1), 2, dict(bn=64, num_tiles=128, grid=128, k_blocks=128)),
-    ((512, 512, 512, 0, 2), 0, dict(bn=64, num_tiles=32, grid=32)),
-    ((257, 263, 251, 1, 2), 3, dict(m_tiles=3, k_blocks=4, a_mn=1, b_mn=0)),
+    # big squares: CTA-pair tiles of 256 x 256 (one cta_group::2 MMA over two SMs)
+    ((2048, 2048, 2048, 0, 2), 0, dict(cta_group=2, bm=256, bn=256, num_tiles=64, grid=128,
+                                       k_blocks=32, b_mn=1, stages=6)),
+    ((4096, 4096, 4096, 1, 1), 0, dict(cta_group=2, bn=256, num_tiles=256, grid=152)),
+    ((8192, 8192, 8192, 1, 2), 2, dict(cta_group=2, bn=256, num_tiles=1024, grid=152, b_mn=0)),
+    # a single 128-row panel: single-CTA 128 x 64 tiles
+    ((128, 8192, 8192, 1, 1), 2, dict(cta_group=1, bm=128, bn=64, num_tiles=128, grid=128,
+                                      k_blocks=128, stages=8)),
+    ((257, 263, 251, 1, 2), 3, dict(m_tiles=2, k_blocks=4, a_mn=1, b_mn=0)),
 ])
 def test_plan(g, shape, layout, expect):
     M, N, K, din, dout = shape
@@ -126,13 +129,30 @@ def test_plan(g, shape, layout, expect):
         assert d[k] == v, (k, d)
     assert d["smem_bytes"] <= 232448
     assert d["tmem_cols"] in (128, 256, 512)
-    assert d["stages"] * (128 * 64 * 2 + d["bn"] * 64 * 2) <= 192 * 1024
+    b_cols = d["bn"] // d["cta_group"]
+    assert d["stages"] * (128 * 64 * 2 + b_cols * 64 * 2) <= 192 * 1024
+    assert d["grid"] % d["cta_group"] == 0
+
+
+def test_plan_prefers_pairs_only_with_more_than_one_panel(g):
+    for M in (1, 64, 128):
+        s, p = g.gemm_plan(M, 4096, 4096, 1, 1, 0, 152)
+        assert s == 0 and p.cta_group == 1
+    s, p = g.gemm_plan(4096, 4096, 4096, 1, 1, 0, 152, {"cta_group": 1})
+    assert s == 0 and p.cta_group == 1 and p.bm == 128 and p.num_tiles == 512
+    s, p = g.gemm_plan(512, 512, 512, 0, 2, 0, 152, {"cta_group": 2, "bn": 128})
+    assert s == 0 and (p.cta_group, p.bm, p.bn, p.num_tiles, p.grid) == (2, 256, 128, 8, 16)
 
 
 def test_plan_overrides_and_errors(g):
-    s, p = g.gemm_plan(1024, 1024, 1024, 0, 2, 0, 152, {"bn": 128, "group_m": 3, "grid": 10})
-    assert s == 0 and (p.bn, p.group_m, p.grid) == (128, 3, 10)
+    s, p = g.gemm_plan(1024, 1024, 1024, 0, 2, 0, 152, {"bn": 128, "group_m": 3, "grid": 10,
+                                                         "cta_group": 1})
+    assert s == 0 and (p.bn, p.group_m, p.grid, p.cta_group) == (128, 3, 10, 1)
     s, _ = g.gemm_plan(1024, 1024, 1024, 0, 2, 0, 152, {"bn": 96})
+    assert s == g.GEMM_ERR_INVALID_ARG
+    s, _ = g.gemm_plan(1024, 1024, 1024, 0, 2, 0, 152, {"bn": 64, "cta_group": 2})
+    assert s == g.GEMM_ERR_INVALID_ARG
+    s, _ = g.gemm_plan(1024, 1024, 1024, 0, 2, 0, 152, {"cta_group": 3})
     assert s == g.GEMM_ERR_INVALID_ARG
     s, _ = g.gemm_plan(1024, 1024, 1024, 0, 2, 0, 0)
     assert s == g.GEMM_ERR_INVALID_ARG
