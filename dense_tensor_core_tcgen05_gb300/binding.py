@@ -26,14 +26,15 @@ EXPORTS = ("gemm", "gemm_ex", "gemm_host", "gemm_status_string", "gemm_sync_stat
 
 class gemm_config_t(ctypes.Structure):
     _fields_ = [("bn", ctypes.c_int32), ("group_m", ctypes.c_int32),
-                ("grid", ctypes.c_int32), ("cta_group", ctypes.c_int32)]
+                ("grid", ctypes.c_int32), ("cta_group", ctypes.c_int32),
+                ("split_k", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 class gemm_plan_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "bm", "bn", "bk", "stages", "m_tiles", "n_tiles", "k_blocks", "num_tiles",
         "grid", "group_m", "threads", "smem_bytes", "tmem_cols", "a_mn", "b_mn",
-        "epi_chunk_cols", "cta_group", "reserved")]
+        "epi_chunk_cols", "cta_group", "split_k")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -96,8 +97,10 @@ def _cfg(cfg):
         return None
     if isinstance(cfg, gemm_config_t):
         return ctypes.byref(cfg)
-    return ctypes.byref(gemm_config_t(int(cfg.get("bn", 0)), int(cfg.get("group_m", 0)),
-                                      int(cfg.get("grid", 0)), int(cfg.get("cta_group", 0))))
+    c = gemm_config_t()
+    c.bn, c.group_m, c.grid = int(cfg.get("bn", 0)), int(cfg.get("group_m", 0)), int(cfg.get("grid", 0))
+    c.cta_group, c.split_k = int(cfg.get("cta_group", 0)), int(cfg.get("split_k", 0))
+    return ctypes.byref(c)
 
 
 def gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout, stream):

@@ -130,10 +130,11 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // delivery is ~64 B per SM clock, so a k-block costs max(2W, bytes/64) cycles.
 // A launch costs waves * k-block cost (a wave = one unit per SM, or per SM pair),
 // so the choice weighs tile efficiency against wave quantisation.  Pairs need
-// more than 128 rows.  Ties go to the earlier candidate (wider, pair first).
+// more than 128 rows.  Ties go to the earlier candidate (single CTA first, then
+// the wider tile: fewer clusters to launch, fewer tiles to store).
 void choose_unit(int64_t M, int64_t N, int num_sms, int* bn_out, bool* pair_out) {
   struct Cand { int bn; bool pair; };
-  const Cand cands[5] = {{256, true}, {128, true}, {256, false}, {128, false}, {64, false}};
+  const Cand cands[5] = {{256, false}, {128, false}, {64, false}, {256, true}, {128, true}};
   int64_t best_cost = -1;
   *bn_out = 256;
   *pair_out = false;
@@ -154,20 +155,48 @@ void choose_unit(int64_t M, int64_t N, int num_sms, int* bn_out, bool* pair_out)
   }
 }
 
+// Split-K choice for a single 128-row panel (M <= 128), where output tiles alone
+// cannot occupy the GPU: 256-wide tiles (full-rate MMAs) split over a cluster of
+// 4 or 2 CTAs, as long as the clusters fit in one wave and each CTA keeps at
+// least 8 k-blocks.  Returns 1 (no split) otherwise.
+int choose_split(int64_t M, int64_t N, int64_t K, int num_sms, int* bn_out) {
+  if (M > BM) return 1;
+  const int64_t kb = ceil_div(K, BK);
+  const int64_t nt = ceil_div(N, 256);
+  for (int s : {4, 2}) {
+    if (nt * s <= num_sms && kb >= 8 * s && nt * s >= std::min<int64_t>(ceil_div(N, 64), num_sms / 2)) {
+      *bn_out = 256;
+      return s;
+    }
+  }
+  return 1;
+}
+
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layout, int num_sms,
                         const gemm_config_t* cfg, gemm_plan_t* p) {
   if (num_sms <= 0) return GEMM_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
+  if (cfg && (cfg->reserved[0] || cfg->reserved[1] || cfg->reserved[2])) return GEMM_ERR_INVALID_ARG;
   int bn = 0;
   bool pair = false;
   choose_unit(M, N, num_sms, &bn, &pair);
+  int split = choose_split(M, N, K, num_sms, &bn);
+  if (split > 1) pair = false;
   if (cfg && cfg->cta_group) {
     if (cfg->cta_group != 1 && cfg->cta_group != 2) return GEMM_ERR_INVALID_ARG;
     pair = cfg->cta_group == 2;
     if (!cfg->bn) bn = 256;
+    if (pair) split = 1;
+  }
+  if (cfg && cfg->split_k) {
+    if (cfg->split_k < 1) return GEMM_ERR_INVALID_ARG;
+    split = cfg->split_k;
+    if (!cfg->bn) bn = 256;
   }
   if (cfg && cfg->bn) bn = cfg->bn;
   if (pair ? (bn != 128 && bn != 256) : (bn != 64 && bn != 128 && bn != 256))
+    return GEMM_ERR_INVALID_ARG;
+  if (split > 1 && (pair || !split_supported(bn, split) || ceil_div(K, BK) < split))
     return GEMM_ERR_INVALID_ARG;
   const int rows = pair ? 2 * BM : BM;
   p->bm = rows;
@@ -190,7 +219,12 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
   if (grid < 0) return GEMM_ERR_INVALID_ARG;
   if (grid > p->num_tiles * per_unit) grid = p->num_tiles * per_unit;
   if (pair) grid = std::max(2, grid & ~1);
+  if (split > 1) {
+    if (int64_t(p->num_tiles) * split >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
+    grid = p->num_tiles * split;   // exactly one tile per split-K cluster
+  }
   p->grid = grid;
+  p->split_k = split;
   p->threads = NUM_THREADS;
   p->smem_bytes = smem_alloc_bytes(bn, pair);
   p->tmem_cols = 2 * bn;
@@ -295,12 +329,16 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.c_ptr = C;
   ka.ldc = ldc;
   ka.n_ragged = ((N * out_size(out_dtype)) % 16) != 0 ? 1 : 0;
+  // An operand every work unit re-reads (the single A panel when there is one
+  // row of tiles, or the single B panel) is kept in L2; the other one streams.
+  ka.a_hint = p.m_tiles == 1 && p.n_tiles > 1 ? 2 : (p.n_tiles == 1 && p.m_tiles > 1 ? 1 : 0);
+  ka.b_hint = p.m_tiles == 1 && p.n_tiles > 1 ? 1 : (p.n_tiles == 1 && p.m_tiles > 1 ? 2 : 0);
 
   cudaError_t e;
   switch (out_dtype) {
-    case GEMM_F32: e = launch_gemm_f32(p.bn, pair, ta, tb, tc, ka, p.grid, stream, dev); break;
-    case GEMM_BF16: e = launch_gemm_bf16(p.bn, pair, ta, tb, tc, ka, p.grid, stream, dev); break;
-    default: e = launch_gemm_f16(p.bn, pair, ta, tb, tc, ka, p.grid, stream, dev); break;
+    case GEMM_F32: e = launch_gemm_f32(p.bn, pair, p.split_k, ta, tb, tc, ka, p.grid, stream, dev); break;
+    case GEMM_BF16: e = launch_gemm_bf16(p.bn, pair, p.split_k, ta, tb, tc, ka, p.grid, stream, dev); break;
+    default: e = launch_gemm_f16(p.bn, pair, p.split_k, ta, tb, tc, ka, p.grid, stream, dev); break;
   }
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -77,6 +77,7 @@ struct KernelArgs {
   void* c_ptr;           // C base (for the ragged right edge, written with plain stores)
   long long ldc;         // C leading dimension in elements
   int n_ragged;          // 1 when N * sizeof(out) is not a multiple of 16 bytes
+  int a_hint, b_hint;    // L2 policy of the operand loads: 0 default, 1 evict first, 2 evict last
 };
 
 }  // namespace gemm_tc

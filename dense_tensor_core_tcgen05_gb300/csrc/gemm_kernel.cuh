@@ -177,7 +177,141 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, int out_kind) {
   return __half22float2(h);
 }
 
-template <int BN, int STAGES, int OUT, bool PAIR>
+// One 16-byte piece of an output row: x holds its accumulator values (4 for
+// fp32 output, 8 for 16-bit output, alpha not yet applied).  Applies
+// alpha*acc + beta*c (c read from the staged C chunk at p when read_c), casts,
+// and either writes the piece to the swizzled staging buffer (p) or, for a
+// chunk crossing the ragged right edge of C, stores its in-range elements
+// straight to global memory.
+template <int OUT>
+__device__ __forceinline__ void finish_piece(float* x, uint4* p, const KernelArgs& args,
+                                             bool ragged, bool store_row, int grow, int gcol) {
+  constexpr int E = OUT == OUT_F32 ? 4 : 8;
+#pragma unroll
+  for (int e = 0; e < E; ++e) x[e] *= args.alpha;
+  if (args.read_c) {
+    const uint4 ci = *p;
+    if (OUT == OUT_F32) {
+      x[0] = fmaf(args.beta, __uint_as_float(ci.x), x[0]);
+      x[1] = fmaf(args.beta, __uint_as_float(ci.y), x[1]);
+      x[2] = fmaf(args.beta, __uint_as_float(ci.z), x[2]);
+      x[3] = fmaf(args.beta, __uint_as_float(ci.w), x[3]);
+    } else {
+      const uint32_t cw[4] = {ci.x, ci.y, ci.z, ci.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack2(cw[e], OUT);
+        x[2 * e] = fmaf(args.beta, f.x, x[2 * e]);
+        x[2 * e + 1] = fmaf(args.beta, f.y, x[2 * e + 1]);
+      }
+    }
+  }
+  uint4 o;
+  if (OUT == OUT_F32) {
+    o = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                   __float_as_uint(x[3]));
+  } else {
+    o = make_uint4(pack2(x[0], x[1], OUT), pack2(x[2], x[3], OUT), pack2(x[4], x[5], OUT),
+                   pack2(x[6], x[7], OUT));
+  }
+  if (!ragged) {
+    *p = o;
+  } else if (store_row) {
+    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+    if (OUT == OUT_F32) {
+      float* dst = static_cast<float*>(args.c_ptr) + static_cast<long long>(grow) * args.ldc + gcol;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (gcol + e < args.N) dst[e] = __uint_as_float(ow[e]);
+    } else {
+      uint16_t* dst =
+          static_cast<uint16_t*>(args.c_ptr) + static_cast<long long>(grow) * args.ldc + gcol;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (gcol + e < args.N) dst[e] = static_cast<uint16_t>(ow[e >> 1] >> (16 * (e & 1)));
+    }
+  }
+}
+
+// Epilogue bookkeeping shared by the chunk loops of one epilogue warp.
+struct EpiState {
+  uint8_t* stage0;        // this warp's staging buffers
+  uint64_t* cload;        // this warp's C-load barriers
+  uint32_t chunk_ctr;     // chunks finished so far (alternates the two buffers)
+  int pending_cload;      // buffer with a C load in flight (abort drain), or -1
+  uint32_t pending_phase;
+};
+
+// Prepare the next staging buffer for an output chunk at (row0, col0): wait
+// until the store that last read it has finished, and when beta != 0 fetch the
+// C chunk into it.  Returns false if a wait gave up.
+template <bool CLUSTER, int EPI_BUF_BYTES>
+__device__ __forceinline__ bool begin_chunk(EpiState& st, uint8_t*& stg, const CUtensorMap* tmC,
+                                            int row0, int col0, volatile int* abort_flag,
+                                            const KernelArgs& args) {
+  const int lane = threadIdx.x & 31;
+  const int sbuf = st.chunk_ctr & 1;
+  stg = st.stage0 + sbuf * EPI_BUF_BYTES;
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+  if (args.read_c) {
+    uint64_t* cb = &st.cload[sbuf];
+    const uint32_t cph = (st.chunk_ctr >> 1) & 1;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(cb, EPI_BUF_BYTES);
+      tma_load_2d(stg, tmC, col0, row0, cb);
+    }
+    st.pending_cload = sbuf;
+    st.pending_phase = cph;
+    if (!wait_warp<CLUSTER>(cb, cph, abort_flag, args, SITE_EPI_C_LOAD)) return false;
+    st.pending_cload = -1;
+  }
+  return true;
+}
+
+// Issue the tensor store of a finished chunk (unless it was ragged or entirely
+// outside C) and commit exactly one bulk group per chunk, so that "at most one
+// group still reading" in begin_chunk always means "the other buffer".
+__device__ __forceinline__ void end_chunk(EpiState& st, const uint8_t* stg, const CUtensorMap* tmC,
+                                          int row0, int col0, bool ragged, bool skip_store) {
+  const int lane = threadIdx.x & 31;
+  if (!ragged && !skip_store) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tma_store_2d(tmC, stg, col0, row0);
+  }
+  if (lane == 0) bulk_commit_group();
+  __syncwarp();
+  ++st.chunk_ctr;
+}
+
+// Shared-memory address (this CTA) of 16-byte piece `piece` of row `row` in the
+// fp32 split-K partial buffer (rows of BN floats, pieces XOR-swizzled by row).
+template <int BN>
+__device__ __forceinline__ uint32_t partial_addr(uint32_t base, int row, int piece) {
+  return base + static_cast<uint32_t>(row * (BN * 4) + ((piece ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// PAIR: two CTAs per 256-row tile (cta_group::2).  SPLIT > 1: a cluster of
+// SPLIT CTAs shares one 128-row tile, each accumulating 1/SPLIT of the K range;
+// the partial sums meet in distributed shared memory (split-K without a global
+// workspace; one tile per cluster).
+template <int BN, int STAGES, int OUT, bool PAIR, int SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -186,8 +320,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int CHUNK = OutTraits<OUT>::CHUNK_COLS;
   constexpr int CHUNKS = BN / CHUNK;
   constexpr int TILE_M = PAIR ? 2 * BM : BM;       // rows of one work unit
+  constexpr bool SPLITK = SPLIT > 1;
+  constexpr bool CLUSTERED = PAIR || SPLITK;
+  constexpr int SLICE = BN / SPLIT;                // output columns each split CTA reduces
   static_assert(BN % CHUNK == 0, "tile width must be a whole number of epilogue chunks");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be in [16,256], N%16==0");
+  static_assert(!(PAIR && SPLITK), "pair and split-K modes are exclusive");
+  static_assert(!SPLITK || SLICE % CHUNK == 0, "each split CTA reduces whole epilogue chunks");
+  static_assert(!SPLITK || STAGES * L::STAGE_BYTES >= BM * BN * 4,
+                "the fp32 partial tile must fit in the ring's shared memory");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -208,9 +349,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // "full" and "tmem empty" barriers both CTAs signal; each CTA computes rows
   // [rank * 128, rank * 128 + 128) of the 256-row unit.
   const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+  const uint32_t srank = SPLITK ? cluster_ctarank() : 0;  // K slice of a split-K CTA
   const bool leader = rank == 0;
-  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int unit_stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  constexpr int UNIT_CTAS = PAIR ? 2 : SPLIT;
+  const int unit0 = static_cast<int>(blockIdx.x) / UNIT_CTAS;
+  const int unit_stride = static_cast<int>(gridDim.x) / UNIT_CTAS;
+  const int kb_begin = SPLITK ? (args.k_blocks * static_cast<int>(srank)) / SPLIT : 0;
+  const int kb_end = SPLITK ? (args.k_blocks * static_cast<int>(srank + 1)) / SPLIT : args.k_blocks;
   uint32_t producer_iters = 0;  // ring iterations armed (producer thread only)
 
   if (threadIdx.x == 0) {
@@ -252,12 +397,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------ TMA producer
       uint32_t it = 0;
       bool ok = true;
+      // L2 policies: 0 = default, 1 = evict first (streamed once), 2 = evict last (reused)
+      const uint64_t pol_a = args.a_hint == 1 ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_b = args.b_hint == 1 ? policy_evict_first() : policy_evict_last();
       for (int t = unit0; ok && t < args.num_tiles; t += unit_stride) {
         int mb, nb;
         tile_coord(t, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
         const int a_row = mb * TILE_M + static_cast<int>(rank) * BM;
         const int b_col = nb * BN + static_cast<int>(rank) * L::B_COLS;
-        for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
+        for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!wait_one<PAIR>(&empty[s], ph ^ 1, abort_flag, args, SITE_PRODUCER_EMPTY)) {
@@ -271,24 +419,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* sb = smem + L::off_b + s * L::B_BYTES;
           const int k0 = kb * BK;
           const uint32_t bar_c = PAIR ? map_to_rank(&full[s], 0) : 0;
-          auto load = [&](void* dst, const CUtensorMap* m, int x, int y) {
+          auto load = [&](void* dst, const CUtensorMap* m, int x, int y, int hint, uint64_t pol) {
             if (PAIR)
               tma_load_2d_pair(dst, m, x, y, bar_c);
+            else if (hint)
+              tma_load_2d_hint(dst, m, x, y, &full[s], pol);
             else
               tma_load_2d(dst, m, x, y, &full[s]);
           };
           if (!args.a_mn) {
-            load(sa, &tmA, k0, a_row);
+            load(sa, &tmA, k0, a_row, args.a_hint, pol_a);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / ATOM_MN; ++j) load(sa + j * (BK * SW), &tmA, a_row + j * ATOM_MN, k0);
+            for (int j = 0; j < BM / ATOM_MN; ++j)
+              load(sa + j * (BK * SW), &tmA, a_row + j * ATOM_MN, k0, args.a_hint, pol_a);
           }
           if (!args.b_mn) {
-            load(sb, &tmB, k0, b_col);
+            load(sb, &tmB, k0, b_col, args.b_hint, pol_b);
           } else {
 #pragma unroll
             for (int j = 0; j < L::B_COLS / ATOM_MN; ++j)
-              load(sb + j * (BK * SW), &tmB, b_col + j * ATOM_MN, k0);
+              load(sb + j * (BK * SW), &tmB, b_col + j * ATOM_MN, k0, args.b_hint, pol_b);
           }
         }
       }
@@ -299,6 +450,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------ MMA issuer
       uint32_t it = 0, tl = 0;
       bool ok = true;
+      // MN-major operands: 64-element atoms BK*128 B apart (LBO); K-major: LBO unused
+      const uint32_t a_lbo = args.a_mn ? BK * SW : 16, b_lbo = args.b_mn ? BK * SW : 16;
+      const uint32_t a_step = (args.a_mn ? UMMA_K * SW : UMMA_K * 2) >> 4;
+      const uint32_t b_step = (args.b_mn ? UMMA_K * SW : UMMA_K * 2) >> 4;
       for (int t = unit0; ok && t < args.num_tiles; t += unit_stride, ++tl) {
         const int buf = tl & 1;
         const uint32_t aph = (tl >> 1) & 1;
@@ -308,7 +463,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
+        for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!wait_one<PAIR>(&full[s], ph, abort_flag, args, SITE_MMA_FULL)) {
@@ -318,15 +473,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + L::off_a + s * L::A_BYTES);
           const uint32_t sb = smem_u32(smem + L::off_b + s * L::B_BYTES);
+          // Descriptor of the stage's first K16 slice; later slices only move the
+          // start address (K-major: +32 B inside the swizzled row; MN-major: +16
+          // rows of 128 B), i.e. add a constant to the low field.
+          const uint64_t da0 = make_sdesc_sw128(sa, a_lbo, 8 * SW);
+          const uint64_t db0 = make_sdesc_sw128(sb, b_lbo, 8 * SW);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // K-major: +32 B per K16 step inside the swizzled row.
-            // MN-major: +16 rows of 128 B per K16 step; MN atoms are BK*128 B apart.
-            const uint64_t da = args.a_mn ? make_sdesc_sw128(sa + kk * (UMMA_K * SW), BK * SW, 8 * SW)
-                                          : make_sdesc_sw128(sa + kk * (UMMA_K * 2), 16, 8 * SW);
-            const uint64_t db = args.b_mn ? make_sdesc_sw128(sb + kk * (UMMA_K * SW), BK * SW, 8 * SW)
-                                          : make_sdesc_sw128(sb + kk * (UMMA_K * 2), 16, 8 * SW);
-            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+            const uint64_t da = da0 + static_cast<uint64_t>(kk) * a_step;
+            const uint64_t db = db0 + static_cast<uint64_t>(kk) * b_step;
+            const uint32_t acc = (kb != kb_begin || kk != 0) ? 1u : 0u;
             if (PAIR)
               umma_f16_pair(d_tmem, da, db, args.idesc, acc);
             else
@@ -348,10 +504,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // -------------------------------------------------------- epilogue
     const int ew = warp - EPI_WARP0;     // 0..3
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
-    uint8_t* stage0 = smem + L::off_epi + ew * EPI_BUFS * L::EPI_BUF_BYTES;
-    uint32_t tl = 0, chunk_ctr = 0;
-    int pending_cload = -1;              // staging buffer with a C load in flight (abort drain)
-    uint32_t pending_phase = 0;
+    EpiState st{smem + L::off_epi + ew * EPI_BUFS * L::EPI_BUF_BYTES, &cload[ew * EPI_BUFS], 0,
+                -1, 0};
+    uint32_t tl = 0;
     bool ok = true;
     const int r = lane;                  // this thread's row inside the warp's 32-row block
     for (int t = unit0; ok && t < args.num_tiles; t += unit_stride, ++tl) {
@@ -367,28 +522,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
       const int row0 = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32;
+      if (SPLITK) {
+        // Phase 1: this CTA's fp32 partial sum -> its own shared memory (the
+        // ring is idle: every MMA that read it has completed).
+        const uint32_t pbase = smem_u32(smem);
+        const int prow = quarter * 32 + r;
 #pragma unroll 1
-      for (int c = 0; c < CHUNKS; ++c, ++chunk_ctr) {
-        const int sbuf = chunk_ctr & 1;
-        uint8_t* stg = stage0 + sbuf * L::EPI_BUF_BYTES;
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_row, v, c * 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(partial_addr<BN>(pbase, prow, c * 8 + j),
+                         make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        }
+        continue;   // one tile per split-K cluster; phase 2 runs after the cluster barrier
+      }
+#pragma unroll 1
+      for (int c = 0; c < CHUNKS; ++c) {
         const int col0 = nb * BN + c * CHUNK;
-        // the buffer was last read by the store issued two chunks ago
-        if (lane == 0) bulk_wait_group_read<1>();
-        __syncwarp();
-        if (args.read_c) {
-          uint64_t* cb = &cload[ew * EPI_BUFS + sbuf];
-          const uint32_t cph = (chunk_ctr >> 1) & 1;
-          if (lane == 0) {
-            mbar_arrive_expect_tx(cb, L::EPI_BUF_BYTES);
-            tma_load_2d(stg, &tmC, col0, row0, cb);
-          }
-          pending_cload = sbuf;
-          pending_phase = cph;
-          if (!wait_warp<PAIR>(cb, cph, abort_flag, args, SITE_EPI_C_LOAD)) {
-            ok = false;
-            break;
-          }
-          pending_cload = -1;
+        uint8_t* stg;
+        if (!begin_chunk<PAIR, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args)) {
+          ok = false;
+          break;
         }
         // A chunk that crosses the right edge of C when N * sizeof(out) is not a
         // multiple of 16 bytes is written with predicated plain stores: the
@@ -415,78 +572,89 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {   // 16-byte pieces of the 128-byte row
           uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
-          uint4 o;
-          if (OUT == OUT_F32) {
-            const uint32_t* src = v0 + 4 * j;
-            float x[4];
+          constexpr int E = OUT == OUT_F32 ? 4 : 8;
+          float x[E];
+          const uint32_t* src = (OUT == OUT_F32) ? (v0 + 4 * j) : ((j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4)));
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = args.alpha * __uint_as_float(src[e]);
-            if (args.read_c) {
-              const uint4 ci = *p;
-              x[0] = fmaf(args.beta, __uint_as_float(ci.x), x[0]);
-              x[1] = fmaf(args.beta, __uint_as_float(ci.y), x[1]);
-              x[2] = fmaf(args.beta, __uint_as_float(ci.z), x[2]);
-              x[3] = fmaf(args.beta, __uint_as_float(ci.w), x[3]);
-            }
-            o = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
-                           __float_as_uint(x[3]));
-          } else {
-            const uint32_t* src = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = args.alpha * __uint_as_float(src[e]);
-            if (args.read_c) {
-              const uint4 ci = *p;
-              const uint32_t cw[4] = {ci.x, ci.y, ci.z, ci.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 f = unpack2(cw[e], OUT);
-                x[2 * e] = fmaf(args.beta, f.x, x[2 * e]);
-                x[2 * e + 1] = fmaf(args.beta, f.y, x[2 * e + 1]);
-              }
-            }
-            o = make_uint4(pack2(x[0], x[1], OUT), pack2(x[2], x[3], OUT), pack2(x[4], x[5], OUT),
-                           pack2(x[6], x[7], OUT));
-          }
-          if (!ragged) {
-            *p = o;
-          } else if (!skip_store && row0 + r < args.M) {
-            const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
-            if (OUT == OUT_F32) {
-              float* dst = static_cast<float*>(args.c_ptr) +
-                           static_cast<long long>(row0 + r) * args.ldc + col0 + 4 * j;
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (col0 + 4 * j + e < args.N) dst[e] = __uint_as_float(ow[e]);
-            } else {
-              uint16_t* dst = static_cast<uint16_t*>(args.c_ptr) +
-                              static_cast<long long>(row0 + r) * args.ldc + col0 + 8 * j;
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                if (col0 + 8 * j + e < args.N)
-                  dst[e] = static_cast<uint16_t>(ow[e >> 1] >> (16 * (e & 1)));
-            }
-          }
+          for (int e = 0; e < E; ++e) x[e] = __uint_as_float(src[e]);
+          finish_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
+                            col0 + E * j);
         }
-        if (!ragged && !skip_store) {
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) tma_store_2d(&tmC, stg, col0, row0);
-        }
-        // exactly one bulk group per chunk (empty when nothing was stored), so
-        // "at most one group still reading" above always means "the other buffer"
-        if (lane == 0) bulk_commit_group();
-        __syncwarp();
+        end_chunk(st, stg, &tmC, row0, col0, ragged, skip_store);
       }
     }
-    if (!ok && pending_cload >= 0 && lane == 0)
-      wait_drain<PAIR>(&cload[ew * EPI_BUFS + pending_cload], pending_phase, args);
-    if (lane == 0) bulk_wait_group<0>();
-    __syncwarp();
+    if (!SPLITK) {
+      if (!ok && st.pending_cload >= 0 && lane == 0)
+        wait_drain<PAIR>(&st.cload[st.pending_cload], st.pending_phase, args);
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (SPLITK) {
+    // Phase 2: every partial is in its CTA's shared memory.  CTA `srank` sums
+    // columns [srank*SLICE, (srank+1)*SLICE) of the tile over the SPLIT partials
+    // in rank order (deterministic), then finishes them like the plain epilogue.
+    cluster_sync();
+    if (warp >= EPI_WARP0 && !*abort_flag && unit0 < args.num_tiles) {
+      const int ew = warp - EPI_WARP0;
+      const int quarter = warp & 3;
+      const int r = lane;
+      EpiState st{smem + L::off_epi + ew * EPI_BUFS * L::EPI_BUF_BYTES, &cload[ew * EPI_BUFS], 0,
+                  -1, 0};
+      int mb, nb;
+      tile_coord(unit0, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
+      const int row0 = mb * BM + quarter * 32;
+      const int prow = quarter * 32 + r;
+      const uint32_t pbase = smem_u32(smem);
+      bool ok = true;
+#pragma unroll 1
+      for (int c = 0; ok && c < SLICE / CHUNK; ++c) {
+        const int tcol = static_cast<int>(srank) * SLICE + c * CHUNK;   // column inside the tile
+        const int col0 = nb * BN + tcol;
+        uint8_t* stg;
+        if (!begin_chunk<true, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args)) {
+          ok = false;
+          break;
+        }
+        const bool ragged = args.n_ragged && (col0 + CHUNK > args.N);
+        const bool skip_store = col0 >= args.N || row0 >= args.M;
+        uint8_t* rowp = stg + r * SW;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          constexpr int E = OUT == OUT_F32 ? 4 : 8;
+          float x[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) x[e] = 0.0f;
+          const int piece0 = (tcol + E * j) / 4;       // first fp32 piece of the partial row
+#pragma unroll
+          for (int q = 0; q < SPLIT; ++q) {
+#pragma unroll
+            for (int h = 0; h < E / 4; ++h) {
+              const uint32_t local = partial_addr<BN>(pbase, prow, piece0 + h);
+              const uint4 pv = ld_shared_cluster_v4(map_addr_to_rank(local, q));
+              x[4 * h + 0] += __uint_as_float(pv.x);
+              x[4 * h + 1] += __uint_as_float(pv.y);
+              x[4 * h + 2] += __uint_as_float(pv.z);
+              x[4 * h + 3] += __uint_as_float(pv.w);
+            }
+          }
+          uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
+          finish_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
+                            col0 + E * j);
+        }
+        end_chunk(st, stg, &tmC, row0, col0, ragged, skip_store);
+      }
+      if (!ok && st.pending_cload >= 0 && lane == 0)
+        wait_drain<true>(&st.cload[st.pending_cload], st.pending_phase, args);
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (*abort_flag) {
     // Some role gave up.  Before TMEM is freed and the CTA exits, every
     // asynchronous operation this CTA started must have finished:
@@ -518,9 +686,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       wait_drain<PAIR>(drain, 0, args);
     }
   }
-  if (PAIR) {
-    // neither CTA may free TMEM or exit while its peer can still signal its
-    // barriers or read its shared memory
+  if (CLUSTERED) {
+    // no CTA may free TMEM or exit while a peer can still signal its barriers
+    // or read its shared memory
     tc_fence_before();
     cluster_sync();
   }

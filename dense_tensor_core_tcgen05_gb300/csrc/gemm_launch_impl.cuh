@@ -8,12 +8,12 @@ namespace gemm_tc {
 namespace {
 constexpr int kMaxDevices = 64;
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int SPLIT>
 cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                         const KernelArgs& args, int grid, cudaStream_t stream, int dev) {
   constexpr int ST = stages_for(BN, PAIR);
   using L = SmemLayout<BN, ST, PAIR>;
-  auto kern = gemm_tcgen05_kernel<BN, ST, GEMM_OUT_KIND, PAIR>;
+  auto kern = gemm_tcgen05_kernel<BN, ST, GEMM_OUT_KIND, PAIR, SPLIT>;
   static volatile bool attr_set[kMaxDevices] = {};
   static volatile int max_clusters[kMaxDevices] = {};
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
@@ -27,7 +27,15 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = L::ALLOC;
   cfg.stream = stream;
-  if (PAIR) {
+  if (SPLIT > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = SPLIT;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (grid % SPLIT != 0) return cudaErrorInvalidConfiguration;
+  } else if (PAIR) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
@@ -53,20 +61,27 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 }
 }  // namespace
 
-cudaError_t GEMM_LAUNCH_NAME(int bn, bool pair, const CUtensorMap& a, const CUtensorMap& b,
-                             const CUtensorMap& c, const KernelArgs& args, int grid,
-                             cudaStream_t stream, int dev) {
+cudaError_t GEMM_LAUNCH_NAME(int bn, bool pair, int split, const CUtensorMap& a,
+                             const CUtensorMap& b, const CUtensorMap& c, const KernelArgs& args,
+                             int grid, cudaStream_t stream, int dev) {
+  if (split > 1) {
+    if (pair) return cudaErrorInvalidValue;
+    if (bn == 256 && split == 2) return launch_inst<256, false, 2>(a, b, c, args, grid, stream, dev);
+    if (bn == 256 && split == 4) return launch_inst<256, false, 4>(a, b, c, args, grid, stream, dev);
+    if (bn == 128 && split == 2) return launch_inst<128, false, 2>(a, b, c, args, grid, stream, dev);
+    return cudaErrorInvalidValue;
+  }
   if (pair) {
     switch (bn) {
-      case 128: return launch_inst<128, true>(a, b, c, args, grid, stream, dev);
-      case 256: return launch_inst<256, true>(a, b, c, args, grid, stream, dev);
+      case 128: return launch_inst<128, true, 1>(a, b, c, args, grid, stream, dev);
+      case 256: return launch_inst<256, true, 1>(a, b, c, args, grid, stream, dev);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (bn) {
-    case 64: return launch_inst<64, false>(a, b, c, args, grid, stream, dev);
-    case 128: return launch_inst<128, false>(a, b, c, args, grid, stream, dev);
-    case 256: return launch_inst<256, false>(a, b, c, args, grid, stream, dev);
+    case 64: return launch_inst<64, false, 1>(a, b, c, args, grid, stream, dev);
+    case 128: return launch_inst<128, false, 1>(a, b, c, args, grid, stream, dev);
+    case 256: return launch_inst<256, false, 1>(a, b, c, args, grid, stream, dev);
     default: return cudaErrorInvalidValue;
   }
 }

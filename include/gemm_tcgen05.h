@@ -96,12 +96,19 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *             pair mode).
  *   cta_group 1: one CTA per tile (tcgen05 cta_group::1); 2: a cluster of two
  *             CTAs per 256-row tile, one MMA spanning both SMs (cta_group::2),
- *             each SM loading its own half of A and of B. */
+ *             each SM loading its own half of A and of B.
+ *   split_k   1: no split; 2 or 4: a cluster of that many CTAs shares each
+ *             128-row tile, each accumulating 1/split_k of K, the partial sums
+ *             reduced in distributed shared memory in a fixed order (needs
+ *             cta_group 1; supported for bn 256 with split_k 2 or 4 and bn 128
+ *             with split_k 2; one tile per cluster, so grid is ignored). */
 typedef struct {
   int32_t bn;
   int32_t group_m;
   int32_t grid;
   int32_t cta_group;
+  int32_t split_k;
+  int32_t reserved[3];  /* must be zero */
 } gemm_config_t;
 
 /* gemm with an explicit configuration (cfg may be NULL = gemm()).  Same
@@ -156,7 +163,7 @@ typedef struct {
   int32_t m_tiles, n_tiles, k_blocks, num_tiles;
   int32_t grid, group_m, threads, smem_bytes;
   int32_t tmem_cols, a_mn, b_mn, epi_chunk_cols;
-  int32_t cta_group, reserved;
+  int32_t cta_group, split_k;
 } gemm_plan_t;
 
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int layout,

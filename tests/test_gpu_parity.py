@@ -37,29 +37,42 @@ def _lib():
 # shows up as a misplaced value (checked by exact equality).
 
 MODES = [{"cta_group": 1}, {"cta_group": 2}]
+# every way the kernel can split the work: single CTA, CTA pair, split-K clusters
+ALL_MODES = [{"cta_group": 1}, {"cta_group": 2}, {"split_k": 2}, {"split_k": 4}]
+MODE_IDS = ["cta1", "pair", "splitk2", "splitk4"]
+
+
+def _mode_fits(mode, K):
+    return (K + 63) // 64 >= mode.get("split_k", 1)
 
 
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
 @pytest.mark.parametrize("in_dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("cta_group", [1, 2])
-def test_probe_identity_left(a_col, b_col, in_dtype, cta_group):
-    M, N, K = 128 * cta_group, 256, 256
+@pytest.mark.parametrize("mode", ALL_MODES, ids=MODE_IDS)
+def test_probe_identity_left(a_col, b_col, in_dtype, mode):
+    M, N, K = 128 * mode.get("cta_group", 1), 256, 256
     eye = si.to_bits(np.eye(M, K, dtype=np.float32), in_dtype)
     A = np.ascontiguousarray(eye.T) if a_col else eye
     Bv = si.normal(77, K * N, 1.0).reshape(K, N)
     Bl = si.to_bits(Bv, in_dtype)
     B = np.ascontiguousarray(Bl.T) if b_col else Bl
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype=in_dtype, out_dtype="f32",
-                         a_col=a_col, b_col=b_col, cfg={"bn": 256, "cta_group": cta_group})
+                         a_col=a_col, b_col=b_col, cfg=dict(mode, bn=256))
     np.testing.assert_array_equal(oracle.decode(out, "f32"), oracle.decode(Bl, in_dtype)[:M])
 
 
+PROBE_CFGS = [{"bn": 64}, {"bn": 128}, {"bn": 256}, {"bn": 128, "cta_group": 2},
+              {"bn": 256, "cta_group": 2}, {"bn": 128, "split_k": 2}, {"bn": 256, "split_k": 2},
+              {"bn": 256, "split_k": 4}]
+
+
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
-@pytest.mark.parametrize("bn,cta_group", [(64, 1), (128, 1), (256, 1), (128, 2), (256, 2)])
-def test_probe_permutations(a_col, b_col, bn, cta_group):
+@pytest.mark.parametrize("cfg", PROBE_CFGS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_probe_permutations(a_col, b_col, cfg):
     """A = P (rows pick unique-valued rows of B): every output is one exact product,
     so a misplaced operand row/column or accumulator lane/column is caught."""
-    M, N, K = 128 * cta_group, bn, 64
+    bn, cta_group = cfg["bn"], cfg.get("cta_group", 1)
+    M, N, K = 128 * cta_group, bn, 64 * cfg.get("split_k", 1)
     rng = np.random.default_rng(bn + 7 * a_col + 13 * b_col)
     P = np.zeros((M, K), np.float32)
     rows = rng.integers(0, K, size=M)
@@ -70,7 +83,7 @@ def test_probe_permutations(a_col, b_col, bn, cta_group):
     A = np.ascontiguousarray(Al.T) if a_col else Al
     B = np.ascontiguousarray(Bl.T) if b_col else Bl
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="f16", out_dtype="f32",
-                         a_col=a_col, b_col=b_col, cfg={"bn": bn, "cta_group": cta_group})
+                         a_col=a_col, b_col=b_col, cfg=cfg)
     np.testing.assert_array_equal(oracle.decode(out, "f32"), Bv[rows])
 
 
@@ -100,9 +113,18 @@ def test_workload_integer_bit_exact_full(cfg):
     _check_w(w, out, exact=True)
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", ALL_MODES, ids=MODE_IDS)
 def test_workload2_integer_bit_exact_each_mode(mode):
     w = _workload(2, integer=True)
+    out, _ = _run_w(w, cfg=mode)
+    _check_w(w, out, exact=True)
+
+
+@pytest.mark.parametrize("mode", [{"cta_group": 1, "bn": 64}, {"split_k": 2}, {"split_k": 4},
+                                  {"split_k": 2, "bn": 128}],
+                         ids=["bn64", "splitk2", "splitk4", "splitk2-bn128"])
+def test_workload5_skinny_integer_each_mode(mode):
+    w = _workload(5, integer=True)
     out, _ = _run_w(w, cfg=mode)
     _check_w(w, out, exact=True)
 
@@ -149,13 +171,15 @@ ODD_SHAPES = [(257, 263, 251), (31, 29, 37), (17, 65, 19), (73, 61, 67), (1, 1, 
 
 @pytest.mark.parametrize("shape", ODD_SHAPES)
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
-@pytest.mark.parametrize("cta_group", [1, 2])
-def test_odd_shapes_integer_exact(shape, a_col, b_col, cta_group):
+@pytest.mark.parametrize("mode", ALL_MODES, ids=MODE_IDS)
+def test_odd_shapes_integer_exact(shape, a_col, b_col, mode):
     M, N, K = shape
+    if not _mode_fits(mode, K):
+        pytest.skip("fewer k-blocks than splits")
     A, B = operands(M, N, K, "bf16", a_col, b_col, dist="int", seed=M + N + K, pad=True)
     ldc = pad8(N) + 8
     out, full = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
-                            a_col=a_col, b_col=b_col, ldc=ldc, cfg={"cta_group": cta_group})
+                            a_col=a_col, b_col=b_col, ldc=ldc, cfg=mode)
     check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
                          a_col=a_col, b_col=b_col, exact=True)
     # guard columns of C (beyond N) untouched: still the NaN poison
@@ -164,27 +188,25 @@ def test_odd_shapes_integer_exact(shape, a_col, b_col, cta_group):
 
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("in_dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("bn,cta_group", [(64, 1), (128, 1), (256, 1), (128, 2), (256, 2)])
-def test_formats_and_tile_widths(out_dtype, in_dtype, bn, cta_group):
+@pytest.mark.parametrize("cfg", PROBE_CFGS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_formats_and_tile_widths(out_dtype, in_dtype, cfg):
     M, N, K = 300, 520, 333
-    A, B = operands(M, N, K, in_dtype, False, False, dist="uniform", seed=bn, pad=True)
+    A, B = operands(M, N, K, in_dtype, False, False, dist="uniform", seed=cfg["bn"], pad=True)
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype=in_dtype, out_dtype=out_dtype,
-                         a_col=False, b_col=False, cfg={"bn": bn, "cta_group": cta_group},
-                         ldc=pad8(N))
+                         a_col=False, b_col=False, cfg=cfg, ldc=pad8(N))
     check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype=in_dtype, out_dtype=out_dtype,
                          a_col=False, b_col=False)
 
 
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("alpha,beta", [(1.0, 0.5), (-2.0, 1.0), (0.5, -1.0)])
-@pytest.mark.parametrize("cta_group", [1, 2])
-def test_alpha_beta(out_dtype, alpha, beta, cta_group):
-    M, N, K = 512, 384, 192
+@pytest.mark.parametrize("mode", ALL_MODES, ids=MODE_IDS)
+def test_alpha_beta(out_dtype, alpha, beta, mode):
+    M, N, K = 512, 384, 320
     A, B = operands(M, N, K, "bf16", False, True, dist="int", seed=3)
     C = si.matrix("int", 3003, M, N, out_dtype)
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype=out_dtype,
-                         a_col=False, b_col=True, alpha=alpha, beta=beta, C=C,
-                         cfg={"cta_group": cta_group})
+                         a_col=False, b_col=True, alpha=alpha, beta=beta, C=C, cfg=mode)
     # integer inputs and power-of-two alpha/beta keep alpha*acc + beta*c exact in
     # fp32, so both sides round the same exact value once: bit-exact for every format
     check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype=out_dtype,
@@ -302,8 +324,8 @@ def test_device_checks_on_gpu(_lib):
 
 # ------------------------------------------------------------ bounded waits
 
-@pytest.mark.parametrize("cta_group", [1, 2])
-def test_wait_timeout_is_reported_and_context_survives(_lib, cta_group):
+@pytest.mark.parametrize("mode", ALL_MODES, ids=MODE_IDS)
+def test_wait_timeout_is_reported_and_context_survives(_lib, mode):
     """The producer leaves one ring slot unarmed (host-set debug flag): the MMA
     issuer's wait must run out, the kernel must record the timeout and return,
     and the device must stay usable."""
@@ -315,13 +337,13 @@ def test_wait_timeout_is_reported_and_context_survives(_lib, cta_group):
         dA = to_device(A, "bf16")
         dB = to_device(B, "bf16")
         c = torch.zeros(M, N, device="cuda", dtype=torch.float32)
-        g.matmul(dA, dB, c, cfg={"cta_group": cta_group})
+        g.matmul(dA, dB, c, cfg=mode)
         s, site = g.gemm_sync_status(torch.cuda.current_stream().cuda_stream)
         assert s == g.GEMM_ERR_TIMEOUT
         assert site in (2, 3, 4, 1)
     finally:
         g.gemm_debug_set(0, 0)
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32", a_col=False,
-                         b_col=False, cfg={"cta_group": cta_group})
+                         b_col=False, cfg=mode)
     check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
                          a_col=False, b_col=False, exact=True)

@@ -115,10 +115,13 @@ def test_no_cpu_fallback_without_device(g):
                                        k_blocks=32, b_mn=1, stages=6)),
     ((4096, 4096, 4096, 1, 1), 0, dict(cta_group=2, bn=256, num_tiles=256, grid=152)),
     ((8192, 8192, 8192, 1, 2), 2, dict(cta_group=2, bn=256, num_tiles=1024, grid=152, b_mn=0)),
-    # a single 128-row panel: single-CTA 128 x 64 tiles
-    ((128, 8192, 8192, 1, 1), 2, dict(cta_group=1, bm=128, bn=64, num_tiles=128, grid=128,
-                                      k_blocks=128, stages=8)),
-    ((257, 263, 251, 1, 2), 3, dict(m_tiles=2, k_blocks=4, a_mn=1, b_mn=0)),
+    # a single 128-row panel with long K: 256-wide tiles, K split over 4-CTA clusters
+    ((128, 8192, 8192, 1, 1), 2, dict(cta_group=1, bm=128, bn=256, num_tiles=32, grid=128,
+                                      k_blocks=128, stages=4, split_k=4)),
+    # a single panel with short K: no split (too few k-blocks per CTA)
+    ((128, 8192, 256, 1, 1), 2, dict(cta_group=1, split_k=1)),
+    ((257, 263, 251, 1, 2), 3, dict(cta_group=1, m_tiles=3, k_blocks=4, a_mn=1, b_mn=0)),
+    ((512, 512, 512, 0, 2), 0, dict(cta_group=1, bn=64, num_tiles=32, grid=32)),
 ])
 def test_plan(g, shape, layout, expect):
     M, N, K, din, dout = shape
@@ -142,6 +145,25 @@ def test_plan_prefers_pairs_only_with_more_than_one_panel(g):
     assert s == 0 and p.cta_group == 1 and p.bm == 128 and p.num_tiles == 512
     s, p = g.gemm_plan(512, 512, 512, 0, 2, 0, 152, {"cta_group": 2, "bn": 128})
     assert s == 0 and (p.cta_group, p.bm, p.bn, p.num_tiles, p.grid) == (2, 256, 128, 8, 16)
+
+
+def test_plan_split_k_overrides(g):
+    s, p = g.gemm_plan(128, 4096, 4096, 1, 1, 2, 152, {"split_k": 2})
+    assert s == 0 and (p.split_k, p.bn, p.grid, p.num_tiles) == (2, 256, 32, 16)
+    s, p = g.gemm_plan(128, 4096, 4096, 1, 1, 2, 152, {"split_k": 2, "bn": 128})
+    assert s == 0 and (p.split_k, p.bn, p.grid) == (2, 128, 64)
+    for bad in ({"split_k": 3}, {"split_k": 4, "bn": 128}, {"split_k": 2, "cta_group": 2},
+                {"split_k": 2, "bn": 64}):
+        assert g.gemm_plan(256, 4096, 4096, 1, 1, 2, 152, bad)[0] == g.GEMM_ERR_INVALID_ARG, bad
+    # fewer k-blocks than splits
+    assert g.gemm_plan(128, 4096, 128, 1, 1, 2, 152, {"split_k": 4})[0] == g.GEMM_ERR_INVALID_ARG
+    # reserved fields must be zero
+    import ctypes
+    cfg = g.gemm_config_t()
+    cfg.reserved[1] = 7
+    p = g.gemm_plan_t()
+    lib = g.library()
+    assert lib.gemm_plan(256, 256, 256, 1, 1, 0, 152, ctypes.byref(cfg), ctypes.byref(p)) == 1
 
 
 def test_plan_overrides_and_errors(g):
