@@ -192,6 +192,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
     if (cfg->split_k < 1) return GEMM_ERR_INVALID_ARG;
     split = cfg->split_k;
     if (!cfg->bn) bn = 256;
+    if (split > 1 && !cfg->cta_group) pair = false;   // split-K clusters are single-CTA tiles
   }
   if (cfg && cfg->bn) bn = cfg->bn;
   if (pair ? (bn != 128 && bn != 256) : (bn != 64 && bn != 128 && bn != 256))
