@@ -182,11 +182,12 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
   choose_unit(M, N, num_sms, &bn, &pair);
   int split = choose_split(M, N, K, num_sms, &bn);
   if (split > 1) pair = false;
+  // a manual tile setting without an explicit split_k turns the automatic split off
+  if (cfg && (cfg->cta_group || cfg->bn) && !cfg->split_k) split = 1;
   if (cfg && cfg->cta_group) {
     if (cfg->cta_group != 1 && cfg->cta_group != 2) return GEMM_ERR_INVALID_ARG;
     pair = cfg->cta_group == 2;
     if (!cfg->bn) bn = 256;
-    if (pair) split = 1;
   }
   if (cfg && cfg->split_k) {
     if (cfg->split_k < 1) return GEMM_ERR_INVALID_ARG;

@@ -155,6 +155,9 @@ def test_plan_split_k_overrides(g):
     for bad in ({"split_k": 3}, {"split_k": 4, "bn": 128}, {"split_k": 2, "cta_group": 2},
                 {"split_k": 2, "bn": 64}):
         assert g.gemm_plan(256, 4096, 4096, 1, 1, 2, 152, bad)[0] == g.GEMM_ERR_INVALID_ARG, bad
+    # a manual tile setting turns the automatic split off
+    s, p = g.gemm_plan(128, 8192, 8192, 1, 1, 2, 152, {"cta_group": 1, "bn": 64})
+    assert s == 0 and (p.split_k, p.bn, p.num_tiles) == (1, 64, 128)
     # an explicit split overrides an automatic pair choice
     s, p = g.gemm_plan(4096, 4096, 4096, 1, 1, 2, 152, {"split_k": 2})
     assert s == 0 and (p.cta_group, p.split_k, p.bm) == (1, 2, 128)
