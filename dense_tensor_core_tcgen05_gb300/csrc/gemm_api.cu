@@ -203,7 +203,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
   const int rows = pair ? 2 * BM : BM;
   p->bm = rows;
   p->bn = bn;
-  p->bk = BK;
+  p->bk = BK * ko_for(bn, pair);   // K per ring stage
   p->stages = stages_for(bn, pair);
   const int64_t mt = ceil_div(M, rows), nt = ceil_div(N, bn), kb = ceil_div(K, BK);
   if (mt * nt >= (int64_t(1) << 30)) return GEMM_ERR_UNSUPPORTED;
@@ -246,6 +246,24 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t elem_strides[2] = {1, 1};
   CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D operand map: (64 elements, `d1` rows, `d2` whole 64-element blocks), the
+// blocks 128 B apart along the row, so one box {64, box1, box2} covers box2
+// consecutive blocks of each of its rows.  Only whole blocks are mapped: the
+// kernel uses it for copies that stay inside them and the 2-D map otherwise.
+bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d1, uint64_t d2,
+               uint64_t row_bytes, uint32_t box1, uint32_t box2) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, d1, d2};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {64, box1, box2};
+  cuuint32_t elem_strides[3] = {1, 1, 1};
+  CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, elem_strides,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -296,17 +314,34 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   s = make_plan(M, N, K, out_dtype, layout, di->num_sms, cfg, &p);
   if (s != GEMM_OK) return s;
 
-  CUtensorMap ta, tb, tc;
+  OperandMaps mp;
   const bool a_col = (layout & GEMM_A_COL) != 0, b_col = (layout & GEMM_B_COL) != 0;
   const CUtensorMapDataType din = tma_dtype(in_dtype);
-  bool ok = a_col ? encode_2d(&ta, din, A, M, K, lda * 2, ATOM_MN, BK)
-                  : encode_2d(&ta, din, A, K, M, lda * 2, BK, BM);
   const bool pair = p.cta_group == 2;
-  ok = ok && (b_col ? encode_2d(&tb, din, B, K, N, ldb * 2, BK, b_cols_per_cta(p.bn, pair))
-                    : encode_2d(&tb, din, B, N, K, ldb * 2, ATOM_MN, BK));
-  ok = ok && encode_2d(&tc, tma_dtype(out_dtype), C, N, M, ldc * out_size(out_dtype),
+  const int ko = ko_for(p.bn, pair);
+  const int b_cols = b_cols_per_cta(p.bn, pair);
+  bool ok = a_col ? encode_2d(&mp.a, din, A, M, K, lda * 2, ATOM_MN, BK)
+                  : encode_2d(&mp.a, din, A, K, M, lda * 2, BK, BM);
+  ok = ok && (b_col ? encode_2d(&mp.b, din, B, K, N, ldb * 2, BK, b_cols)
+                    : encode_2d(&mp.b, din, B, N, K, ldb * 2, ATOM_MN, BK));
+  ok = ok && encode_2d(&mp.c, tma_dtype(out_dtype), C, N, M, ldc * out_size(out_dtype),
                        p.epi_chunk_cols, EPI_ROWS);
   if (!ok) return GEMM_ERR_CUDA;
+  // 3-D maps over whole 64-element blocks: K-major (A row-major, B column-major)
+  // -> blocks along K; MN-major (A column-major, B row-major) -> 64-wide atoms.
+  const int64_t a_full = a_col ? M / ATOM_MN : K / BK;
+  const int64_t b_full = b_col ? K / BK : N / ATOM_MN;
+  int a_full3d = 0, b_full3d = 0;
+  if (a_full > 0 && (a_col ? encode_3d(&mp.a3, din, A, K, a_full, lda * 2, ko * BK, BM / ATOM_MN)
+                           : encode_3d(&mp.a3, din, A, M, a_full, lda * 2, BM, ko)))
+    a_full3d = static_cast<int>(a_full);
+  else
+    mp.a3 = mp.a;
+  if (b_full > 0 && (b_col ? encode_3d(&mp.b3, din, B, N, b_full, ldb * 2, b_cols, ko)
+                           : encode_3d(&mp.b3, din, B, K, b_full, ldb * 2, ko * BK, b_cols / ATOM_MN)))
+    b_full3d = static_cast<int>(b_full);
+  else
+    mp.b3 = mp.b;
 
   KernelArgs ka;
   std::memset(&ka, 0, sizeof(ka));
@@ -335,12 +370,14 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   // row of tiles, or the single B panel) is kept in L2; the other one streams.
   ka.a_hint = p.m_tiles == 1 && p.n_tiles > 1 ? 2 : (p.n_tiles == 1 && p.m_tiles > 1 ? 1 : 0);
   ka.b_hint = p.m_tiles == 1 && p.n_tiles > 1 ? 1 : (p.n_tiles == 1 && p.m_tiles > 1 ? 2 : 0);
+  ka.a_full3d = a_full3d;
+  ka.b_full3d = b_full3d;
 
   cudaError_t e;
   switch (out_dtype) {
-    case GEMM_F32: e = launch_gemm_f32(p.bn, pair, p.split_k, ta, tb, tc, ka, p.grid, stream, dev); break;
-    case GEMM_BF16: e = launch_gemm_bf16(p.bn, pair, p.split_k, ta, tb, tc, ka, p.grid, stream, dev); break;
-    default: e = launch_gemm_f16(p.bn, pair, p.split_k, ta, tb, tc, ka, p.grid, stream, dev); break;
+    case GEMM_F32: e = launch_gemm_f32(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev); break;
+    case GEMM_BF16: e = launch_gemm_bf16(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev); break;
+    default: e = launch_gemm_f16(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev); break;
   }
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -349,19 +386,22 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
 
 namespace gemm_tc {
 int smem_alloc_bytes(int bn, bool pair) {
+#define GEMM_SMEM(BN_, PAIR_) \
+  SmemLayout<BN_, stages_for(BN_, PAIR_), PAIR_, ko_for(BN_, PAIR_)>::ALLOC
   if (pair) {
     switch (bn) {
-      case 128: return SmemLayout<128, stages_for(128, true), true>::ALLOC;
-      case 256: return SmemLayout<256, stages_for(256, true), true>::ALLOC;
+      case 128: return GEMM_SMEM(128, true);
+      case 256: return GEMM_SMEM(256, true);
       default: return 0;
     }
   }
   switch (bn) {
-    case 64: return SmemLayout<64, stages_for(64, false), false>::ALLOC;
-    case 128: return SmemLayout<128, stages_for(128, false), false>::ALLOC;
-    case 256: return SmemLayout<256, stages_for(256, false), false>::ALLOC;
+    case 64: return GEMM_SMEM(64, false);
+    case 128: return GEMM_SMEM(128, false);
+    case 256: return GEMM_SMEM(256, false);
     default: return 0;
   }
+#undef GEMM_SMEM
 }
 }  // namespace gemm_tc
 

@@ -78,6 +78,9 @@ struct KernelArgs {
   long long ldc;         // C leading dimension in elements
   int n_ragged;          // 1 when N * sizeof(out) is not a multiple of 16 bytes
   int a_hint, b_hint;    // L2 policy of the operand loads: 0 default, 1 evict first, 2 evict last
+  // Extent of the 3-D operand maps in whole 64-element blocks (0: no 3-D map):
+  // K-major operand -> full k-blocks (K / 64); MN-major -> full 64-wide atoms.
+  int a_full3d, b_full3d;
 };
 
 }  // namespace gemm_tc

@@ -52,14 +52,20 @@ enum WaitSite {
   SITE_DRAIN = 6,
 };
 
-// Shared-memory map of one CTA.  In pair mode (two CTAs computing a 256-row
-// tile with one cta_group::2 MMA) each CTA holds its own 128 rows of A and half
-// of the tile's B columns.
-template <int BN, int STAGES, bool PAIR>
+// Shared-memory map of one CTA.  A ring stage holds KO consecutive k-blocks
+// (one TMA copy per operand fetches all of them).  In pair mode (two CTAs
+// computing a 256-row tile with one cta_group::2 MMA) each CTA holds its own
+// 128 rows of A and half of the tile's B columns.
+//   K-major operand tile of a stage:  [KO k-blocks][rows][128 B]
+//   MN-major operand tile of a stage: [64-wide atoms][KO * 64 K-rows][128 B]
+template <int BN, int STAGES, bool PAIR, int KO>
 struct SmemLayout {
   static constexpr int B_COLS = PAIR ? BN / 2 : BN;   // B columns (N) held by this CTA
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = B_COLS * BK * 2;
+  static constexpr int KB_A_BYTES = BM * BK * 2;      // one k-block of A
+  static constexpr int KB_B_BYTES = B_COLS * BK * 2;  // one k-block of B
+  static constexpr int KB_BYTES = KB_A_BYTES + KB_B_BYTES;
+  static constexpr int A_BYTES = KO * KB_A_BYTES;
+  static constexpr int B_BYTES = KO * KB_B_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int EPI_BUF_BYTES = EPI_ROWS * SW;
   static constexpr int off_a = 0;
@@ -77,6 +83,8 @@ struct SmemLayout {
                 "TMEM allocation must be a power of two in [32, 512]");
   static_assert(ALLOC <= 232448, "exceeds the 227 KB per-block shared memory limit");
   static_assert(B_COLS % ATOM_MN == 0, "B half-tiles are whole 64-column swizzle atoms");
+  static_assert(KO >= 1 && KO * BK <= 256, "a stage's K-rows must fit one copy box");
+  static_assert(STAGES >= 2, "the ring needs at least two stages");
 };
 
 __device__ __forceinline__ void record_error(int* status, int code) {
@@ -311,12 +319,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 // SPLIT CTAs shares one 128-row tile, each accumulating 1/SPLIT of the K range;
 // the partial sums meet in distributed shared memory (split-K without a global
 // workspace; one tile per cluster).
-template <int BN, int STAGES, int OUT, bool PAIR, int SPLIT>
+template <int BN, int STAGES, int OUT, bool PAIR, int SPLIT, int KO>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmA3,
+                        const __grid_constant__ CUtensorMap tmB3,
                         const __grid_constant__ CUtensorMap tmC, const KernelArgs args) {
-  using L = SmemLayout<BN, STAGES, PAIR>;
+  using L = SmemLayout<BN, STAGES, PAIR, KO>;
   constexpr int CHUNK = OutTraits<OUT>::CHUNK_COLS;
   constexpr int CHUNKS = BN / CHUNK;
   constexpr int TILE_M = PAIR ? 2 * BM : BM;       // rows of one work unit
@@ -373,6 +383,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_barrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    if (args.a_full3d) prefetch_tensormap(&tmA3);
+    if (args.b_full3d) prefetch_tensormap(&tmB3);
     prefetch_tensormap(&tmC);
   }
   if (warp == 1) {
@@ -405,7 +417,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tile_coord(t, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
         const int a_row = mb * TILE_M + static_cast<int>(rank) * BM;
         const int b_col = nb * BN + static_cast<int>(rank) * L::B_COLS;
-        for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+        for (int kb0 = kb_begin; kb0 < kb_end; kb0 += KO, ++it) {
+          const int nkb = kb_end - kb0 < KO ? kb_end - kb0 : KO;
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!wait_one<PAIR>(&empty[s], ph ^ 1, abort_flag, args, SITE_PRODUCER_EMPTY)) {
@@ -414,12 +427,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (args.inject_skip != 0 && it + 1 == static_cast<uint32_t>(args.inject_skip)) continue;
           // the leader's full[s] counts the bytes of both CTAs of a pair
-          if (leader) mbar_arrive_expect_tx(&full[s], (PAIR ? 2 : 1) * L::STAGE_BYTES);
+          if (leader) mbar_arrive_expect_tx(&full[s], (PAIR ? 2 : 1) * nkb * L::KB_BYTES);
           uint8_t* sa = smem + L::off_a + s * L::A_BYTES;
           uint8_t* sb = smem + L::off_b + s * L::B_BYTES;
-          const int k0 = kb * BK;
           const uint32_t bar_c = PAIR ? map_to_rank(&full[s], 0) : 0;
-          auto load = [&](void* dst, const CUtensorMap* m, int x, int y, int hint, uint64_t pol) {
+          auto load2 = [&](void* dst, const CUtensorMap* m, int x, int y, int hint, uint64_t pol) {
             if (PAIR)
               tma_load_2d_pair(dst, m, x, y, bar_c);
             else if (hint)
@@ -427,20 +439,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else
               tma_load_2d(dst, m, x, y, &full[s]);
           };
-          if (!args.a_mn) {
-            load(sa, &tmA, k0, a_row, args.a_hint, pol_a);
-          } else {
-#pragma unroll
-            for (int j = 0; j < BM / ATOM_MN; ++j)
-              load(sa + j * (BK * SW), &tmA, a_row + j * ATOM_MN, k0, args.a_hint, pol_a);
-          }
-          if (!args.b_mn) {
-            load(sb, &tmB, k0, b_col, args.b_hint, pol_b);
-          } else {
-#pragma unroll
-            for (int j = 0; j < L::B_COLS / ATOM_MN; ++j)
-              load(sb + j * (BK * SW), &tmB, b_col + j * ATOM_MN, k0, args.b_hint, pol_b);
-          }
+          auto load3 = [&](void* dst, const CUtensorMap* m, int y, int z, int hint, uint64_t pol) {
+            if (PAIR)
+              tma_load_3d_pair(dst, m, 0, y, z, bar_c);
+            else if (hint)
+              tma_load_3d_hint(dst, m, 0, y, z, &full[s], pol);
+            else
+              tma_load_3d(dst, m, 0, y, z, &full[s]);
+          };
+          // One operand's share of the stage.  The 3-D map fetches all KO k-blocks
+          // (K-major) or all atoms (MN-major) in one copy; it only covers whole
+          // 64-element blocks, so a group touching a ragged edge takes the 2-D
+          // map, whose out-of-range elements read as zero.
+          auto load_operand = [&](uint8_t* dst, const CUtensorMap* m2, const CUtensorMap* m3,
+                                  int mn, int rows, int row0, int full3d, int hint, uint64_t pol) {
+            if (!mn) {
+              if (nkb == KO && kb0 + KO <= full3d) {
+                load3(dst, m3, row0, kb0, hint, pol);
+              } else {
+                for (int j = 0; j < nkb; ++j) load2(dst + j * rows * SW, m2, (kb0 + j) * BK, row0, hint, pol);
+              }
+            } else {
+              const int atoms = rows / ATOM_MN;
+              if (nkb == KO && row0 / ATOM_MN + atoms <= full3d) {
+                load3(dst, m3, kb0 * BK, row0 / ATOM_MN, hint, pol);
+              } else {
+                for (int a = 0; a < atoms; ++a)
+                  for (int j = 0; j < nkb; ++j)
+                    load2(dst + a * (KO * BK * SW) + j * (BK * SW), m2, row0 + a * ATOM_MN,
+                          (kb0 + j) * BK, hint, pol);
+              }
+            }
+          };
+          load_operand(sa, &tmA, &tmA3, args.a_mn, BM, a_row, args.a_full3d, args.a_hint, pol_a);
+          load_operand(sb, &tmB, &tmB3, args.b_mn, L::B_COLS, b_col, args.b_full3d, args.b_hint,
+                       pol_b);
         }
       }
       producer_iters = it;
@@ -450,8 +483,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------ MMA issuer
       uint32_t it = 0, tl = 0;
       bool ok = true;
-      // MN-major operands: 64-element atoms BK*128 B apart (LBO); K-major: LBO unused
-      const uint32_t a_lbo = args.a_mn ? BK * SW : 16, b_lbo = args.b_mn ? BK * SW : 16;
+      // Per k-block j of a stage: K-major tiles are rows*128 B apart and a K16
+      // slice moves the start address 32 B inside the swizzled row; MN-major
+      // operands step 64 K-rows (8 KB) per k-block and 16 rows (2 KB) per K16
+      // slice, their 64-wide atoms KO*8 KB apart (LBO).
+      const uint32_t a_lbo = args.a_mn ? KO * BK * SW : 16, b_lbo = args.b_mn ? KO * BK * SW : 16;
+      const uint32_t a_kb = args.a_mn ? BK * SW : BM * SW;
+      const uint32_t b_kb = args.b_mn ? BK * SW : L::B_COLS * SW;
       const uint32_t a_step = (args.a_mn ? UMMA_K * SW : UMMA_K * 2) >> 4;
       const uint32_t b_step = (args.b_mn ? UMMA_K * SW : UMMA_K * 2) >> 4;
       for (int t = unit0; ok && t < args.num_tiles; t += unit_stride, ++tl) {
@@ -463,7 +501,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
+        for (int kb0 = kb_begin; kb0 < kb_end; kb0 += KO, ++it) {
+          const int nkb = kb_end - kb0 < KO ? kb_end - kb0 : KO;
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!wait_one<PAIR>(&full[s], ph, abort_flag, args, SITE_MMA_FULL)) {
@@ -473,20 +512,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + L::off_a + s * L::A_BYTES);
           const uint32_t sb = smem_u32(smem + L::off_b + s * L::B_BYTES);
-          // Descriptor of the stage's first K16 slice; later slices only move the
-          // start address (K-major: +32 B inside the swizzled row; MN-major: +16
-          // rows of 128 B), i.e. add a constant to the low field.
-          const uint64_t da0 = make_sdesc_sw128(sa, a_lbo, 8 * SW);
-          const uint64_t db0 = make_sdesc_sw128(sb, b_lbo, 8 * SW);
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            const uint64_t da = da0 + static_cast<uint64_t>(kk) * a_step;
-            const uint64_t db = db0 + static_cast<uint64_t>(kk) * b_step;
-            const uint32_t acc = (kb != kb_begin || kk != 0) ? 1u : 0u;
-            if (PAIR)
-              umma_f16_pair(d_tmem, da, db, args.idesc, acc);
-            else
-              umma_f16(d_tmem, da, db, args.idesc, acc);
+          for (int j = 0; j < KO; ++j) {
+            if (j < nkb) {
+              const uint64_t da0 = make_sdesc_sw128(sa + j * a_kb, a_lbo, 8 * SW);
+              const uint64_t db0 = make_sdesc_sw128(sb + j * b_kb, b_lbo, 8 * SW);
+#pragma unroll
+              for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                const uint64_t da = da0 + static_cast<uint64_t>(kk) * a_step;
+                const uint64_t db = db0 + static_cast<uint64_t>(kk) * b_step;
+                const uint32_t acc = (kb0 != kb_begin || j != 0 || kk != 0) ? 1u : 0u;
+                if (PAIR)
+                  umma_f16_pair(d_tmem, da, db, args.idesc, acc);
+                else
+                  umma_f16(d_tmem, da, db, args.idesc, acc);
+              }
+            }
           }
           if (PAIR)
             umma_commit_pair_multicast(&empty[s], 0x3);   // free slot s in both CTAs

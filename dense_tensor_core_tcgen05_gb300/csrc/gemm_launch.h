@@ -11,10 +11,16 @@ namespace gemm_tc {
 // B columns one CTA holds: the whole tile width, or half of it in pair mode.
 constexpr int b_cols_per_cta(int bn, bool pair) { return pair ? bn / 2 : bn; }
 
-// Pipeline depth: as many ring slots as fit in 192 KB of shared memory (the rest
+// k-blocks per ring stage: two, so that each operand copy reads at least 256
+// contiguous bytes of every row it touches (GB300's DRAM delivers ~3.7 TB/s to
+// 128-byte row pieces and ~5.3 TB/s to 256-byte ones, measured with a TMA
+// streaming probe).
+constexpr int ko_for(int /*bn*/, bool /*pair*/) { return 2; }
+
+// Pipeline depth: as many stages as fit in 192 KB of shared memory (the rest
 // holds the epilogue staging buffers and barriers).
 constexpr int stages_for(int bn, bool pair) {
-  return (192 * 1024) / (BM * BK * 2 + b_cols_per_cta(bn, pair) * BK * 2);
+  return (192 * 1024) / (ko_for(bn, pair) * (BM * BK * 2 + b_cols_per_cta(bn, pair) * BK * 2));
 }
 
 // Dynamic shared memory bytes of an instance (layout + alignment slack).
@@ -25,15 +31,18 @@ int smem_alloc_bytes(int bn, bool pair);
 // cluster size).  Pair launches are capped at the number of co-resident 2-CTA
 // clusters (the pair kernel is persistent); split-K launches run exactly one
 // tile per cluster.  `dev` indexes the per-device attribute cache.
-cudaError_t launch_gemm_f32(int bn, bool pair, int split, const CUtensorMap& a,
-                            const CUtensorMap& b, const CUtensorMap& c, const KernelArgs& args,
-                            int grid, cudaStream_t stream, int dev);
-cudaError_t launch_gemm_bf16(int bn, bool pair, int split, const CUtensorMap& a,
-                             const CUtensorMap& b, const CUtensorMap& c, const KernelArgs& args,
-                             int grid, cudaStream_t stream, int dev);
-cudaError_t launch_gemm_f16(int bn, bool pair, int split, const CUtensorMap& a,
-                            const CUtensorMap& b, const CUtensorMap& c, const KernelArgs& args,
-                            int grid, cudaStream_t stream, int dev);
+// The operand maps: 2-D (one k-block or one atom per copy, exact bounds) and
+// 3-D (several whole 64-element blocks per copy), plus the C map.
+struct OperandMaps {
+  CUtensorMap a, b, a3, b3, c;
+};
+
+cudaError_t launch_gemm_f32(int bn, bool pair, int split, const OperandMaps& m,
+                            const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_bf16(int bn, bool pair, int split, const OperandMaps& m,
+                             const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_f16(int bn, bool pair, int split, const OperandMaps& m,
+                            const KernelArgs& args, int grid, cudaStream_t stream, int dev);
 
 // Split-K cluster shapes that have kernel instances: (bn, split).
 constexpr bool split_supported(int bn, int split) {

@@ -9,11 +9,12 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 template <int BN, bool PAIR, int SPLIT>
-cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                        const KernelArgs& args, int grid, cudaStream_t stream, int dev) {
+cudaError_t launch_inst(const OperandMaps& m, const KernelArgs& args, int grid,
+                        cudaStream_t stream, int dev) {
   constexpr int ST = stages_for(BN, PAIR);
-  using L = SmemLayout<BN, ST, PAIR>;
-  auto kern = gemm_tcgen05_kernel<BN, ST, GEMM_OUT_KIND, PAIR, SPLIT>;
+  constexpr int KO = ko_for(BN, PAIR);
+  using L = SmemLayout<BN, ST, PAIR, KO>;
+  auto kern = gemm_tcgen05_kernel<BN, ST, GEMM_OUT_KIND, PAIR, SPLIT, KO>;
   static volatile bool attr_set[kMaxDevices] = {};
   static volatile int max_clusters[kMaxDevices] = {};
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
@@ -55,33 +56,32 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap& b, const CUtens
     if (grid < 2) return cudaErrorInvalidConfiguration;
   }
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, c, args);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, m.a, m.b, m.a3, m.b3, m.c, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t GEMM_LAUNCH_NAME(int bn, bool pair, int split, const CUtensorMap& a,
-                             const CUtensorMap& b, const CUtensorMap& c, const KernelArgs& args,
-                             int grid, cudaStream_t stream, int dev) {
+cudaError_t GEMM_LAUNCH_NAME(int bn, bool pair, int split, const OperandMaps& m,
+                             const KernelArgs& args, int grid, cudaStream_t stream, int dev) {
   if (split > 1) {
     if (pair) return cudaErrorInvalidValue;
-    if (bn == 256 && split == 2) return launch_inst<256, false, 2>(a, b, c, args, grid, stream, dev);
-    if (bn == 256 && split == 4) return launch_inst<256, false, 4>(a, b, c, args, grid, stream, dev);
-    if (bn == 128 && split == 2) return launch_inst<128, false, 2>(a, b, c, args, grid, stream, dev);
+    if (bn == 256 && split == 2) return launch_inst<256, false, 2>(m, args, grid, stream, dev);
+    if (bn == 256 && split == 4) return launch_inst<256, false, 4>(m, args, grid, stream, dev);
+    if (bn == 128 && split == 2) return launch_inst<128, false, 2>(m, args, grid, stream, dev);
     return cudaErrorInvalidValue;
   }
   if (pair) {
     switch (bn) {
-      case 128: return launch_inst<128, true, 1>(a, b, c, args, grid, stream, dev);
-      case 256: return launch_inst<256, true, 1>(a, b, c, args, grid, stream, dev);
+      case 128: return launch_inst<128, true, 1>(m, args, grid, stream, dev);
+      case 256: return launch_inst<256, true, 1>(m, args, grid, stream, dev);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (bn) {
-    case 64: return launch_inst<64, false, 1>(a, b, c, args, grid, stream, dev);
-    case 128: return launch_inst<128, false, 1>(a, b, c, args, grid, stream, dev);
-    case 256: return launch_inst<256, false, 1>(a, b, c, args, grid, stream, dev);
+    case 64: return launch_inst<64, false, 1>(m, args, grid, stream, dev);
+    case 128: return launch_inst<128, false, 1>(m, args, grid, stream, dev);
+    case 256: return launch_inst<256, false, 1>(m, args, grid, stream, dev);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -159,7 +159,8 @@ void gemm_debug_set(uint64_t wait_timeout_ns, int32_t inject_skip);
  * num_sms is the SM count to plan for.  Returns the same argument errors as
  * gemm() for the size/dtype/layout arguments. */
 typedef struct {
-  int32_t bm, bn, bk, stages;             /* bm: rows per tile (128, or 256 for a pair) */
+  int32_t bm, bn, bk, stages;             /* bm: rows per tile (128, or 256 for a pair);
+                                              bk: K per ring stage */
   int32_t m_tiles, n_tiles, k_blocks, num_tiles;
   int32_t grid, group_m, threads, smem_bytes;
   int32_t tmem_cols, a_mn, b_mn, epi_chunk_cols;

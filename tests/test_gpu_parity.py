@@ -330,7 +330,7 @@ def test_wait_timeout_is_reported_and_context_survives(_lib, mode):
     issuer's wait must run out, the kernel must record the timeout and return,
     and the device must stay usable."""
     g = _lib
-    M, N, K = 512, 256, 1024   # every mode gets >= 3 ring iterations per CTA
+    M, N, K = 512, 256, 2048   # every mode gets >= 3 ring stages per CTA
     A, B = operands(M, N, K, "bf16", False, False, dist="int", seed=5)
     try:
         g.gemm_debug_set(50_000_000, 3)   # 50 ms limit; skip ring iteration 2
