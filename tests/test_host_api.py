@@ -115,9 +115,11 @@ def test_no_cpu_fallback_without_device(g):
                                        k_blocks=32, b_mn=1, stages=3, bk=128)),
     ((4096, 4096, 4096, 1, 1), 0, dict(cta_group=2, bn=256, num_tiles=256, grid=152)),
     ((8192, 8192, 8192, 1, 2), 2, dict(cta_group=2, bn=256, num_tiles=1024, grid=152, b_mn=0)),
-    # a single 128-row panel with long K: 256-wide tiles, K split over 4-CTA clusters
-    ((128, 8192, 8192, 1, 1), 2, dict(cta_group=1, bm=128, bn=256, num_tiles=32, grid=128,
-                                      k_blocks=128, stages=2, split_k=4)),
+    # a single 128-row panel with long K: 128-wide tiles, K split over 2-CTA clusters
+    ((128, 8192, 8192, 1, 1), 2, dict(cta_group=1, bm=128, bn=128, num_tiles=64, grid=128,
+                                      k_blocks=128, stages=3, split_k=2)),
+    # N too wide for 128-wide tiles in one wave: 256-wide, split 4
+    ((128, 16384, 8192, 1, 1), 2, dict(cta_group=1, bn=256, num_tiles=64, split_k=2)),
     # a single panel with short K: no split (too few k-blocks per CTA)
     ((128, 8192, 256, 1, 1), 2, dict(cta_group=1, split_k=1)),
     ((257, 263, 251, 1, 2), 3, dict(cta_group=1, m_tiles=3, k_blocks=4, a_mn=1, b_mn=0)),
