@@ -161,6 +161,22 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def aggregate_ranks(local_step_ms, flops_per_step, world, device=None):
+    """Whole-job result of a replicated run: the step time is the MAX over ranks
+    (the slowest replica bounds the job) and the value is the FLOPs all ranks
+    processed per step divided by that time, in TFLOP/s.  With world > 1 it must
+    be called by every rank of the initialised process group (any backend)."""
+    step_ms = float(local_step_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dev = device if (device is not None and dist.get_backend() == "nccl") else "cpu"
+        tt = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_ms = float(tt.item())
+    return step_ms, world * flops_per_step / (step_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ our arm
 
 def upload(bits, fmt, device):
@@ -302,13 +318,8 @@ def run_ours(args, rank, world, device):
     t_wall = time.perf_counter() - t_wall0
     clocks = sampler.stop() if sampler else None
 
-    step_ms = sum(times) / len(times)
     flops = gemm_flops(w["M"], w["N"], w["K"])
-    if world > 1:
-        tt = torch.tensor([step_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(tt.item())
-    value = world * flops / (step_ms * 1e-3) / 1e12
+    step_ms, value = aggregate_ranks(sum(times) / len(times), flops, world, device)
 
     # roofline of the GEMM kernel (the only kernel of a step)
     peak_t = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])

@@ -1,0 +1,190 @@
+// Hardware probes behind the GEMM's design choices (measurement only; not on the
+// GEMM path):
+//  * mma_rate: back-to-back tcgen05.mma (kind::f16, K = 16) from one thread per CTA
+//    (or per CTA pair), timed with clock64 -> cycles per instruction and dense
+//    FLOP/clk/SM for a given N.  The tensor-core peak used by the roofline is this
+//    rate times the SM count times the clock (the Ada GEMM page's advice to measure
+//    FLOP/clk/SM with an in-kernel clock and convert with the clock seen under load).
+//  * tma_stream: one producer thread per CTA streams a K-major [N, K] bf16 matrix
+//    through a ring of TMA tile copies of `R` rows x `KO` consecutive 64-element
+//    blocks (a 3-D map whose third dimension walks blocks along the row) -> the DRAM
+//    bandwidth a tile-copy access pattern reaches.
+// Every wait is bounded (1-2 s, %globaltimer); a CTA that gives up writes ~0.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gemm_common.h"
+#include "ptx.cuh"
+
+using namespace gemm_tc;
+
+namespace {
+
+template <int N, bool PAIR>
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned long long* out) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 64 * 1024);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + 64 * 1024 + 64);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+  // operands: 64 KB of finite bf16 values (the contents do not matter for timing)
+  for (int i = threadIdx.x; i < 16 * 1024; i += blockDim.x) reinterpret_cast<uint32_t*>(smem)[i] = 0x3f803f80u;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    if (PAIR) {
+      tmem_alloc_pair(slot, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(slot, 512);
+      tmem_relinquish();
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  if (PAIR) cluster_sync(); else __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  if (warp == 0 && lane == 0 && rank == 0) {
+    const uint32_t idesc = make_idesc_f16(1, 0, 0, PAIR ? 256 : 128, N);
+    const uint64_t da = make_sdesc_sw128(smem_u32(smem), 16, 1024);
+    const uint64_t db = make_sdesc_sw128(smem_u32(smem + 32 * 1024), 16, 1024);
+    const long long t0 = clock64();
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        if (PAIR) umma_f16_pair(tmem, da + 2 * kk, db + 2 * kk, idesc, 1);
+        else umma_f16(tmem, da + 2 * kk, db + 2 * kk, idesc, 1);
+      }
+    }
+    if (PAIR) umma_commit_pair_multicast(bar, 0x1); else umma_commit(bar);
+    const uint64_t g0 = globaltimer_ns();
+    bool done = false;
+    while (!(done = mbar_try_wait(bar, 0)) && globaltimer_ns() - g0 < 2000000000ull) {
+    }
+    out[blockIdx.x] = done ? static_cast<unsigned long long>(clock64() - t0) : ~0ull;
+  }
+  tc_fence_before();
+  if (PAIR) cluster_sync(); else __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    __syncwarp();
+    if (PAIR) tmem_dealloc_pair(tmem, 512); else tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void __launch_bounds__(64, 1)
+    tma_stream_kernel(const __grid_constant__ CUtensorMap tm, int rows_per_cta, int R, int KO, int S,
+                      int K, unsigned long long* out) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  const int box_bytes = R * 128 * KO;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * box_bytes);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  const int row0 = blockIdx.x * rows_per_cta;
+  const int kgroups = K / (64 * KO), rblocks = rows_per_cta / R, total = kgroups * rblocks;
+  const uint64_t t0 = globaltimer_ns();
+  for (int i = 0; i < total + S; ++i) {
+    if (i >= S) {   // the copy issued S iterations ago must have landed before its slot is reused
+      const int j = i - S, s = j % S;
+      const uint64_t g0 = globaltimer_ns();
+      while (!mbar_try_wait(&bars[s], (j / S) & 1)) {
+        if (globaltimer_ns() - g0 > 1000000000ull) {
+          // give the copies still in flight a bounded moment to land, then report failure
+          const uint64_t g1 = globaltimer_ns();
+          while (globaltimer_ns() - g1 < 1000000ull) {
+          }
+          out[blockIdx.x] = ~0ull;
+          return;
+        }
+      }
+    }
+    if (i < total) {
+      const int s = i % S, kg = i % kgroups, rb = i / kgroups;
+      mbar_arrive_expect_tx(&bars[s], box_bytes);
+      tma_load_3d(smem + s * box_bytes, &tm, 0, row0 + rb * R, kg * KO, &bars[s]);
+    }
+  }
+  out[blockIdx.x] = globaltimer_ns() - t0;
+}
+
+template <int N, bool PAIR>
+int launch_mma(int grid, int iters, unsigned long long* dout) {
+  auto k = mma_rate_kernel<N, PAIR>;
+  const int smem = 64 * 1024 + 2048;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (cudaLaunchKernelEx(&cfg, k, iters, dout) != cudaSuccess) return -2;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace
+
+// Cycles for `iters` x 4 back-to-back MMAs (M = 128, or 256 over a pair; K = 16;
+// the given N) per issuing CTA, written to dout[blockIdx.x] (~0 if a wait gave up).
+// grid must be even when pair != 0.  Returns 0 or a negative error.
+extern "C" int probe_mma_rate(int n, int pair, int grid, int iters, unsigned long long* dout) {
+  if (grid <= 0 || iters <= 0 || (pair && (grid & 1))) return -10;
+#define GEMM_PROBE_CASE(NN, PP) \
+  if (n == NN && pair == PP) return launch_mma<NN, PP>(grid, iters, dout);
+  GEMM_PROBE_CASE(64, 0) GEMM_PROBE_CASE(128, 0) GEMM_PROBE_CASE(256, 0)
+  GEMM_PROBE_CASE(128, 1) GEMM_PROBE_CASE(256, 1)
+#undef GEMM_PROBE_CASE
+  return -11;
+}
+
+// Nanoseconds per CTA to stream B ([N, K] bf16, row pitch K, 16-byte aligned) with
+// copies of R rows x KO blocks of 64 elements, S copies in flight per CTA, grid
+// CTAs each owning N / grid rows.  Requires K % (64 * KO) == 0, (N / grid) % R == 0,
+// R <= 256, KO * 64 * 2 * ... <= 227 KB of ring.  Returns 0 or a negative error.
+extern "C" int probe_tma_stream(const void* B, int N, int K, int grid, int R, int KO, int S,
+                                unsigned long long* dout) {
+  if (grid <= 0 || N % grid || (N / grid) % R || R > 256 || R % 8 || KO < 1 || K % (64 * KO) || S < 1)
+    return -10;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return -1;
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  CUtensorMap tm;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(R), static_cast<cuuint32_t>(KO)};
+  cuuint32_t es[3] = {1, 1, 1};
+  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return -2;
+  const int smem = S * R * 128 * KO + 1024 + 8 * S + 64;
+  if (smem > 232448) return -12;
+  if (cudaFuncSetAttribute(tma_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return -3;
+  tma_stream_kernel<<<grid, 64, smem>>>(tm, N / grid, R, KO, S, K, dout);
+  if (cudaGetLastError() != cudaSuccess) return -4;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -5;
+}
