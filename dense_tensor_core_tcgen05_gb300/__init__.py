@@ -14,7 +14,7 @@ _BINDING_NAMES = frozenset((
     "GEMM_ERR_UNSUPPORTED", "GEMM_F16", "GEMM_F32", "GEMM_OK", "LIB_PATH", "GemmError",
     "gemm", "gemm_config_t", "gemm_debug_set", "gemm_encode_idesc", "gemm_encode_sdesc",
     "gemm_ex", "gemm_host", "gemm_plan", "gemm_plan_t", "gemm_sync_status",
-    "gemm_tile_coord", "gemm_version", "library", "matmul", "status_string"))
+    "gemm_tile_coord", "gemm_version", "gemm_work_items", "library", "matmul", "status_string"))
 
 
 def __getattr__(name):

@@ -20,21 +20,23 @@ GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ARCH, GEMM_ERR_CUD
 
 # Symbols declared in include/gemm_tcgen05.h.
 EXPORTS = ("gemm", "gemm_ex", "gemm_host", "gemm_status_string", "gemm_sync_status",
-           "gemm_debug_set", "gemm_plan", "gemm_tile_coord", "gemm_encode_idesc",
-           "gemm_encode_sdesc", "gemm_version")
+           "gemm_debug_set", "gemm_plan", "gemm_tile_coord", "gemm_work_items",
+           "gemm_encode_idesc", "gemm_encode_sdesc", "gemm_version")
 
 
 class gemm_config_t(ctypes.Structure):
     _fields_ = [("bn", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("cta_group", ctypes.c_int32),
-                ("split_k", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("split_k", ctypes.c_int32), ("stream_k", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 class gemm_plan_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "bm", "bn", "bk", "stages", "m_tiles", "n_tiles", "k_blocks", "num_tiles",
         "grid", "group_m", "threads", "smem_bytes", "tmem_cols", "a_mn", "b_mn",
-        "epi_chunk_cols", "cta_group", "split_k")]
+        "epi_chunk_cols", "cta_group", "split_k", "groups", "dp_tiles")] + [
+        ("sk_iters", ctypes.c_int64), ("scratch_bytes", ctypes.c_int64)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -71,6 +73,8 @@ def _load():
     lib.gemm_plan.restype = ci
     lib.gemm_tile_coord.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
     lib.gemm_tile_coord.restype = None
+    lib.gemm_work_items.argtypes = [i32, i32, i32, i64, i32, ctypes.POINTER(i32), i32]
+    lib.gemm_work_items.restype = i32
     lib.gemm_encode_idesc.argtypes = [ci, ci, ci, ci, ci]
     lib.gemm_encode_idesc.restype = ctypes.c_uint32
     lib.gemm_encode_sdesc.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
@@ -100,6 +104,7 @@ def _cfg(cfg):
     c = gemm_config_t()
     c.bn, c.group_m, c.grid = int(cfg.get("bn", 0)), int(cfg.get("group_m", 0)), int(cfg.get("grid", 0))
     c.cta_group, c.split_k = int(cfg.get("cta_group", 0)), int(cfg.get("split_k", 0))
+    c.stream_k = int(cfg.get("stream_k", 0))
     return ctypes.byref(c)
 
 
@@ -141,6 +146,12 @@ def gemm_tile_coord(t, m_tiles, n_tiles, group_m):
     m, n = ctypes.c_int32(0), ctypes.c_int32(0)
     _lib.gemm_tile_coord(t, m_tiles, n_tiles, group_m, ctypes.byref(m), ctypes.byref(n))
     return m.value, n.value
+
+
+def gemm_work_items(unit, units, dp_tiles, sk_iters, groups, max_items=4096):
+    buf = (ctypes.c_int32 * (3 * max_items))()
+    n = _lib.gemm_work_items(unit, units, dp_tiles, sk_iters, groups, buf, max_items)
+    return [tuple(buf[3 * i:3 * i + 3]) for i in range(min(n, max_items))]
 
 
 def gemm_encode_idesc(in_dtype, a_mn, b_mn, m, n):

@@ -15,7 +15,9 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "gemm_common.h"
 #include "gemm_kernel.cuh"
@@ -59,6 +61,51 @@ const DeviceInfo* device_info(int dev) {
     d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_gemm_status_word);
   });
   return &d;
+}
+
+// Stream-K scratch, one per (device, stream) so that launches on different
+// streams never share it: a fixed region of kMaxSkCtas ready flags (so a flag's
+// address never depends on the launch shape), then one fp32 partial tile slot
+// per CTA.  Grown on demand (the old buffer is freed after the stream drains),
+// zeroed on the stream when allocated; every launch gets the next epoch, so a
+// flag equal to the current epoch can only have been written by this launch.
+constexpr int kMaxSkCtas = 1024;
+constexpr size_t kFlagBytes = sizeof(unsigned int) * kMaxSkCtas;
+
+struct Scratch {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  unsigned int epoch = 0;
+};
+std::mutex g_scratch_mu;
+std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
+
+gemm_status_t scratch_for(int dev, cudaStream_t st, size_t slot_bytes, int ctas, float** ws,
+                          unsigned int** flags, unsigned int* epoch) {
+  if (ctas > kMaxSkCtas) return GEMM_ERR_INVALID_ARG;
+  const size_t need = kFlagBytes + slot_bytes * static_cast<size_t>(ctas);
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  Scratch& sc = g_scratch[std::make_pair(dev, st)];
+  if (sc.bytes < need) {
+    if (sc.ptr) {
+      if (cudaStreamSynchronize(st) != cudaSuccess) return GEMM_ERR_CUDA;
+      cudaFree(sc.ptr);
+      sc.ptr = nullptr;
+      sc.bytes = 0;
+    }
+    if (cudaMalloc(&sc.ptr, need) != cudaSuccess) return GEMM_ERR_CUDA;
+    sc.bytes = need;
+    if (cudaMemsetAsync(sc.ptr, 0, kFlagBytes, st) != cudaSuccess) return GEMM_ERR_CUDA;
+    sc.epoch = 0;
+  }
+  *flags = static_cast<unsigned int*>(sc.ptr);
+  *ws = reinterpret_cast<float*>(static_cast<char*>(sc.ptr) + kFlagBytes);
+  if (++sc.epoch == 0) {   // wrapped: old flags could match again, so clear them
+    if (cudaMemsetAsync(sc.ptr, 0, kFlagBytes, st) != cudaSuccess) return GEMM_ERR_CUDA;
+    sc.epoch = 1;
+  }
+  *epoch = sc.epoch;
+  return GEMM_OK;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -181,7 +228,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
                         const gemm_config_t* cfg, gemm_plan_t* p) {
   if (num_sms <= 0) return GEMM_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
-  if (cfg && (cfg->reserved[0] || cfg->reserved[1] || cfg->reserved[2])) return GEMM_ERR_INVALID_ARG;
+  if (cfg && (cfg->reserved[0] || cfg->reserved[1])) return GEMM_ERR_INVALID_ARG;
   int bn = 0;
   bool pair = false;
   choose_unit(M, N, num_sms, &bn, &pair);
@@ -224,14 +271,39 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
   const int per_unit = pair ? 2 : 1;
   int grid = (cfg && cfg->grid) ? cfg->grid : (pair ? (num_sms / 2) * 2 : num_sms);
   if (grid < 0) return GEMM_ERR_INVALID_ARG;
-  if (grid > p->num_tiles * per_unit) grid = p->num_tiles * per_unit;
   if (pair) grid = std::max(2, grid & ~1);
+  // Work split: k-groups per tile, then stream-K for the last wave(s).  All but
+  // the last whole wave stay data-parallel; the rest of the tiles' k-groups are
+  // shared evenly by all units when the last wave would otherwise leave more
+  // than 1/16 of the units idle and a tile has enough k-groups to share.
+  const int ko = ko_for(bn, pair);
+  p->groups = static_cast<int32_t>(ceil_div(kb, ko));
+  p->dp_tiles = p->num_tiles;
+  p->sk_iters = 0;
+  const int sk_mode = cfg ? cfg->stream_k : 0;
+  if (sk_mode < 0 || sk_mode > 2) return GEMM_ERR_INVALID_ARG;
+  if (split == 1 && sk_mode != 1 && grid <= kMaxSkCtas) {
+    const int64_t units = grid / per_unit;
+    const int64_t waves = p->num_tiles / units, rem = p->num_tiles % units;
+    const bool worth = rem != 0 && (units - rem) * 16 > units && p->groups >= 4;
+    if (sk_mode == 2 || worth) {
+      const int64_t dp = (waves > 0 ? waves - 1 : 0) * units;
+      const int64_t sk = (p->num_tiles - dp) * int64_t(p->groups);
+      if (sk >= units && sk < (int64_t(1) << 40)) {
+        p->dp_tiles = static_cast<int32_t>(dp);
+        p->sk_iters = sk;
+      }
+    }
+  }
+  // a data-parallel launch needs no more units than tiles
+  if (!p->sk_iters && grid > p->num_tiles * per_unit) grid = p->num_tiles * per_unit;
   if (split > 1) {
     if (int64_t(p->num_tiles) * split >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
     grid = p->num_tiles * split;   // exactly one tile per split-K cluster
   }
   p->grid = grid;
   p->split_k = split;
+  p->scratch_bytes = p->sk_iters ? int64_t(kFlagBytes) + int64_t(grid) * BM * int64_t(bn) * 4 : 0;
   p->threads = NUM_THREADS;
   p->smem_bytes = smem_alloc_bytes(bn, pair);
   p->tmem_cols = 2 * bn;
@@ -377,6 +449,13 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.b_hint = p.m_tiles == 1 && p.n_tiles > 1 ? 1 : (p.n_tiles == 1 && p.m_tiles > 1 ? 2 : 0);
   ka.a_full3d = a_full3d;
   ka.b_full3d = b_full3d;
+  ka.groups = p.groups;
+  ka.dp_tiles = p.dp_tiles;
+  ka.sk_iters = p.sk_iters;
+  if (p.sk_iters) {
+    s = scratch_for(dev, stream, size_t(BM) * p.bn * 4, p.grid, &ka.ws, &ka.ws_flags, &ka.epoch);
+    if (s != GEMM_OK) return s;
+  }
 
   cudaError_t e;
   switch (out_dtype) {
@@ -505,6 +584,25 @@ void gemm_tile_coord(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_
   tile_coord(t, m_tiles, n_tiles, group_m, &m, &n);
   *m_blk = m;
   *n_blk = n;
+}
+
+int32_t gemm_work_items(int32_t unit, int32_t units, int32_t dp_tiles, int64_t sk_iters,
+                        int32_t groups, int32_t* items, int32_t max_items) {
+  if (unit < 0 || units <= 0 || unit >= units || groups <= 0 || dp_tiles < 0 || sk_iters < 0)
+    return 0;
+  WorkIter wi;
+  wi.init(unit, units, dp_tiles, sk_iters, groups);
+  WorkItem w;
+  int32_t n = 0;
+  while (wi.next(&w)) {
+    if (items && n < max_items) {
+      items[3 * n] = w.tile;
+      items[3 * n + 1] = w.g0;
+      items[3 * n + 2] = w.g1;
+    }
+    ++n;
+  }
+  return n;
 }
 
 uint32_t gemm_encode_idesc(int in_dtype, int a_mn, int b_mn, int m, int n) {

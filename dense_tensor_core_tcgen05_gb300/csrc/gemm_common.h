@@ -63,6 +63,62 @@ GEMM_HD uint64_t make_sdesc_sw128(uint32_t smem_addr, uint32_t lbo_bytes, uint32
          ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// ------------------------------------------------------------- work split
+//
+// A launch's work is a list of tiles, each a sequence of `groups` k-groups (ring
+// stages).  Data-parallel phase: unit u (a CTA, or a CTA pair) takes whole tiles
+// u, u + units, ... below dp_tiles.  Stream-K phase: the remaining tiles' k-groups
+// form one iteration space of sk_iters = (num_tiles - dp_tiles) * groups entries,
+// split evenly: unit u takes [u * sk_iters / units, (u + 1) * sk_iters / units),
+// walked tile by tile.  A segment that does not end its tile leaves a partial sum;
+// the unit whose segment ends a tile adds the earlier units' partials.
+struct WorkItem {
+  int tile, g0, g1;   // tile index and k-group range [g0, g1)
+};
+
+struct WorkIter {
+  int units, dp_tiles, groups, next_dp;
+  long long i, hi, sk_iters;
+  GEMM_HD void init(int unit, int units_, int dp_tiles_, long long sk_iters_, int groups_) {
+    units = units_;
+    dp_tiles = dp_tiles_;
+    groups = groups_;
+    next_dp = unit;
+    sk_iters = sk_iters_;
+    i = (static_cast<long long>(unit) * sk_iters) / units;
+    hi = (static_cast<long long>(unit + 1) * sk_iters) / units;
+  }
+  GEMM_HD bool next(WorkItem* w) {
+    if (next_dp < dp_tiles) {
+      w->tile = next_dp;
+      w->g0 = 0;
+      w->g1 = groups;
+      next_dp += units;
+      return true;
+    }
+    if (i < hi) {
+      const long long t = i / groups;
+      const int g0 = static_cast<int>(i - t * groups);
+      const long long left = hi - i;
+      const int g1 = left < groups - g0 ? g0 + static_cast<int>(left) : groups;
+      w->tile = dp_tiles + static_cast<int>(t);
+      w->g0 = g0;
+      w->g1 = g1;
+      i += g1 - g0;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Stream-K unit whose iteration range contains iteration i (0 <= i < sk_iters).
+GEMM_HD int sk_unit_of(long long i, int units, long long sk_iters) {
+  int u = static_cast<int>((i * units) / sk_iters);
+  while (u + 1 < units && ((static_cast<long long>(u) + 1) * sk_iters) / units <= i) ++u;
+  while (u > 0 && (static_cast<long long>(u) * sk_iters) / units > i) --u;
+  return u;
+}
+
 // Kernel arguments (plain data, built on the host).
 struct KernelArgs {
   int M, N, K;
@@ -81,6 +137,15 @@ struct KernelArgs {
   // Extent of the 3-D operand maps in whole 64-element blocks (0: no 3-D map):
   // K-major operand -> full k-blocks (K / 64); MN-major -> full 64-wide atoms.
   int a_full3d, b_full3d;
+  // Work split (see WorkIter): k-groups per tile, whole tiles of the
+  // data-parallel phase, stream-K iterations after it.
+  int groups, dp_tiles;
+  long long sk_iters;
+  // Stream-K scratch: one fp32 partial tile slot and one ready flag per CTA;
+  // a flag holds the epoch of the launch whose partial is in the slot.
+  float* ws;
+  unsigned int* ws_flags;
+  unsigned int epoch;
 };
 
 }  // namespace gemm_tc

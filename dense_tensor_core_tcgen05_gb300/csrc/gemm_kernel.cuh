@@ -50,6 +50,7 @@ enum WaitSite {
   SITE_EPI_TMEM_FULL = 4,
   SITE_EPI_C_LOAD = 5,
   SITE_DRAIN = 6,
+  SITE_STREAMK_FLAG = 7,
 };
 
 // Shared-memory map of one CTA.  A ring stage holds KO consecutive k-blocks
@@ -72,8 +73,8 @@ struct SmemLayout {
   static constexpr int off_b = STAGES * A_BYTES;
   static constexpr int off_epi = off_b + STAGES * B_BYTES;
   static constexpr int off_bar = off_epi + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-  // full[STAGES], empty[STAGES], tfull[2], tempty[2], cload[EPI_WARPS*EPI_BUFS], drain
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 1;
+  // full[STAGES], empty[STAGES], tfull[2], tempty[2], cload[EPI_WARPS*EPI_BUFS], drain, esync
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 2;
   static constexpr int off_tmem = off_bar + NUM_BARS * 8;
   static constexpr int off_flag = off_tmem + 8;
   static constexpr int BYTES = off_flag + 8;
@@ -300,6 +301,19 @@ __device__ __forceinline__ uint32_t partial_addr(uint32_t base, int row, int pie
   return base + static_cast<uint32_t>(row * (BN * 4) + ((piece ^ (row & 7)) << 4));
 }
 
+// Stream-K hand-off: a CTA publishes its partial tile with a release store of
+// the launch epoch into its flag; the owner of the tile acquires it.
+__device__ __forceinline__ void flag_release(unsigned int* f, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int flag_acquire(const unsigned int* f) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  return v;
+}
+
+
 __device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -350,6 +364,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* cload = tempty + 2;
   uint64_t* drain = cload + EPI_WARPS * EPI_BUFS;
+  uint64_t* esync = drain + 1;   // rendezvous of the four epilogue warps (stream-K hand-off)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_tmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_flag);
 
@@ -364,8 +379,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int UNIT_CTAS = PAIR ? 2 : SPLIT;
   const int unit0 = static_cast<int>(blockIdx.x) / UNIT_CTAS;
   const int unit_stride = static_cast<int>(gridDim.x) / UNIT_CTAS;
-  const int kb_begin = SPLITK ? (args.k_blocks * static_cast<int>(srank)) / SPLIT : 0;
-  const int kb_end = SPLITK ? (args.k_blocks * static_cast<int>(srank + 1)) / SPLIT : args.k_blocks;
+  // K range of a work item, in k-blocks: a split-K CTA's fixed slice, otherwise
+  // the item's k-groups.
+  const int split_kb0 = SPLITK ? (args.k_blocks * static_cast<int>(srank)) / SPLIT : 0;
+  const int split_kb1 = SPLITK ? (args.k_blocks * static_cast<int>(srank + 1)) / SPLIT : 0;
+  auto kb_range = [&](const WorkItem& w, int* b, int* e) {
+    if (SPLITK) {
+      *b = split_kb0;
+      *e = split_kb1;
+    } else {
+      *b = w.g0 * KO;
+      *e = w.g1 * KO < args.k_blocks ? w.g1 * KO : args.k_blocks;
+    }
+  };
+  auto work_begin = [&](WorkIter& wi) {
+    wi.init(unit0, unit_stride, args.dp_tiles, args.sk_iters, args.groups);
+  };
   uint32_t producer_iters = 0;  // ring iterations armed (producer thread only)
 
   if (threadIdx.x == 0) {
@@ -379,6 +408,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < EPI_WARPS * EPI_BUFS; ++i) mbar_init(&cload[i], 1);
     mbar_init(drain, 1);
+    mbar_init(esync, EPI_WARPS);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -412,9 +442,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // L2 policies: 0 = default, 1 = evict first (streamed once), 2 = evict last (reused)
       const uint64_t pol_a = args.a_hint == 1 ? policy_evict_first() : policy_evict_last();
       const uint64_t pol_b = args.b_hint == 1 ? policy_evict_first() : policy_evict_last();
-      for (int t = unit0; ok && t < args.num_tiles; t += unit_stride) {
-        int mb, nb;
-        tile_coord(t, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
+      WorkIter wi;
+      WorkItem w;
+      work_begin(wi);
+      while (ok && wi.next(&w)) {
+        int mb, nb, kb_begin, kb_end;
+        tile_coord(w.tile, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
+        kb_range(w, &kb_begin, &kb_end);
         const int a_row = mb * TILE_M + static_cast<int>(rank) * BM;
         const int b_col = nb * BN + static_cast<int>(rank) * L::B_COLS;
         for (int kb0 = kb_begin; kb0 < kb_end; kb0 += KO, ++it) {
@@ -492,7 +526,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t b_kb = args.b_mn ? BK * SW : L::B_COLS * SW;
       const uint32_t a_step = (args.a_mn ? UMMA_K * SW : UMMA_K * 2) >> 4;
       const uint32_t b_step = (args.b_mn ? UMMA_K * SW : UMMA_K * 2) >> 4;
-      for (int t = unit0; ok && t < args.num_tiles; t += unit_stride, ++tl) {
+      WorkIter wi;
+      WorkItem w;
+      work_begin(wi);
+      for (; ok && wi.next(&w); ++tl) {
+        int kb_begin, kb_end;
+        kb_range(w, &kb_begin, &kb_end);
         const int buf = tl & 1;
         const uint32_t aph = (tl >> 1) & 1;
         if (!wait_one<PAIR>(&tempty[buf], aph ^ 1, abort_flag, args, SITE_MMA_TMEM_EMPTY)) {
@@ -547,12 +586,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
     EpiState st{smem + L::off_epi + ew * EPI_BUFS * L::EPI_BUF_BYTES, &cload[ew * EPI_BUFS], 0,
                 -1, 0};
-    uint32_t tl = 0;
+    uint32_t tl = 0, esync_uses = 0;
     bool ok = true;
     const int r = lane;                  // this thread's row inside the warp's 32-row block
-    for (int t = unit0; ok && t < args.num_tiles; t += unit_stride, ++tl) {
+    // Rendezvous of the four epilogue warps, bounded like every other wait.
+    auto epilogue_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(esync);
+      return wait_warp<PAIR>(esync, (esync_uses++) & 1, abort_flag, args, SITE_STREAMK_FLAG);
+    };
+    WorkIter wi;
+    WorkItem w;
+    work_begin(wi);
+    for (; ok && wi.next(&w); ++tl) {
       int mb, nb;
-      tile_coord(t, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
+      tile_coord(w.tile, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
       const int buf = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
       if (!wait_warp<PAIR>(&tfull[buf], aph, abort_flag, args, SITE_EPI_TMEM_FULL)) {
@@ -579,6 +627,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                          make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
         }
         continue;   // one tile per split-K cluster; phase 2 runs after the cluster barrier
+      }
+      const int prow = quarter * 32 + r;   // this thread's row of the CTA's 128
+      if (w.g1 < args.groups) {
+        // Stream-K segment that does not finish its tile: publish the fp32
+        // partial sum in this CTA's scratch slot, laid out [BN/4][128 rows][4] so
+        // a warp's 16-byte stores cover 512 contiguous bytes, hand the
+        // accumulator back, then release the CTA's flag with the launch epoch.
+        float4* slot = reinterpret_cast<float4*>(args.ws + static_cast<size_t>(blockIdx.x) * BM * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_row, v, c * 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            slot[(c * 8 + j) * BM + prow] =
+                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(&tempty[buf]);
+          else
+            mbar_arrive_cluster(map_to_rank(&tempty[buf], 0));
+        }
+        __threadfence();
+        if (!epilogue_sync()) {
+          ok = false;
+          break;
+        }
+        if (ew == 0 && lane == 0) flag_release(args.ws_flags + blockIdx.x, args.epoch);
+        continue;
+      }
+      // A stream-K segment that finishes its tile: the units before it in the
+      // iteration space hold the tile's earlier k-groups as partial sums.
+      int contrib0 = unit0, contrib1 = unit0;
+      if (w.g0 > 0) {
+        const long long base = static_cast<long long>(w.tile - args.dp_tiles) * args.groups;
+        contrib0 = sk_unit_of(base, unit_stride, args.sk_iters);
+        if (ew == 0 && lane == 0) {
+          for (int u = contrib0; u < contrib1 && !*abort_flag; ++u) {
+            const unsigned int* f = args.ws_flags + u * UNIT_CTAS + rank;
+            const uint64_t t0 = globaltimer_ns();
+            while (flag_acquire(f) != args.epoch) {
+              __nanosleep(64);
+              if (*abort_flag) break;
+              if (globaltimer_ns() - t0 > args.timeout_ns) {
+                record_error(args.status, SITE_STREAMK_FLAG);
+                *abort_flag = 1;
+                break;
+              }
+            }
+          }
+        }
+        if (!epilogue_sync() || *abort_flag) {
+          ok = false;
+          break;
+        }
       }
 #pragma unroll 1
       for (int c = 0; c < CHUNKS; ++c) {
@@ -618,6 +726,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t* src = (OUT == OUT_F32) ? (v0 + 4 * j) : ((j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4)));
 #pragma unroll
           for (int e = 0; e < E; ++e) x[e] = __uint_as_float(src[e]);
+          // stream-K owner: add the earlier units' partials, in unit order
+          for (int u = contrib0; u < contrib1; ++u) {
+            const float4* slot =
+                reinterpret_cast<const float4*>(args.ws + static_cast<size_t>(u * UNIT_CTAS + rank) * BM * BN);
+#pragma unroll
+            for (int h = 0; h < E / 4; ++h) {
+              const float4 pv = __ldcg(slot + ((c * CHUNK + E * j) / 4 + h) * BM + prow);
+              x[4 * h + 0] += pv.x;
+              x[4 * h + 1] += pv.y;
+              x[4 * h + 2] += pv.z;
+              x[4 * h + 3] += pv.w;
+            }
+          }
           finish_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
                             col0 + E * j);
         }

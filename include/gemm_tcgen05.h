@@ -101,14 +101,20 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *             128-row tile, each accumulating 1/split_k of K, the partial sums
  *             reduced in distributed shared memory in a fixed order (needs
  *             cta_group 1; supported for bn 256 with split_k 2 or 4 and bn 128
- *             with split_k 2; one tile per cluster, so grid is ignored). */
+ *             with split_k 2; one tile per cluster, so grid is ignored).
+ *   stream_k  1: off; 2: on.  Stream-K runs all but the last whole wave of
+ *             tiles data-parallel and splits the remaining tiles' k-groups evenly
+ *             over all CTAs (or CTA pairs); a tile's partial sums are added by the
+ *             CTA that finishes it, in a fixed order, through a scratch buffer the
+ *             library keeps per device and stream.  Ignored with split_k > 1. */
 typedef struct {
   int32_t bn;
   int32_t group_m;
   int32_t grid;
   int32_t cta_group;
   int32_t split_k;
-  int32_t reserved[3];  /* must be zero */
+  int32_t stream_k;
+  int32_t reserved[2];  /* must be zero */
 } gemm_config_t;
 
 /* gemm with an explicit configuration (cfg may be NULL = gemm()).  Same
@@ -165,6 +171,10 @@ typedef struct {
   int32_t grid, group_m, threads, smem_bytes;
   int32_t tmem_cols, a_mn, b_mn, epi_chunk_cols;
   int32_t cta_group, split_k;
+  int32_t groups;      /* k-groups (ring stages) per tile */
+  int32_t dp_tiles;    /* tiles of the data-parallel phase */
+  int64_t sk_iters;    /* stream-K iterations (tile k-groups) after it; 0 = none */
+  int64_t scratch_bytes; /* stream-K scratch the launch uses (0 = none) */
 } gemm_plan_t;
 
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int layout,
@@ -175,6 +185,14 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
  * for t in [0, m_tiles * n_tiles). */
 void gemm_tile_coord(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_m,
                      int32_t* m_blk, int32_t* n_blk);
+
+/* The work split of one unit (a CTA, or a CTA pair) for a plan, computed on the
+ * host exactly as the kernel walks it: whole tiles unit, unit + units, ... below
+ * dp_tiles, then the unit's even share of the sk_iters stream-K iterations, tile
+ * by tile.  Writes up to max_items (tile, first k-group, end k-group) triples to
+ * items[3*i .. 3*i+2] and returns the number of items the unit has. */
+int32_t gemm_work_items(int32_t unit, int32_t units, int32_t dp_tiles, int64_t sk_iters,
+                        int32_t groups, int32_t* items, int32_t max_items);
 
 /* The tcgen05 descriptor encoders, exposed for host checks.  idesc: kind::f16
  * instruction descriptor; sdesc: 128B-swizzled shared-memory descriptor. */

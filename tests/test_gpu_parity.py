@@ -38,8 +38,9 @@ def _lib():
 
 MODES = [{"cta_group": 1}, {"cta_group": 2}]
 # every way the kernel can split the work: single CTA, CTA pair, split-K clusters
-ALL_MODES = [{"cta_group": 1}, {"cta_group": 2}, {"split_k": 2}, {"split_k": 4}]
-MODE_IDS = ["cta1", "pair", "splitk2", "splitk4"]
+ALL_MODES = [{"cta_group": 1}, {"cta_group": 2}, {"split_k": 2}, {"split_k": 4},
+             {"cta_group": 1, "stream_k": 2}, {"cta_group": 2, "stream_k": 2}]
+MODE_IDS = ["cta1", "pair", "splitk2", "splitk4", "streamk1", "streamk2"]
 
 
 def _mode_fits(mode, K):
@@ -221,6 +222,63 @@ def test_k_sweep_64x64(K):
                          a_col=False, b_col=False)
     check_against_oracle(out, A, B, M=64, N=64, K=K, in_dtype="f16", out_dtype="f32",
                          a_col=False, b_col=False)
+
+
+# ------------------------------------------------------------ stream-K
+
+SK_CASES = [
+    (1024, 1024, 2048, {"stream_k": 2, "cta_group": 2}),
+    (1024, 1024, 2048, {"stream_k": 2, "cta_group": 1}),
+    (1000, 1100, 1500, {"stream_k": 2, "cta_group": 2}),
+    (1000, 1100, 1500, {"stream_k": 2, "cta_group": 1, "bn": 128}),
+    (2048, 1536, 1024, {"stream_k": 2, "cta_group": 1, "grid": 20}),   # 2 data-parallel waves + stream-K
+    (2048, 1536, 1024, {"stream_k": 2, "cta_group": 2, "grid": 22}),   # 11 pairs
+    (640, 2304, 4096, {"stream_k": 2, "cta_group": 1, "bn": 64}),
+]
+
+
+def _assert_stream_k(M, N, K, cfg, layout=0):
+    import dense_tensor_core_tcgen05_gb300 as g
+    s, p = g.gemm_plan(M, N, K, g.GEMM_BF16, g.GEMM_F32, layout, torch.cuda.get_device_properties(0).multi_processor_count, cfg)
+    assert s == 0 and p.sk_iters > 0, "case does not exercise stream-K"
+
+
+@pytest.mark.parametrize("case", SK_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-" + "-".join(f"{k}{v}" for k, v in c[3].items()))
+@pytest.mark.parametrize("a_col,b_col", [(False, False), (False, True), (True, True)])
+def test_stream_k_integer_exact(case, a_col, b_col):
+    M, N, K, cfg = case
+    _assert_stream_k(M, N, K, cfg, (1 if a_col else 0) | (2 if b_col else 0))
+    A, B = operands(M, N, K, "bf16", a_col, b_col, dist="int", seed=M + K, pad=True)
+    out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32", a_col=a_col,
+                         b_col=b_col, cfg=cfg, ldc=pad8(N))
+    check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
+                         a_col=a_col, b_col=b_col, exact=True)
+
+
+@pytest.mark.parametrize("case", SK_CASES[:4], ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-cta{c[3]['cta_group']}")
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
+def test_stream_k_uniform_beta(case, out_dtype):
+    M, N, K, cfg = case
+    _assert_stream_k(M, N, K, cfg)
+    A, B = operands(M, N, K, "f16", False, True, dist="uniform", seed=K)
+    C = si.matrix("uniform", 3000 + K, M, N, out_dtype)
+    out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="f16", out_dtype=out_dtype, a_col=False,
+                         b_col=True, alpha=0.75, beta=-0.5, C=C, cfg=cfg)
+    check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="f16", out_dtype=out_dtype,
+                         a_col=False, b_col=True, alpha=0.75, beta=-0.5, C=C)
+
+
+def test_stream_k_deterministic_and_repeated():
+    """Stream-K partials are added in a fixed order: repeated launches (epochs
+    advancing on the same scratch) give bitwise-identical results."""
+    M, N, K, cfg = SK_CASES[0]
+    A, B = operands(M, N, K, "bf16", False, True, dist="normal", seed=11)
+    outs = [run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32", a_col=False,
+                        b_col=True, cfg=cfg)[0] for _ in range(3)]
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], outs[2])
+    check_against_oracle(outs[0], A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
+                         a_col=False, b_col=True, rows=sample_rows(M, 40))
 
 
 # ------------------------------------------------------------ edge cases

@@ -111,10 +111,15 @@ def test_no_cpu_fallback_without_device(g):
 
 @pytest.mark.parametrize("shape,layout,expect", [
     # big squares: CTA-pair tiles of 256 x 256 (one cta_group::2 MMA over two SMs)
-    ((2048, 2048, 2048, 0, 2), 0, dict(cta_group=2, bm=256, bn=256, num_tiles=64, grid=128,
-                                       k_blocks=32, b_mn=1, stages=3, bk=128)),
-    ((4096, 4096, 4096, 1, 1), 0, dict(cta_group=2, bn=256, num_tiles=256, grid=152)),
-    ((8192, 8192, 8192, 1, 2), 2, dict(cta_group=2, bn=256, num_tiles=1024, grid=152, b_mn=0)),
+    # one wave of 64 pair tiles on 76 pairs: stream-K over all of them
+    ((2048, 2048, 2048, 0, 2), 0, dict(cta_group=2, bm=256, bn=256, num_tiles=64, grid=152,
+                                       k_blocks=32, b_mn=1, stages=3, bk=128, groups=16,
+                                       dp_tiles=0, sk_iters=1024)),
+    # 3.37 waves: two data-parallel waves, the remaining 104 tiles stream-K
+    ((4096, 4096, 4096, 1, 1), 0, dict(cta_group=2, bn=256, num_tiles=256, grid=152,
+                                       dp_tiles=152, sk_iters=104 * 32)),
+    ((8192, 8192, 8192, 1, 2), 2, dict(cta_group=2, bn=256, num_tiles=1024, grid=152, b_mn=0,
+                                       dp_tiles=912, sk_iters=112 * 64)),
     # a single 128-row panel with long K: 128-wide tiles, K split over 2-CTA clusters
     ((128, 8192, 8192, 1, 1), 2, dict(cta_group=1, bm=128, bn=128, num_tiles=64, grid=128,
                                       k_blocks=128, stages=3, split_k=2)),
@@ -173,6 +178,43 @@ def test_plan_split_k_overrides(g):
     p = g.gemm_plan_t()
     lib = g.library()
     assert lib.gemm_plan(256, 256, 256, 1, 1, 0, 152, ctypes.byref(cfg), ctypes.byref(p)) == 1
+
+
+def test_stream_k_override(g):
+    s, p = g.gemm_plan(4096, 4096, 4096, 1, 1, 0, 152, {"stream_k": 1})
+    assert s == 0 and p.sk_iters == 0 and p.dp_tiles == p.num_tiles == 256 and p.scratch_bytes == 0
+    s, p = g.gemm_plan(1024, 1024, 1024, 1, 1, 0, 152, {"stream_k": 2, "cta_group": 1, "bn": 128})
+    assert s == 0 and p.sk_iters == 64 * 8 and p.dp_tiles == 0 and p.grid == 152
+    assert p.scratch_bytes == 4096 + 152 * 128 * 128 * 4
+    assert g.gemm_plan(1024, 1024, 1024, 1, 1, 0, 152, {"stream_k": 3})[0] == g.GEMM_ERR_INVALID_ARG
+    # split-K plans never stream-K
+    s, p = g.gemm_plan(128, 8192, 8192, 1, 1, 2, 152, {"stream_k": 2})
+    assert s == 0 and p.split_k == 2 and p.sk_iters == 0
+
+
+@pytest.mark.parametrize("units,num_tiles,groups,waves_dp", [(76, 64, 16, 0), (76, 256, 32, 2),
+                                                             (152, 60, 5, 0), (7, 23, 9, 2),
+                                                             (76, 1024, 64, 12), (5, 3, 4, 0)])
+def test_stream_k_split_covers_every_k_group_once(g, units, num_tiles, groups, waves_dp):
+    dp = waves_dp * units
+    sk = (num_tiles - dp) * groups
+    seen = {}
+    for u in range(units):
+        items = g.gemm_work_items(u, units, dp, sk, groups)
+        for t, g0, g1 in items:
+            assert 0 <= t < num_tiles and 0 <= g0 < g1 <= groups
+            if t < dp:
+                assert (g0, g1) == (0, groups) and t % units == u
+            for k in range(g0, g1):
+                assert (t, k) not in seen
+                seen[(t, k)] = u
+    assert len(seen) == num_tiles * groups
+    # a split tile is finished by the highest unit touching it, and the units that
+    # hold its earlier k-groups are exactly the ones before it (contiguous)
+    for t in range(dp, num_tiles):
+        owners = [seen[(t, k)] for k in range(groups)]
+        assert owners == sorted(owners)
+        assert set(owners) == set(range(owners[0], owners[-1] + 1))
 
 
 def test_plan_overrides_and_errors(g):
