@@ -260,10 +260,10 @@ def test_stream_k_integer_exact(case, a_col, b_col):
 def test_stream_k_uniform_beta(case, out_dtype):
     M, N, K, cfg = case
     _assert_stream_k(M, N, K, cfg)
-    A, B = operands(M, N, K, "f16", False, True, dist="uniform", seed=K)
+    A, B = operands(M, N, K, "f16", False, True, dist="uniform", seed=K, pad=True)
     C = si.matrix("uniform", 3000 + K, M, N, out_dtype)
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="f16", out_dtype=out_dtype, a_col=False,
-                         b_col=True, alpha=0.75, beta=-0.5, C=C, cfg=cfg)
+                         b_col=True, alpha=0.75, beta=-0.5, C=C, cfg=cfg, ldc=pad8(N))
     check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="f16", out_dtype=out_dtype,
                          a_col=False, b_col=True, alpha=0.75, beta=-0.5, C=C)
 
