@@ -282,7 +282,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
   p->sk_iters = 0;
   const int sk_mode = cfg ? cfg->stream_k : 0;
   if (sk_mode < 0 || sk_mode > 2) return GEMM_ERR_INVALID_ARG;
-  if (split == 1 && sk_mode != 1 && grid <= kMaxSkCtas) {
+  // Owners wait for partials of higher-numbered units, so stream-K needs every
+  // unit resident at once: at most one CTA per SM.
+  if (split == 1 && sk_mode != 1 && grid <= kMaxSkCtas && grid <= num_sms) {
     const int64_t units = grid / per_unit;
     const int64_t waves = p->num_tiles / units, rem = p->num_tiles % units;
     const bool worth = rem != 0 && (units - rem) * 16 > units && p->groups >= 4;

@@ -70,8 +70,10 @@ GEMM_HD uint64_t make_sdesc_sw128(uint32_t smem_addr, uint32_t lbo_bytes, uint32
 // u, u + units, ... below dp_tiles.  Stream-K phase: the remaining tiles' k-groups
 // form one iteration space of sk_iters = (num_tiles - dp_tiles) * groups entries,
 // split evenly: unit u takes [u * sk_iters / units, (u + 1) * sk_iters / units),
-// walked tile by tile.  A segment that does not end its tile leaves a partial sum;
-// the unit whose segment ends a tile adds the earlier units' partials.
+// walked tile by tile.  The unit holding a tile's first k-groups owns the tile
+// (for it that is its last segment); every later unit touching the tile leaves
+// its share as a partial sum in its first (or only) segment, so partials are
+// ready long before their owner needs them and no unit waits on a chain.
 struct WorkItem {
   int tile, g0, g1;   // tile index and k-group range [g0, g1)
 };

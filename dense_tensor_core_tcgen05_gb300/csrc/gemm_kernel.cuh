@@ -629,11 +629,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;   // one tile per split-K cluster; phase 2 runs after the cluster barrier
       }
       const int prow = quarter * 32 + r;   // this thread's row of the CTA's 128
-      if (w.g1 < args.groups) {
-        // Stream-K segment that does not finish its tile: publish the fp32
-        // partial sum in this CTA's scratch slot, laid out [BN/4][128 rows][4] so
-        // a warp's 16-byte stores cover 512 contiguous bytes, hand the
-        // accumulator back, then release the CTA's flag with the launch epoch.
+      if (w.g0 > 0) {
+        // Stream-K segment that does not hold its tile's first k-groups: publish
+        // the fp32 partial sum in this CTA's scratch slot, laid out
+        // [BN/4][128 rows][4] so a warp's 16-byte stores cover 512 contiguous
+        // bytes, hand the accumulator back, then release the CTA's flag with the
+        // launch epoch.  Such a segment is the first (or only) one of its unit, so
+        // it is published early.
         float4* slot = reinterpret_cast<float4*>(args.ws + static_cast<size_t>(blockIdx.x) * BM * BN);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -662,12 +664,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (ew == 0 && lane == 0) flag_release(args.ws_flags + blockIdx.x, args.epoch);
         continue;
       }
-      // A stream-K segment that finishes its tile: the units before it in the
-      // iteration space hold the tile's earlier k-groups as partial sums.
+      // A stream-K segment holding its tile's first k-groups but not the last
+      // ones (the last segment of its unit) owns the tile: the units after it in
+      // the iteration space hold the later k-groups as partial sums.
       int contrib0 = unit0, contrib1 = unit0;
-      if (w.g0 > 0) {
+      if (w.g1 < args.groups) {
         const long long base = static_cast<long long>(w.tile - args.dp_tiles) * args.groups;
-        contrib0 = sk_unit_of(base, unit_stride, args.sk_iters);
+        contrib0 = unit0 + 1;
+        contrib1 = sk_unit_of(base + args.groups - 1, unit_stride, args.sk_iters) + 1;
         if (ew == 0 && lane == 0) {
           for (int u = contrib0; u < contrib1 && !*abort_flag; ++u) {
             const unsigned int* f = args.ws_flags + u * UNIT_CTAS + rank;
@@ -726,7 +730,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t* src = (OUT == OUT_F32) ? (v0 + 4 * j) : ((j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4)));
 #pragma unroll
           for (int e = 0; e < E; ++e) x[e] = __uint_as_float(src[e]);
-          // stream-K owner: add the earlier units' partials, in unit order
+          // stream-K owner: add the later units' partials, in unit order
           for (int u = contrib0; u < contrib1; ++u) {
             const float4* slot =
                 reinterpret_cast<const float4*>(args.ws + static_cast<size_t>(u * UNIT_CTAS + rank) * BM * BN);

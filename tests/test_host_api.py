@@ -209,12 +209,21 @@ def test_stream_k_split_covers_every_k_group_once(g, units, num_tiles, groups, w
                 assert (t, k) not in seen
                 seen[(t, k)] = u
     assert len(seen) == num_tiles * groups
-    # a split tile is finished by the highest unit touching it, and the units that
-    # hold its earlier k-groups are exactly the ones before it (contiguous)
+    # the units touching a split tile are consecutive, in k order; the lowest one
+    # (holding k-group 0) owns the tile and its share is that unit's last item,
+    # while every other unit's share is its first item
     for t in range(dp, num_tiles):
         owners = [seen[(t, k)] for k in range(groups)]
         assert owners == sorted(owners)
         assert set(owners) == set(range(owners[0], owners[-1] + 1))
+        for u in set(owners):
+            items = [it for it in g.gemm_work_items(u, units, dp, sk, groups) if it[0] >= dp]
+            share = [it for it in items if it[0] == t]
+            assert len(share) == 1
+            if u == owners[0] and len(set(owners)) > 1:
+                assert share[0] == items[-1] and share[0][1] == 0
+            elif u != owners[0]:
+                assert share[0] == items[0]
 
 
 def test_plan_overrides_and_errors(g):
