@@ -39,8 +39,14 @@ constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_ROWS = 32;     // rows per epilogue warp = its TMEM lane quarter
 constexpr int EPI_BUFS = 2;      // staging buffers per epilogue warp
+constexpr int PSLOTS_MAX = 8;    // stream-K partial staging slots per epilogue warp
 
 enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_F16 = 2 };
+
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
 
 // Where a bounded wait gave up (written to the status word, first error wins).
 enum WaitSite {
@@ -73,8 +79,13 @@ struct SmemLayout {
   static constexpr int off_b = STAGES * A_BYTES;
   static constexpr int off_epi = off_b + STAGES * B_BYTES;
   static constexpr int off_bar = off_epi + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-  // full[STAGES], empty[STAGES], tfull[2], tempty[2], cload[EPI_WARPS*EPI_BUFS], drain, esync
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 2;
+  // Stream-K owner: each epilogue warp stages the partial sums it adds in its
+  // quarter of the ring (idle by then), in up to PSLOTS_MAX slots.
+  static constexpr int RING_BYTES = off_epi;
+  static constexpr int PWARP_BYTES = RING_BYTES / EPI_WARPS;
+  // full[STAGES], empty[STAGES], tfull[2], tempty[2], cload[EPI_WARPS*EPI_BUFS], drain, esync,
+  // pfull[EPI_WARPS*PSLOTS_MAX]
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 2 + EPI_WARPS * PSLOTS_MAX;
   static constexpr int off_tmem = off_bar + NUM_BARS * 8;
   static constexpr int off_flag = off_tmem + 8;
   static constexpr int BYTES = off_flag + 8;
@@ -365,6 +376,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* cload = tempty + 2;
   uint64_t* drain = cload + EPI_WARPS * EPI_BUFS;
   uint64_t* esync = drain + 1;   // rendezvous of the four epilogue warps (stream-K hand-off)
+  uint64_t* pfull = esync + 1;   // stream-K partial staging slots, PSLOTS_MAX per epilogue warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_tmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_flag);
 
@@ -409,6 +421,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0; i < EPI_WARPS * EPI_BUFS; ++i) mbar_init(&cload[i], 1);
     mbar_init(drain, 1);
     mbar_init(esync, EPI_WARPS);
+    for (int i = 0; i < EPI_WARPS * PSLOTS_MAX; ++i) mbar_init(&pfull[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -595,6 +608,116 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(esync);
       return wait_warp<PAIR>(esync, (esync_uses++) & 1, abort_flag, args, SITE_STREAMK_FLAG);
     };
+    // Stream-K owner tiles: this warp fetches each later unit's partial sum of
+    // its 32 rows chunk by chunk (one bulk copy per chunk and contributing
+    // unit) into PSLOTS slots of its quarter of the idle ring.  Copies are
+    // numbered in issue order; p_issued and p_done (waited for) are warp-uniform.
+    constexpr int PART_BYTES = CHUNK * EPI_ROWS * 4;
+    constexpr int PSLOTS =
+        L::PWARP_BYTES / PART_BYTES < PSLOTS_MAX ? L::PWARP_BYTES / PART_BYTES : PSLOTS_MAX;
+    static_assert(PSLOTS >= 2 && L::PWARP_BYTES % 128 == 0, "partial staging does not fit the ring");
+    uint8_t* const pstage = smem + ew * L::PWARP_BYTES;
+    uint64_t* const pbar = pfull + ew * PSLOTS_MAX;
+    uint32_t p_issued = 0, p_done = 0;
+
+    // Write one finished tile: TMEM -> registers (+ the later units' partial
+    // sums, in unit order, when ADD) -> alpha * acc + beta * C -> output.
+    // Returns false if a wait gave up.
+    auto store_tile = [&](auto add_tag, uint32_t t_row, int nb, int row0, int buf, int contrib0,
+                          int ncontrib) -> bool {
+      constexpr bool ADD = decltype(add_tag)::value;
+      const uint32_t first = p_issued;
+      const uint32_t total = ADD ? static_cast<uint32_t>(CHUNKS * ncontrib) : 0u;
+      uint64_t pol = 0;
+      // issue copies until number `upto`; copy n = first + c * ncontrib + k
+      // holds chunk c of contributing unit contrib0 + k
+      auto refill = [&](uint32_t upto) {
+        for (; p_issued < upto; ++p_issued) {
+          if (lane != 0) continue;
+          const uint32_t i = p_issued - first;
+          const int c = static_cast<int>(i) / ncontrib, k = static_cast<int>(i) % ncontrib;
+          const float* src = args.ws +
+                             static_cast<size_t>((contrib0 + k) * UNIT_CTAS + rank) * BM * BN +
+                             static_cast<size_t>(quarter) * BN * EPI_ROWS +
+                             static_cast<size_t>(c) * CHUNK * EPI_ROWS;
+          uint64_t* b = &pbar[p_issued % PSLOTS];
+          mbar_arrive_expect_tx(b, PART_BYTES);
+          bulk_load_g2s(pstage + (p_issued % PSLOTS) * PART_BYTES, src, PART_BYTES, b, pol);
+        }
+      };
+      if (ADD) {
+        if (lane == 0) {
+          pol = policy_evict_first();
+          fence_proxy_async_global();   // the partials were published by other CTAs
+        }
+        refill(first + (total < static_cast<uint32_t>(PSLOTS) ? total : PSLOTS));
+      }
+#pragma unroll 1
+      for (int c = 0; c < CHUNKS; ++c) {
+        const int col0 = nb * BN + c * CHUNK;
+        uint8_t* stg;
+        if (!begin_chunk<PAIR, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args))
+          return false;
+        // A chunk that crosses the right edge of C when N * sizeof(out) is not a
+        // multiple of 16 bytes is written with predicated plain stores: the
+        // tensor store writes whole 16-byte pieces and would touch the columns
+        // just past N.  Chunks entirely right of N are not stored at all.
+        const bool ragged = args.n_ragged && (col0 + CHUNK > args.N);
+        const bool skip_store = col0 >= args.N || row0 >= args.M;
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(t_row, v0, c * CHUNK);
+        if (CHUNK == 64) tmem_ld_32x32b_x32(t_row, v1, c * CHUNK + 32);
+        tmem_ld_wait();
+        if (c == CHUNKS - 1) {
+          // accumulator fully read: hand it back to the MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader)
+              mbar_arrive(&tempty[buf]);
+            else
+              mbar_arrive_cluster(map_to_rank(&tempty[buf], 0));
+          }
+        }
+        if (ADD) {
+          for (int k = 0; k < ncontrib; ++k) {
+            const uint32_t n = first + static_cast<uint32_t>(c * ncontrib + k);
+            if (!wait_warp(&pbar[n % PSLOTS], (n / PSLOTS) & 1, abort_flag, args,
+                           SITE_STREAMK_FLAG))
+              return false;
+            // staged as [CHUNK/4 pieces][32 rows][16 B]: conflict-free rows
+            const uint32_t pb = smem_u32(pstage + (n % PSLOTS) * PART_BYTES) + r * 16;
+#pragma unroll
+            for (int q = 0; q < CHUNK / 4; ++q) {
+              const uint4 pv = ld_shared_v4(pb + q * EPI_ROWS * 16);
+              uint32_t* a = q < 8 ? v0 + 4 * q : v1 + 4 * (q - 8);
+              a[0] = __float_as_uint(__uint_as_float(a[0]) + __uint_as_float(pv.x));
+              a[1] = __float_as_uint(__uint_as_float(a[1]) + __uint_as_float(pv.y));
+              a[2] = __float_as_uint(__uint_as_float(a[2]) + __uint_as_float(pv.z));
+              a[3] = __float_as_uint(__uint_as_float(a[3]) + __uint_as_float(pv.w));
+            }
+            __syncwarp();
+            if (lane == 0) fence_proxy_async_smem();   // slot reads before its next copy
+            p_done = n + 1;
+            refill(p_done + PSLOTS < first + total ? p_done + PSLOTS : first + total);
+          }
+        }
+        uint8_t* rowp = stg + r * SW;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {   // 16-byte pieces of the 128-byte row
+          uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
+          constexpr int E = OUT == OUT_F32 ? 4 : 8;
+          float x[E];
+          const uint32_t* src = (OUT == OUT_F32) ? (v0 + 4 * j) : ((j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4)));
+#pragma unroll
+          for (int e = 0; e < E; ++e) x[e] = __uint_as_float(src[e]);
+          finish_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
+                            col0 + E * j);
+        }
+        end_chunk(st, stg, &tmC, row0, col0, ragged, skip_store);
+      }
+      return true;
+    };
     WorkIter wi;
     WorkItem w;
     work_begin(wi);
@@ -628,15 +751,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         continue;   // one tile per split-K cluster; phase 2 runs after the cluster barrier
       }
-      const int prow = quarter * 32 + r;   // this thread's row of the CTA's 128
       if (w.g0 > 0) {
         // Stream-K segment that does not hold its tile's first k-groups: publish
-        // the fp32 partial sum in this CTA's scratch slot, laid out
-        // [BN/4][128 rows][4] so a warp's 16-byte stores cover 512 contiguous
-        // bytes, hand the accumulator back, then release the CTA's flag with the
-        // launch epoch.  Such a segment is the first (or only) one of its unit, so
-        // it is published early.
-        float4* slot = reinterpret_cast<float4*>(args.ws + static_cast<size_t>(blockIdx.x) * BM * BN);
+        // the fp32 partial sum in this CTA's scratch slot, hand the accumulator
+        // back, then release the CTA's flag with the launch epoch.  Such a
+        // segment is the first (or only) one of its unit, so it is published
+        // early.  Slot layout [quarter][BN/4 pieces][32 rows][4 floats]: a warp's
+        // store covers 512 contiguous bytes and each epilogue warp's rows form
+        // one contiguous span, which the owner fetches with bulk copies.
+        float4* slot = reinterpret_cast<float4*>(args.ws + static_cast<size_t>(blockIdx.x) * BM * BN) +
+                       quarter * (BN / 4) * EPI_ROWS;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
@@ -644,7 +768,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            slot[(c * 8 + j) * BM + prow] =
+            slot[(c * 8 + j) * EPI_ROWS + r] =
                 make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
         }
@@ -656,6 +780,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           else
             mbar_arrive_cluster(map_to_rank(&tempty[buf], 0));
         }
+        fence_proxy_async_global();   // the owner reads the slot with bulk copies
         __threadfence();
         if (!epilogue_sync()) {
           ok = false;
@@ -665,8 +790,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;
       }
       // A stream-K segment holding its tile's first k-groups but not the last
-      // ones (the last segment of its unit) owns the tile: the units after it in
-      // the iteration space hold the later k-groups as partial sums.
+      // ones owns the tile: the units after it in the iteration space hold the
+      // later k-groups as partial sums.  It is always the last segment of its
+      // unit, so the ring is idle once its accumulator is complete.
       int contrib0 = unit0, contrib1 = unit0;
       if (w.g1 < args.groups) {
         const long long base = static_cast<long long>(w.tile - args.dp_tiles) * args.groups;
@@ -692,66 +818,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
       }
-#pragma unroll 1
-      for (int c = 0; c < CHUNKS; ++c) {
-        const int col0 = nb * BN + c * CHUNK;
-        uint8_t* stg;
-        if (!begin_chunk<PAIR, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args)) {
-          ok = false;
-          break;
-        }
-        // A chunk that crosses the right edge of C when N * sizeof(out) is not a
-        // multiple of 16 bytes is written with predicated plain stores: the
-        // tensor store writes whole 16-byte pieces and would touch the columns
-        // just past N.  Chunks entirely right of N are not stored at all.
-        const bool ragged = args.n_ragged && (col0 + CHUNK > args.N);
-        const bool skip_store = col0 >= args.N || row0 >= args.M;
-        uint32_t v0[32], v1[32];
-        tmem_ld_32x32b_x32(t_row, v0, c * CHUNK);
-        if (CHUNK == 64) tmem_ld_32x32b_x32(t_row, v1, c * CHUNK + 32);
-        tmem_ld_wait();
-        if (c == CHUNKS - 1) {
-          // accumulator fully read: hand it back to the MMA issuer
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            if (leader)
-              mbar_arrive(&tempty[buf]);
-            else
-              mbar_arrive_cluster(map_to_rank(&tempty[buf], 0));
-          }
-        }
-        uint8_t* rowp = stg + r * SW;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {   // 16-byte pieces of the 128-byte row
-          uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
-          constexpr int E = OUT == OUT_F32 ? 4 : 8;
-          float x[E];
-          const uint32_t* src = (OUT == OUT_F32) ? (v0 + 4 * j) : ((j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4)));
-#pragma unroll
-          for (int e = 0; e < E; ++e) x[e] = __uint_as_float(src[e]);
-          // stream-K owner: add the later units' partials, in unit order
-          for (int u = contrib0; u < contrib1; ++u) {
-            const float4* slot =
-                reinterpret_cast<const float4*>(args.ws + static_cast<size_t>(u * UNIT_CTAS + rank) * BM * BN);
-#pragma unroll
-            for (int h = 0; h < E / 4; ++h) {
-              const float4 pv = __ldcg(slot + ((c * CHUNK + E * j) / 4 + h) * BM + prow);
-              x[4 * h + 0] += pv.x;
-              x[4 * h + 1] += pv.y;
-              x[4 * h + 2] += pv.z;
-              x[4 * h + 3] += pv.w;
-            }
-          }
-          finish_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
-                            col0 + E * j);
-        }
-        end_chunk(st, stg, &tmC, row0, col0, ragged, skip_store);
-      }
+      const int ncontrib = contrib1 - contrib0;
+      ok = ncontrib == 0 ? store_tile(BoolC<false>{}, t_row, nb, row0, buf, 0, 0)
+                         : store_tile(BoolC<true>{}, t_row, nb, row0, buf, contrib0, ncontrib);
     }
     if (!SPLITK) {
       if (!ok && st.pending_cload >= 0 && lane == 0)
         wait_drain<PAIR>(&st.cload[st.pending_cload], st.pending_phase, args);
+      if (!ok && lane == 0)   // partial copies still landing in the ring
+        for (uint32_t n = p_done; n < p_issued; ++n) wait_drain(&pbar[n % PSLOTS], (n / PSLOTS) & 1, args);
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
     }

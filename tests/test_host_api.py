@@ -111,15 +111,19 @@ def test_no_cpu_fallback_without_device(g):
 
 @pytest.mark.parametrize("shape,layout,expect", [
     # big squares: CTA-pair tiles of 256 x 256 (one cta_group::2 MMA over two SMs)
-    # one wave of 64 pair tiles on 76 pairs: stream-K over all of them
-    ((2048, 2048, 2048, 0, 2), 0, dict(cta_group=2, bm=256, bn=256, num_tiles=64, grid=152,
+    # one wave of 64 pair tiles on 76 pairs: data-parallel, one tile per pair
+    ((2048, 2048, 2048, 0, 2), 0, dict(cta_group=2, bm=256, bn=256, num_tiles=64, grid=128,
                                        k_blocks=32, b_mn=1, stages=3, bk=128, groups=16,
-                                       dp_tiles=0, sk_iters=1024)),
-    # 3.37 waves: two data-parallel waves, the remaining 104 tiles stream-K
+                                       dp_tiles=64, sk_iters=0, scratch_bytes=0)),
+    # 3.37 waves, the last one 37% full: two data-parallel waves, the remaining
+    # 104 tiles stream-K
     ((4096, 4096, 4096, 1, 1), 0, dict(cta_group=2, bn=256, num_tiles=256, grid=152,
                                        dp_tiles=152, sk_iters=104 * 32)),
+    # 1.89 waves (last one 89% full) and 13.5 waves: data-parallel
+    ((3072, 3072, 4096, 1, 1), 0, dict(cta_group=2, bn=256, num_tiles=144, grid=152,
+                                       dp_tiles=144, sk_iters=0)),
     ((8192, 8192, 8192, 1, 2), 2, dict(cta_group=2, bn=256, num_tiles=1024, grid=152, b_mn=0,
-                                       dp_tiles=912, sk_iters=112 * 64)),
+                                       dp_tiles=1024, sk_iters=0)),
     # a single 128-row panel with long K: 128-wide tiles, K split over 2-CTA clusters
     ((128, 8192, 8192, 1, 1), 2, dict(cta_group=1, bm=128, bn=128, num_tiles=64, grid=128,
                                       k_blocks=128, stages=3, split_k=2)),
