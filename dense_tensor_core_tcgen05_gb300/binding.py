@@ -16,10 +16,12 @@ LIB_PATH = os.path.join(_PKG, "libgemm_tcgen05.so")
 GEMM_F16, GEMM_BF16, GEMM_F32 = 0, 1, 2
 GEMM_A_ROW, GEMM_A_COL, GEMM_B_ROW, GEMM_B_COL = 0, 1, 0, 2
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ARCH, GEMM_ERR_CUDA, \
-    GEMM_ERR_TIMEOUT = range(6)
+    GEMM_ERR_TIMEOUT, GEMM_ERR_SCRATCH = range(7)
+GEMM_NOALLOC_SCRATCH_BYTES = 24 * 1024 * 1024
 
 # Symbols declared in include/gemm_tcgen05.h.
-EXPORTS = ("gemm", "gemm_ex", "gemm_host", "gemm_status_string", "gemm_sync_status",
+EXPORTS = ("gemm", "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_status_string",
+           "gemm_sync_status",
            "gemm_debug_set", "gemm_plan", "gemm_tile_coord", "gemm_work_items",
            "gemm_encode_idesc", "gemm_encode_sdesc", "gemm_version")
 
@@ -59,6 +61,8 @@ def _load():
     lib.gemm.restype = ci
     lib.gemm_ex.argtypes = gemm_args + [ctypes.POINTER(gemm_config_t)]
     lib.gemm_ex.restype = ci
+    lib.gemm_ex_noalloc.argtypes = gemm_args + [ctypes.POINTER(gemm_config_t)]
+    lib.gemm_ex_noalloc.restype = ci
     lib.gemm_host.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ci, ci, ci,
                               vp, vp, vp, vp]
     lib.gemm_host.restype = ci
@@ -118,6 +122,14 @@ def gemm_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, l
             cfg=None):
     return _lib.gemm_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
                         stream, _cfg(cfg))
+
+
+def gemm_ex_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
+                    stream, cfg=None):
+    """gemm_ex with stream-K scratch taken from the library's fixed per-device
+    buffer instead of cudaMalloc (calls that overlap on the device race)."""
+    return _lib.gemm_ex_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype,
+                                layout, stream, _cfg(cfg))
 
 
 def gemm_host(M, N, K, alpha, hA, lda, hB, ldb, beta, hC, ldc, in_dtype, out_dtype, layout,

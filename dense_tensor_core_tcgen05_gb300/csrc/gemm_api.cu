@@ -108,6 +108,49 @@ gemm_status_t scratch_for(int dev, cudaStream_t st, size_t slot_bytes, int ctas,
   return GEMM_OK;
 }
 
+// Fixed stream-K scratch of gemm_ex_noalloc, for callers that must not
+// allocate device memory on the call path (their memory is held by another
+// allocator, or their loop must not synchronise or fail on cudaMalloc): a
+// file-scope device array, one per device, laid out like the cached scratch
+// (kFlagBytes of ready flags, then the fp32 partial slots).  Every call on a
+// device shares it, so calls that overlap on the device race.
+constexpr size_t kNoAllocScratchBytes = GEMM_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoAllocScratchBytes > kFlagBytes, "the fixed scratch must hold the flags");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocScratch {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  void* ptr = nullptr;
+  bool cleared = false;
+  unsigned int epoch = 0;
+};
+NoAllocScratch g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Set-up, once per device with that device current: the array's device
+// address.  The flags are cleared on the stream of the first launch that uses
+// them (and again when the epoch wraps), then every launch takes the next epoch.
+gemm_status_t noalloc_scratch(int dev, cudaStream_t st, size_t need, float** ws,
+                              unsigned int** flags, unsigned int* epoch) {
+  if (need > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH;
+  NoAllocScratch& n = g_noalloc[dev];
+  std::call_once(n.once, [&n]() {
+    n.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&n.ptr), g_noalloc_scratch);
+  });
+  if (n.err != cudaSuccess || n.ptr == nullptr) return GEMM_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!n.cleared || ++n.epoch == 0) {
+    if (cudaMemsetAsync(n.ptr, 0, kFlagBytes, st) != cudaSuccess) return GEMM_ERR_CUDA;
+    n.cleared = true;
+    n.epoch = 1;
+  }
+  *flags = static_cast<unsigned int*>(n.ptr);
+  *ws = reinterpret_cast<float*>(static_cast<char*>(n.ptr) + kFlagBytes);
+  *epoch = n.epoch;
+  return GEMM_OK;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   std::call_once(g_encode_once, []() {
     void* fn = nullptr;
@@ -373,7 +416,8 @@ gemm_status_t launch_scale(void* C, int64_t ldc, int64_t M, int64_t N, float bet
 
 gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                        const void* B, int64_t ldb, float beta, void* C, int64_t ldc, int in_dtype,
-                       int out_dtype, int layout, void* stream_v, const gemm_config_t* cfg) {
+                       int out_dtype, int layout, void* stream_v, const gemm_config_t* cfg,
+                       bool fixed_scratch = false) {
   bool quick = false;
   gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, layout, &quick);
   if (s != GEMM_OK || quick) return s;
@@ -459,7 +503,10 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.dp_tiles = p.dp_tiles;
   ka.sk_iters = p.sk_iters;
   if (p.sk_iters) {
-    s = scratch_for(dev, stream, size_t(BM) * p.bn * 4, p.grid, &ka.ws, &ka.ws_flags, &ka.epoch);
+    s = fixed_scratch ? noalloc_scratch(dev, stream, static_cast<size_t>(p.scratch_bytes), &ka.ws,
+                                        &ka.ws_flags, &ka.epoch)
+                      : scratch_for(dev, stream, size_t(BM) * p.bn * 4, p.grid, &ka.ws,
+                                    &ka.ws_flags, &ka.epoch);
     if (s != GEMM_OK) return s;
   }
 
@@ -511,6 +558,14 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, float alpha, const void* 
                   stream, cfg);
 }
 
+gemm_status_t gemm_ex_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                              int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                              int64_t ldc, int in_dtype, int out_dtype, int layout, void* stream,
+                              const gemm_config_t* cfg) {
+  return run_gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
+                  stream, cfg, /*fixed_scratch=*/true);
+}
+
 gemm_status_t gemm_host(int64_t M, int64_t N, int64_t K, float alpha, const void* hA, int64_t lda,
                         const void* hB, int64_t ldb, float beta, void* hC, int64_t ldc,
                         int in_dtype, int out_dtype, int layout, void* dA, void* dB, void* dC,
@@ -554,6 +609,8 @@ const char* gemm_status_string(gemm_status_t status) {
     case GEMM_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
     case GEMM_ERR_CUDA: return "CUDA runtime or driver error";
     case GEMM_ERR_TIMEOUT: return "a kernel wait timed out";
+    case GEMM_ERR_SCRATCH:
+      return "the launch needs more stream-K scratch than gemm_ex_noalloc's fixed buffer holds";
     default: return "unknown status";
   }
 }

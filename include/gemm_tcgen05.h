@@ -64,7 +64,9 @@ typedef enum {
   GEMM_ERR_ARCH = 3,        /* current device is not compute capability 10.3 */
   GEMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (no device,
                                launch failure, tensor-map encoding failure) */
-  GEMM_ERR_TIMEOUT = 5      /* a kernel wait gave up (see gemm_sync_status) */
+  GEMM_ERR_TIMEOUT = 5,     /* a kernel wait gave up (see gemm_sync_status) */
+  GEMM_ERR_SCRATCH = 6      /* gemm_ex_noalloc only: the launch needs more scratch
+                               than its fixed buffer holds */
 } gemm_status_t;
 
 /*
@@ -123,6 +125,39 @@ typedef struct {
 gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                       const void* B, int64_t ldb, float beta, void* C, int64_t ldc, int in_dtype,
                       int out_dtype, int layout, void* stream, const gemm_config_t* cfg);
+
+/*
+ * gemm_ex_noalloc -- gemm_ex that never allocates device memory.
+ *
+ * The pages have no counterpart: this entry point exists for callers that must
+ * not allocate on the call path.  gemm_ex obtains a stream-K launch's scratch
+ * (ready flags and fp32 partial tiles) from cudaMalloc the first time a stream
+ * needs it (and again, after a cudaFree that synchronises the stream, when it
+ * needs more).  A caller whose device memory is fully held by another
+ * allocator, or whose steady-state loop must not synchronise or fail on
+ * allocation, cannot accept that.  Here the scratch is a fixed device array of
+ * GEMM_NOALLOC_SCRATCH_BYTES per device, built into the library.
+ *
+ * Same arguments, planning, kernels, results and errors as gemm_ex, plus:
+ *  - GEMM_ERR_SCRATCH when the plan's scratch (gemm_plan_t.scratch_bytes)
+ *    exceeds GEMM_NOALLOC_SCRATCH_BYTES (nothing is enqueued).  Plans without
+ *    stream-K use no scratch and are never rejected.  A stream-K plan needs
+ *    4 KB + (CTAs) * 128 * bn * 4 bytes with at most one CTA per SM, so on a
+ *    152-SM GB300 the largest is 19.0 MiB and every plan fits.
+ *  - Set-up: the first call on a device (that device current) looks up the
+ *    array's device address and enqueues, on that call's stream, a clear of its
+ *    4 KB of ready flags; make that first call before any stream capture.
+ *  - The one array is shared by every call on the device: calls that may
+ *    overlap on the device (different streams with no ordering between them,
+ *    or several host threads) race on it and must be serialised by the caller.
+ *    gemm_ex keeps its own per-stream scratch and does not touch this array.
+ */
+enum { GEMM_NOALLOC_SCRATCH_BYTES = 24 * 1024 * 1024 };
+
+gemm_status_t gemm_ex_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                              int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                              int64_t ldc, int in_dtype, int out_dtype, int layout, void* stream,
+                              const gemm_config_t* cfg);
 
 /*
  * gemm_host -- the same GEMM on HOST operands (end-to-end path).
