@@ -57,6 +57,7 @@ enum WaitSite {
   SITE_EPI_C_LOAD = 5,
   SITE_DRAIN = 6,
   SITE_STREAMK_FLAG = 7,
+  SITE_SPLITK_SLICES = 8,
 };
 
 // Shared-memory map of one CTA.  A ring stage holds KO consecutive k-blocks
@@ -84,8 +85,9 @@ struct SmemLayout {
   static constexpr int RING_BYTES = off_epi;
   static constexpr int PWARP_BYTES = RING_BYTES / EPI_WARPS;
   // full[STAGES], empty[STAGES], tfull[2], tempty[2], cload[EPI_WARPS*EPI_BUFS], drain, esync,
-  // pfull[EPI_WARPS*PSLOTS_MAX]
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 2 + EPI_WARPS * PSLOTS_MAX;
+  // pfull[EPI_WARPS*PSLOTS_MAX], rfull
+  static constexpr int NUM_BARS =
+      2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 2 + EPI_WARPS * PSLOTS_MAX + 1;
   static constexpr int off_tmem = off_bar + NUM_BARS * 8;
   static constexpr int off_flag = off_tmem + 8;
   static constexpr int BYTES = off_flag + 8;
@@ -305,11 +307,12 @@ __device__ __forceinline__ void end_chunk(EpiState& st, const uint8_t* stg, cons
   ++st.chunk_ctr;
 }
 
-// Shared-memory address (this CTA) of 16-byte piece `piece` of row `row` in the
-// fp32 split-K partial buffer (rows of BN floats, pieces XOR-swizzled by row).
-template <int BN>
-__device__ __forceinline__ uint32_t partial_addr(uint32_t base, int row, int piece) {
-  return base + static_cast<uint32_t>(row * (BN * 4) + ((piece ^ (row & 7)) << 4));
+// Shared-memory address of 16-byte piece `piece` of row `row` in a split-K
+// slice block (128 rows of SLICE floats; pieces XOR-swizzled by row, so the 32
+// rows of a warp touch every bank once per 8 rows).
+template <int SLICE>
+__device__ __forceinline__ uint32_t slice_addr(uint32_t base, int row, int piece) {
+  return base + static_cast<uint32_t>(row * (SLICE * 4) + ((piece ^ (row & 7)) << 4));
 }
 
 // Stream-K hand-off: a CTA publishes its partial tile with a release store of
@@ -324,15 +327,6 @@ __device__ __forceinline__ unsigned int flag_acquire(const unsigned int* f) {
   return v;
 }
 
-
-__device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
@@ -362,8 +356,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be in [16,256], N%16==0");
   static_assert(!(PAIR && SPLITK), "pair and split-K modes are exclusive");
   static_assert(!SPLITK || SLICE % CHUNK == 0, "each split CTA reduces whole epilogue chunks");
-  static_assert(!SPLITK || STAGES * L::STAGE_BYTES >= BM * BN * 4,
-                "the fp32 partial tile must fit in the ring's shared memory");
+  // split-K: the fp32 slices a CTA sends to its SPLIT-1 peers and the ones it
+  // receives from them share the (idle) ring
+  constexpr int SLICE_BYTES = BM * SLICE * 4;
+  static_assert(!SPLITK || 2 * (SPLIT - 1) * SLICE_BYTES <= STAGES * L::STAGE_BYTES,
+                "the split-K slices must fit in the ring's shared memory");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -377,6 +374,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* drain = cload + EPI_WARPS * EPI_BUFS;
   uint64_t* esync = drain + 1;   // rendezvous of the four epilogue warps (stream-K hand-off)
   uint64_t* pfull = esync + 1;   // stream-K partial staging slots, PSLOTS_MAX per epilogue warp
+  uint64_t* rfull = pfull + EPI_WARPS * PSLOTS_MAX;   // split-K: the peers' slices have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_tmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_flag);
 
@@ -422,6 +420,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(drain, 1);
     mbar_init(esync, EPI_WARPS);
     for (int i = 0; i < EPI_WARPS * PSLOTS_MAX; ++i) mbar_init(&pfull[i], 1);
+    mbar_init(rfull, 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -735,20 +734,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              static_cast<uint32_t>(buf * BN);
       const int row0 = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32;
       if (SPLITK) {
-        // Phase 1: this CTA's fp32 partial sum -> its own shared memory (the
-        // ring is idle: every MMA that read it has completed).
-        const uint32_t pbase = smem_u32(smem);
+        // Phase 1: this CTA's fp32 partial of every peer's column slice ->
+        // this CTA's ring (idle: every MMA that read it has completed), one
+        // contiguous [128 rows][SLICE] block per peer, 16-byte pieces
+        // XOR-swizzled by row; the blocks are bulk-copied to the peers after
+        // the cluster barrier.  The CTA's own slice stays in TMEM.
         const int prow = quarter * 32 + r;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(t_row, v, c * 32);
-          tmem_ld_wait();
+        for (int qi = 0; qi < SPLIT - 1; ++qi) {
+          const int q = qi < static_cast<int>(srank) ? qi : qi + 1;
+          const uint32_t sbase = smem_u32(smem) + static_cast<uint32_t>(qi * SLICE_BYTES);
+#pragma unroll 1
+          for (int c = 0; c < SLICE / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_row, v, q * SLICE + c * 32);
+            tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_v4(partial_addr<BN>(pbase, prow, c * 8 + j),
-                         make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            for (int j = 0; j < 8; ++j)
+              st_shared_v4(slice_addr<SLICE>(sbase, prow, c * 8 + j),
+                           make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+          }
         }
+        fence_proxy_async_smem();   // read next by the bulk copies
         continue;   // one tile per split-K cluster; phase 2 runs after the cluster barrier
       }
       if (w.g0 > 0) {
@@ -827,7 +834,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         wait_drain<PAIR>(&st.cload[st.pending_cload], st.pending_phase, args);
       if (!ok && lane == 0)   // partial copies still landing in the ring
         for (uint32_t n = p_done; n < p_issued; ++n) wait_drain(&pbar[n % PSLOTS], (n / PSLOTS) & 1, args);
-      if (lane == 0) bulk_wait_group<0>();
+      // the staging buffers must be read out before the CTA exits; the grid's
+      // completion makes the stores themselves visible
+      if (lane == 0) bulk_wait_group_read<0>();
       __syncwarp();
     }
   }
@@ -835,10 +844,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (SPLITK) {
-    // Phase 2: every partial is in its CTA's shared memory.  CTA `srank` sums
-    // columns [srank*SLICE, (srank+1)*SLICE) of the tile over the SPLIT partials
-    // in rank order (deterministic), then finishes them like the plain epilogue.
+    // Phase 2.  CTA `srank` finishes columns [srank*SLICE, (srank+1)*SLICE) of
+    // the tile: after the cluster barrier (every CTA's blocks staged and its ring
+    // idle) each CTA bulk-copies its block for every peer into that peer's
+    // receive area, counted on the peer's rfull; then it sums its own slice
+    // (from TMEM) and the received ones in rank order (deterministic) and
+    // finishes them like the plain epilogue.  The copies are sent even after an
+    // abort, so a peer never waits for a block that will not come.
+    constexpr uint32_t RECV0 = (SPLIT - 1) * SLICE_BYTES;   // receive area, after the send area
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(rfull, (SPLIT - 1) * SLICE_BYTES);
     cluster_sync();
+    if (threadIdx.x == 0) {
+      const uint32_t base = smem_u32(smem);
+      for (int qi = 0; qi < SPLIT - 1; ++qi) {
+        const uint32_t q = qi < static_cast<int>(srank) ? qi : qi + 1;
+        const uint32_t slot = srank < q ? srank : srank - 1;   // this CTA among q's peers
+        bulk_copy_s2cluster(map_addr_to_rank(base + RECV0 + slot * SLICE_BYTES, q),
+                            base + static_cast<uint32_t>(qi) * SLICE_BYTES, SLICE_BYTES,
+                            map_addr_to_rank(smem_u32(rfull), q));
+      }
+    }
+    bool received = false;
     if (warp >= EPI_WARP0 && !*abort_flag && unit0 < args.num_tiles) {
       const int ew = warp - EPI_WARP0;
       const int quarter = warp & 3;
@@ -849,8 +875,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tile_coord(unit0, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
       const int row0 = mb * BM + quarter * 32;
       const int prow = quarter * 32 + r;
-      const uint32_t pbase = smem_u32(smem);
-      bool ok = true;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+      const uint32_t rbase = smem_u32(smem) + RECV0;
+      bool ok = wait_warp<true>(rfull, 0, abort_flag, args, SITE_SPLITK_SLICES);
+      received = ok;
 #pragma unroll 1
       for (int c = 0; ok && c < SLICE / CHUNK; ++c) {
         const int tcol = static_cast<int>(srank) * SLICE + c * CHUNK;   // column inside the tile
@@ -862,24 +890,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const bool ragged = args.n_ragged && (col0 + CHUNK > args.N);
         const bool skip_store = col0 >= args.N || row0 >= args.M;
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(t_row, v0, tcol);
+        if (CHUNK == 64) tmem_ld_32x32b_x32(t_row, v1, tcol + 32);
+        tmem_ld_wait();
         uint8_t* rowp = stg + r * SW;
+        constexpr int E = OUT == OUT_F32 ? 4 : 8;   // outputs per 16-byte piece
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          constexpr int E = OUT == OUT_F32 ? 4 : 8;
+          const uint32_t* own = (OUT == OUT_F32) ? (v0 + 4 * j) : ((j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4)));
           float x[E];
 #pragma unroll
           for (int e = 0; e < E; ++e) x[e] = 0.0f;
-          const int piece0 = (tcol + E * j) / 4;       // first fp32 piece of the partial row
 #pragma unroll
           for (int q = 0; q < SPLIT; ++q) {
+            if (q == static_cast<int>(srank)) {
 #pragma unroll
-            for (int h = 0; h < E / 4; ++h) {
-              const uint32_t local = partial_addr<BN>(pbase, prow, piece0 + h);
-              const uint4 pv = ld_shared_cluster_v4(map_addr_to_rank(local, q));
-              x[4 * h + 0] += __uint_as_float(pv.x);
-              x[4 * h + 1] += __uint_as_float(pv.y);
-              x[4 * h + 2] += __uint_as_float(pv.z);
-              x[4 * h + 3] += __uint_as_float(pv.w);
+              for (int e = 0; e < E; ++e) x[e] += __uint_as_float(own[e]);
+            } else {
+              const uint32_t blk = rbase + static_cast<uint32_t>((q < static_cast<int>(srank) ? q : q - 1) * SLICE_BYTES);
+#pragma unroll
+              for (int h = 0; h < E / 4; ++h) {
+                const uint4 pv = ld_shared_v4(slice_addr<SLICE>(blk, prow, (c * CHUNK + E * j) / 4 + h));
+                x[4 * h + 0] += __uint_as_float(pv.x);
+                x[4 * h + 1] += __uint_as_float(pv.y);
+                x[4 * h + 2] += __uint_as_float(pv.z);
+                x[4 * h + 3] += __uint_as_float(pv.w);
+              }
             }
           }
           uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
@@ -890,9 +927,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok && st.pending_cload >= 0 && lane == 0)
         wait_drain<true>(&st.cload[st.pending_cload], st.pending_phase, args);
-      if (lane == 0) bulk_wait_group<0>();
+      // the staging buffers must be read out before the CTA exits; the grid's
+      // completion makes the stores themselves visible
+      if (lane == 0) bulk_wait_group_read<0>();
       __syncwarp();
     }
+    // blocks still landing in this CTA's ring must arrive before it exits
+    if (warp == EPI_WARP0 && lane == 0 && !received) wait_drain<true>(rfull, 0, args);
     tc_fence_before();
     __syncthreads();
   }

@@ -116,6 +116,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, int32_t x, int32_t y,
+                                            int32_t z, int32_t w, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m, int32_t x,
                                                  int32_t y, int32_t z, uint64_t* bar,
                                                  uint64_t policy) {
@@ -183,6 +192,19 @@ __device__ __forceinline__ void bulk_load_g2s(void* dst, const void* src, uint32
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Untiled bulk copy from this CTA's shared memory into another CTA of the
+// cluster: `dst` and `bar` are shared::cluster addresses in the receiving CTA
+// (mapa), `src` a local shared address; `bytes` a multiple of 16, both
+// addresses 16-byte aligned.  Completion is counted on the receiver's barrier.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                    uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "r"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 

@@ -30,7 +30,7 @@ def build(force=False):
                                f"-I{os.path.join(_PKG, 'csrc')}", _SRC, "-o", _LIB])
     lib = ctypes.CDLL(_LIB)
     lib.probe_mma_rate.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p]
-    lib.probe_tma_stream.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 6 + [ctypes.c_void_p]
+    lib.probe_tma_stream.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 8 + [ctypes.c_void_p]
     return lib
 
 
@@ -49,12 +49,13 @@ def mma_rate(lib, n, pair, grid=152, iters=2000):
     return cyc, flop_per_sm / cyc
 
 
-def tma_stream(lib, B, grid, R, KO, S):
+def tma_stream(lib, B, grid, R, KO, S, grouped=False, promo=3):
     """(median in-kernel ns per CTA, TB/s) for streaming B [N, K] bf16."""
     import torch
     N, K = B.shape
     out = torch.zeros(grid, dtype=torch.int64, device="cuda")
-    rc = lib.probe_tma_stream(B.data_ptr(), N, K, grid, R, KO, S, out.data_ptr())
+    rc = lib.probe_tma_stream(B.data_ptr(), N, K, grid, R, KO, S, int(grouped), promo,
+                              out.data_ptr())
     if rc != 0:
         raise RuntimeError(f"probe_tma_stream rc {rc}")
     ns = statistics.median(out.cpu().tolist())
@@ -72,13 +73,18 @@ def main():
     B = torch.randn(8192, 8192, device="cuda").to(torch.bfloat16)
     flush = torch.empty(512 << 18, dtype=torch.float32, device="cuda")
     print("TMA streaming of an 8192 x 8192 K-major bf16 matrix, 128 CTAs (in-kernel time)")
-    for (R, KO, S) in ((64, 1, 16), (64, 2, 8), (64, 4, 4), (32, 4, 8), (64, 8, 3)):
+    promos = ("none", "64B", "128B", "256B")
+    for (R, KO, S, grouped, promo) in ((64, 1, 16, 0, 3), (64, 2, 8, 0, 3), (64, 2, 8, 0, 0),
+                                       (64, 2, 8, 1, 3), (64, 2, 8, 1, 0), (64, 4, 4, 0, 3),
+                                       (64, 4, 4, 1, 3), (32, 4, 8, 0, 3), (64, 8, 3, 0, 3),
+                                       (64, 8, 3, 1, 3)):
         res = []
         for _ in range(5):
             flush.zero_()
-            res.append(tma_stream(lib, B, 128, R, KO, S))
+            res.append(tma_stream(lib, B, 128, R, KO, S, grouped, promo))
         ns, tbs = sorted(res)[len(res) // 2]
-        print(f"  copy = {R:3d} rows x {KO} blocks ({KO * 128:4d} B per row), {S:2d} in flight: "
+        print(f"  copy = {R:3d} rows x {KO} blocks ({KO * 128:4d} B per row), {S:2d} in flight, "
+              f"{'8-row groups' if grouped else 'whole box   '}, L2 promotion {promos[promo]:4s}: "
               f"{ns / 1e3:6.1f} us, {tbs:4.2f} TB/s")
 
 

@@ -8,7 +8,10 @@
 //  * tma_stream: one producer thread per CTA streams a K-major [N, K] bf16 matrix
 //    through a ring of TMA tile copies of `R` rows x `KO` consecutive 64-element
 //    blocks (a 3-D map whose third dimension walks blocks along the row) -> the DRAM
-//    bandwidth a tile-copy access pattern reaches.
+//    bandwidth a tile-copy access pattern reaches.  Grouped mode: a 4-D map
+//    (64 elements, 8 rows, KO blocks, row groups) fetches the KO blocks of each
+//    group of 8 rows back to back, landing as the same 128B-swizzled K-major tile
+//    with 8-row atoms KO * 1024 B apart.  The L2 promotion of the map is a knob.
 // Every wait is bounded (1-2 s, %globaltimer); a CTA that gives up writes ~0.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -80,7 +83,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned lo
 
 __global__ void __launch_bounds__(64, 1)
     tma_stream_kernel(const __grid_constant__ CUtensorMap tm, int rows_per_cta, int R, int KO, int S,
-                      int K, unsigned long long* out) {
+                      int K, int grouped, unsigned long long* out) {
   extern __shared__ uint8_t raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   const int box_bytes = R * 128 * KO;
@@ -112,7 +115,10 @@ __global__ void __launch_bounds__(64, 1)
     if (i < total) {
       const int s = i % S, kg = i % kgroups, rb = i / kgroups;
       mbar_arrive_expect_tx(&bars[s], box_bytes);
-      tma_load_3d(smem + s * box_bytes, &tm, 0, row0 + rb * R, kg * KO, &bars[s]);
+      if (grouped)
+        tma_load_4d(smem + s * box_bytes, &tm, 0, 0, kg * KO, (row0 + rb * R) / 8, &bars[s]);
+      else
+        tma_load_3d(smem + s * box_bytes, &tm, 0, row0 + rb * R, kg * KO, &bars[s]);
     }
   }
   out[blockIdx.x] = globaltimer_ns() - t0;
@@ -157,11 +163,14 @@ extern "C" int probe_mma_rate(int n, int pair, int grid, int iters, unsigned lon
 
 // Nanoseconds per CTA to stream B ([N, K] bf16, row pitch K, 16-byte aligned) with
 // copies of R rows x KO blocks of 64 elements, S copies in flight per CTA, grid
-// CTAs each owning N / grid rows.  Requires K % (64 * KO) == 0, (N / grid) % R == 0,
-// R <= 256, KO * 64 * 2 * ... <= 227 KB of ring.  Returns 0 or a negative error.
+// CTAs each owning N / grid rows.  grouped: 4-D map in 8-row groups (see top);
+// promo: L2 promotion 0 none, 1 64 B, 2 128 B, 3 256 B.  Requires
+// K % (64 * KO) == 0, (N / grid) % R == 0, R % 8 == 0, R <= 256, the ring within
+// 227 KB.  Returns 0 or a negative error.
 extern "C" int probe_tma_stream(const void* B, int N, int K, int grid, int R, int KO, int S,
-                                unsigned long long* dout) {
-  if (grid <= 0 || N % grid || (N / grid) % R || R > 256 || R % 8 || KO < 1 || K % (64 * KO) || S < 1)
+                                int grouped, int promo, unsigned long long* dout) {
+  if (grid <= 0 || N % grid || (N / grid) % R || R > 256 || R % 8 || KO < 1 || K % (64 * KO) ||
+      S < 1 || promo < 0 || promo > 3 || N % 8)
     return -10;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
@@ -171,12 +180,20 @@ extern "C" int probe_tma_stream(const void* B, int N, int K, int grid, int R, in
     return -1;
   auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   CUtensorMap tm;
-  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 64)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(R), static_cast<cuuint32_t>(KO)};
-  cuuint32_t es[3] = {1, 1, 1};
-  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUtensorMapL2promotion pr[4] = {CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B};
+  const cuuint64_t ld = static_cast<cuuint64_t>(K) * 2;
+  cuuint64_t dims3[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 64)};
+  cuuint64_t strides3[2] = {ld, 128};
+  cuuint32_t box3[3] = {64, static_cast<cuuint32_t>(R), static_cast<cuuint32_t>(KO)};
+  cuuint64_t dims4[4] = {64, 8, static_cast<cuuint64_t>(K / 64), static_cast<cuuint64_t>(N / 8)};
+  cuuint64_t strides4[3] = {ld, 128, 8 * ld};
+  cuuint32_t box4[4] = {64, 8, static_cast<cuuint32_t>(KO), static_cast<cuuint32_t>(R / 8)};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, grouped ? 4 : 3, const_cast<void*>(B),
+          grouped ? dims4 : dims3, grouped ? strides4 : strides3, grouped ? box4 : box3, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, pr[promo],
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return -2;
   const int smem = S * R * 128 * KO + 1024 + 8 * S + 64;
@@ -184,7 +201,7 @@ extern "C" int probe_tma_stream(const void* B, int N, int K, int grid, int R, in
   if (cudaFuncSetAttribute(tma_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return -3;
-  tma_stream_kernel<<<grid, 64, smem>>>(tm, N / grid, R, KO, S, K, dout);
+  tma_stream_kernel<<<grid, 64, smem>>>(tm, N / grid, R, KO, S, K, grouped, dout);
   if (cudaGetLastError() != cudaSuccess) return -4;
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -5;
 }

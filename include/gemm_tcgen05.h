@@ -181,7 +181,7 @@ const char* gemm_status_string(gemm_status_t status);
 /*
  * gemm_sync_status -- synchronise `stream`, then report whether any GEMM kernel
  * on the current device gave up a wait since the last call.  Returns GEMM_OK,
- * GEMM_ERR_TIMEOUT (and stores the internal wait-site code, 1..6, in *site when
+ * GEMM_ERR_TIMEOUT (and stores the internal wait-site code, 1..8, in *site when
  * site != NULL; the word is then cleared), or GEMM_ERR_CUDA if the
  * synchronisation itself failed.  Meant for tests and benchmarks.
  */
