@@ -6,8 +6,10 @@
 
 A step is one GEMM C <- alpha*A*B + beta*C of the chosen workload (default: the
 2048^3 fp16 -> fp32 workload) with operands already resident in HBM.  Between
-timed steps L2 is flushed by writing a buffer larger than L2, and only the GEMM
-launch is inside each step's CUDA-event pair (on the stream the kernel runs on).
+timed steps L2 is flushed by writing a buffer larger than L2 and then reading it
+back (so L2 holds clean lines of the flush buffer, not dirty ones whose write-back
+would be charged to the next step), and only the GEMM launch is inside each
+step's CUDA-event pair (on the stream the kernel runs on).
 Value = whole-job TFLOP/s (2MNK per step, logical FLOPs) over all ranks.
 
 Besides value and ms_per_step the line carries: the roofline of the GEMM kernel
@@ -51,6 +53,23 @@ CSRC = os.path.join(ROOT, "dense_tensor_core_tcgen05_gb300", "csrc")
 
 
 # ------------------------------------------------------------------ helpers
+
+class L2Flush:
+    """Evicts everything of the timed problem from L2 between steps: writes a
+    buffer larger than L2, then reads it back (a column sum), so the next step
+    starts with a cold L2 holding only clean lines."""
+
+    def __init__(self, device):
+        import torch
+        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.rows = self.buf.view(-1, 1 << 16)
+        self.sink = torch.empty(1 << 16, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        import torch
+        self.buf.zero_()
+        torch.sum(self.rows, dim=0, out=self.sink)
+
 
 def gemm_flops(M, N, K):
     """Logical FLOPs, 2MNK (one multiply and one add per inner-loop step)."""
@@ -214,7 +233,7 @@ def time_gemm(g, w, a, b, c, c0, steps, warmup, stream, flush):
         for i in range(warmup + steps):
             if c0 is not None:
                 c.copy_(c0)
-            flush.zero_()
+            flush()
             if i >= warmup:
                 evs[i - warmup][0].record(st)
             g.matmul(a, b, c, alpha=w["alpha"], beta=w["beta"], a_col=w["a_col"],
@@ -293,7 +312,7 @@ def run_ours(args, rank, world, device):
     peaks, peak_src = load_peaks()
     torch.cuda.set_device(device)
     w, a, b, c, c0 = make_device_problem(cfg, device)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(device)
     st = torch.cuda.current_stream(device)
     # correctness launch on a NaN-poisoned output before timing
     c.fill_(float("nan"))
@@ -348,7 +367,7 @@ def run_ours(args, rank, world, device):
                       "layout": ("A col" if w["a_col"] else "A row") + ", " +
                                 ("B col" if w["b_col"] else "B row"),
                       "alpha": w["alpha"], "beta": w["beta"],
-                      "l2": "flushed between timed steps (512 MiB write, outside the events)",
+                      "l2": "flushed between timed steps (512 MiB write, then read back; outside the events)",
                       "parallelism": f"replicas x{world}"},
            "median_ms": statistics.median(times), "min_ms": min(times),
            "wall_s_timed_region": t_wall,
@@ -378,7 +397,7 @@ def time_cublas(w, a, b, steps, warmup, flush):
     bb = b.t() if w["b_col"] else b      # [K, N] view of B (column-major when b_col)
     evs = []
     for i in range(warmup + steps):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         torch.matmul(a, bb)
@@ -395,7 +414,7 @@ def run_suite(g, args, device, peaks, skip_cfg):
     cuBLAS time sits next to it."""
     import torch
     res = {}
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(device)
     for cfg in sorted(si.WORKLOADS):
         w, a, b, c, c0 = make_device_problem(cfg, device)
         times = time_gemm(g, w, a, b, c, c0, 20, 5, torch.cuda.current_stream(device), flush)

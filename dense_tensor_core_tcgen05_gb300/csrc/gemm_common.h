@@ -87,8 +87,11 @@ struct WorkIter {
     groups = groups_;
     next_dp = unit;
     sk_iters = sk_iters_;
-    i = (static_cast<long long>(unit) * sk_iters) / units;
-    hi = (static_cast<long long>(unit + 1) * sk_iters) / units;
+    i = hi = 0;
+    if (sk_iters != 0) {   // 64-bit divisions only for stream-K plans (slow on the device)
+      i = (static_cast<long long>(unit) * sk_iters) / units;
+      hi = (static_cast<long long>(unit + 1) * sk_iters) / units;
+    }
   }
   GEMM_HD bool next(WorkItem* w) {
     if (next_dp < dp_tiles) {

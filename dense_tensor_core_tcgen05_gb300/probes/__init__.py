@@ -30,7 +30,8 @@ def build(force=False):
                                f"-I{os.path.join(_PKG, 'csrc')}", _SRC, "-o", _LIB])
     lib = ctypes.CDLL(_LIB)
     lib.probe_mma_rate.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p]
-    lib.probe_tma_stream.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 8 + [ctypes.c_void_p]
+    lib.probe_tma_stream.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 9 + [ctypes.c_void_p]
+    lib.probe_tma_mcast.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 9 + [ctypes.c_void_p]
     return lib
 
 
@@ -49,17 +50,17 @@ def mma_rate(lib, n, pair, grid=152, iters=2000):
     return cyc, flop_per_sm / cyc
 
 
-def tma_stream(lib, B, grid, R, KO, S, grouped=False, promo=3):
-    """(median in-kernel ns per CTA, TB/s) for streaming B [N, K] bf16."""
+def tma_stream(lib, B, grid, R, KO, S, grouped=False, promo=3, reps=1):
+    """(median in-kernel ns per CTA, TB/s) for streaming B [N, K] bf16 `reps` times."""
     import torch
     N, K = B.shape
     out = torch.zeros(grid, dtype=torch.int64, device="cuda")
-    rc = lib.probe_tma_stream(B.data_ptr(), N, K, grid, R, KO, S, int(grouped), promo,
+    rc = lib.probe_tma_stream(B.data_ptr(), N, K, grid, R, KO, S, int(grouped), promo, reps,
                               out.data_ptr())
     if rc != 0:
         raise RuntimeError(f"probe_tma_stream rc {rc}")
     ns = statistics.median(out.cpu().tolist())
-    return ns, N * K * 2 / ns / 1e3
+    return ns, reps * N * K * 2 / ns / 1e3
 
 
 def main():
@@ -70,6 +71,8 @@ def main():
         cyc, fpc = mma_rate(lib, n, pair)
         print(f"  M={256 if pair else 128:3d} N={n:3d} {'pair' if pair else 'cta '}: "
               f"{cyc:6.1f} cycles/MMA, {fpc:6.0f} FLOP/clk/SM")
+    l2_rate(lib)
+    mcast_rate(lib)
     B = torch.randn(8192, 8192, device="cuda").to(torch.bfloat16)
     flush = torch.empty(512 << 18, dtype=torch.float32, device="cuda")
     print("TMA streaming of an 8192 x 8192 K-major bf16 matrix, 128 CTAs (in-kernel time)")
@@ -86,6 +89,43 @@ def main():
         print(f"  copy = {R:3d} rows x {KO} blocks ({KO * 128:4d} B per row), {S:2d} in flight, "
               f"{'8-row groups' if grouped else 'whole box   '}, L2 promotion {promos[promo]:4s}: "
               f"{ns / 1e3:6.1f} us, {tbs:4.2f} TB/s")
+
+
+def l2_rate(lib):
+    """TMA rate from L2 into shared memory: every CTA re-streams its 128 x 512
+    slice of a 16 MB matrix (L2-resident after the first pass) 64 times, with the
+    GEMM's stage shape (128 rows x 2 blocks)."""
+    import torch
+    A = torch.randn(16384, 512, device="cuda").to(torch.bfloat16)
+    print("TMA from L2 (16 MB matrix re-streamed 64x per CTA, 128 rows x 2 blocks per copy)")
+    for grid, S in ((128, 6), (128, 3), (64, 6), (32, 6), (16, 6)):
+        ns, tbs = tma_stream(lib, A, grid, 128, 2, S, reps=64)
+        print(f"  {grid:3d} CTAs, {S} copies in flight: {tbs:5.2f} TB/s total, "
+              f"{tbs * 1e3 / grid:6.1f} GB/s per SM")
+
+
+def mcast_rate(lib):
+    """Bytes each SM receives per second from L2 when clusters of C CTAs share
+    every copy by multicast (each CTA issues 1/C of it)."""
+    import torch
+    A = torch.randn(16384, 512, device="cuda").to(torch.bfloat16)
+    N, K = A.shape
+    print("TMA multicast from L2 (copies of 128 rows x 2 blocks shared by C CTAs, 128 CTAs)")
+    for batched, C in ((0, 1), (0, 2), (0, 4), (1, 1), (1, 2), (1, 4)):
+        grid, reps = 128, 48
+        out = torch.zeros(grid, dtype=torch.int64, device="cuda")
+        rc = lib.probe_tma_mcast(A.data_ptr(), N, K, grid, 128, 2, 6, C, reps, batched,
+                                 out.data_ptr())
+        if rc != 0:
+            raise RuntimeError(f"probe_tma_mcast rc {rc}")
+        v = out.cpu().tolist()
+        if any(x < 0 for x in v):
+            raise RuntimeError("a CTA gave up its wait")
+        ns = statistics.median(v)
+        per_cta = reps * (N // (grid // C)) * K * 2
+        print(f"  {'batches of 6' if batched else 'per-slot release'}, C = {C}: "
+              f"{per_cta / ns:6.1f} GB/s received per SM "
+              f"({per_cta / C / ns:6.1f} GB/s issued per SM)")
 
 
 if __name__ == "__main__":

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned lo
 
 __global__ void __launch_bounds__(64, 1)
     tma_stream_kernel(const __grid_constant__ CUtensorMap tm, int rows_per_cta, int R, int KO, int S,
-                      int K, int grouped, unsigned long long* out) {
+                      int K, int grouped, int reps, unsigned long long* out) {
   extern __shared__ uint8_t raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   const int box_bytes = R * 128 * KO;
@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(64, 1)
   __syncthreads();
   if (threadIdx.x != 0) return;
   const int row0 = blockIdx.x * rows_per_cta;
-  const int kgroups = K / (64 * KO), rblocks = rows_per_cta / R, total = kgroups * rblocks;
+  const int kgroups = K / (64 * KO), rblocks = rows_per_cta / R, pass = kgroups * rblocks;
+  const int total = pass * reps;
   const uint64_t t0 = globaltimer_ns();
   for (int i = 0; i < total + S; ++i) {
     if (i >= S) {   // the copy issued S iterations ago must have landed before its slot is reused
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(64, 1)
       }
     }
     if (i < total) {
-      const int s = i % S, kg = i % kgroups, rb = i / kgroups;
+      const int s = i % S, kg = i % kgroups, rb = (i % pass) / kgroups;
       mbar_arrive_expect_tx(&bars[s], box_bytes);
       if (grouped)
         tma_load_4d(smem + s * box_bytes, &tm, 0, 0, kg * KO, (row0 + rb * R) / 8, &bars[s]);
@@ -122,6 +123,113 @@ __global__ void __launch_bounds__(64, 1)
     }
   }
   out[blockIdx.x] = globaltimer_ns() - t0;
+}
+
+// Bounded wait for a phase (1 s); false if it gave up.
+template <bool CLUSTER>
+__device__ bool probe_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait<CLUSTER>(bar, parity))
+    if (globaltimer_ns() - t0 > 1000000000ull) return false;
+  return true;
+}
+
+// Multicast streaming: clusters of C CTAs share every copy of R rows x KO
+// blocks; cluster rank k issues rows [k R/C, (k+1) R/C) of it, multicast to all
+// C CTAs, so each CTA receives whole boxes while issuing 1/C of them.  A slot is
+// refilled only after every CTA of the cluster has seen it full (empty[s],
+// C arrivals).  Thread 0 issues, thread 32 consumes; every thread meets at the
+// final cluster barrier, so no CTA exits while a peer may still write into it.
+// A producer that gives up stops issuing; the consumers then give up too.
+__global__ void __launch_bounds__(64, 1)
+    tma_mcast_kernel(const __grid_constant__ CUtensorMap tm, int rows_per_cluster, int R, int KO,
+                     int S, int K, int C, int reps, int batched, unsigned long long* out) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  const int box_bytes = R * 128 * KO;
+  const int piece_rows = R / C;
+  const int piece_bytes = piece_rows * 128 * KO;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * box_bytes);
+  uint64_t* empty = full + S;
+  const uint32_t rank = cluster_ctarank();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C);
+    }
+    fence_barrier_init();
+  }
+  cluster_sync();
+  const int cluster = blockIdx.x / C;
+  const int kgroups = K / (64 * KO), rblocks = rows_per_cluster / R, pass = kgroups * rblocks;
+  const int total = pass * reps;
+  if (batched) {
+    // batches of S copies into distinct slots, the cluster meeting at a
+    // barrier between batches (no per-slot hand-off)
+    const uint16_t mask = static_cast<uint16_t>((1u << C) - 1);
+    const int batches = total / S;
+    bool failed = false;
+    const uint64_t t0 = globaltimer_ns();
+    for (int b = 0; b < batches; ++b) {
+      if (threadIdx.x == 0 && !failed) {
+        for (int s = 0; s < S; ++s) {
+          const int i = b * S + s;
+          mbar_arrive_expect_tx(&full[s], box_bytes);
+          const int kg = i % kgroups, rb = (i % pass) / kgroups;
+          tma_load_3d_mcast(smem + s * box_bytes + rank * piece_bytes, &tm, 0,
+                            cluster * rows_per_cluster + rb * R + static_cast<int>(rank) * piece_rows,
+                            kg * KO, &full[s], mask);
+        }
+        for (int s = 0; s < S && !failed; ++s)
+          if (!probe_wait<true>(&full[s], b & 1)) failed = true;
+      }
+      __syncthreads();
+      cluster_sync();
+    }
+    if (threadIdx.x == 0) {
+      if (failed) {
+        const uint64_t g1 = globaltimer_ns();
+        while (globaltimer_ns() - g1 < 1000000ull) {
+        }
+      }
+      out[blockIdx.x] = failed ? ~0ull : globaltimer_ns() - t0;
+    }
+  } else if (threadIdx.x == 0) {
+    // producer: refill slot s once every CTA of the cluster has consumed it
+    const uint16_t mask = static_cast<uint16_t>((1u << C) - 1);
+    for (int i = 0; i < total; ++i) {
+      const int s = i % S;
+      if (i >= S && !probe_wait<true>(&empty[s], ((i / S) - 1) & 1)) break;
+      mbar_arrive_expect_tx(&full[s], box_bytes);
+      const int kg = i % kgroups, rb = (i % pass) / kgroups;
+      tma_load_3d_mcast(smem + s * box_bytes + rank * piece_bytes, &tm, 0,
+                        cluster * rows_per_cluster + rb * R + static_cast<int>(rank) * piece_rows,
+                        kg * KO, &full[s], mask);
+    }
+  } else if (threadIdx.x == 32) {
+    // consumer: every copy that lands here releases its slot in all C CTAs
+    bool failed = false;
+    const uint64_t t0 = globaltimer_ns();
+    for (int j = 0; j < total; ++j) {
+      const int s = j % S;
+      if (!probe_wait<false>(&full[s], (j / S) & 1)) {
+        failed = true;
+        break;
+      }
+      for (int q = 0; q < C; ++q) mbar_arrive_cluster(map_to_rank(&empty[s], q));
+    }
+    if (failed) {
+      // let copies already in flight land before the CTA can exit
+      const uint64_t g1 = globaltimer_ns();
+      while (globaltimer_ns() - g1 < 1000000ull) {
+      }
+      out[blockIdx.x] = ~0ull;
+    } else {
+      out[blockIdx.x] = globaltimer_ns() - t0;
+    }
+  }
+  __syncthreads();
+  cluster_sync();
 }
 
 template <int N, bool PAIR>
@@ -164,13 +272,14 @@ extern "C" int probe_mma_rate(int n, int pair, int grid, int iters, unsigned lon
 // Nanoseconds per CTA to stream B ([N, K] bf16, row pitch K, 16-byte aligned) with
 // copies of R rows x KO blocks of 64 elements, S copies in flight per CTA, grid
 // CTAs each owning N / grid rows.  grouped: 4-D map in 8-row groups (see top);
-// promo: L2 promotion 0 none, 1 64 B, 2 128 B, 3 256 B.  Requires
+// promo: L2 promotion 0 none, 1 64 B, 2 128 B, 3 256 B; reps: passes over the
+// CTA's rows (reps > 1 on a matrix that fits in L2 measures L2 -> shared).  Requires
 // K % (64 * KO) == 0, (N / grid) % R == 0, R % 8 == 0, R <= 256, the ring within
 // 227 KB.  Returns 0 or a negative error.
 extern "C" int probe_tma_stream(const void* B, int N, int K, int grid, int R, int KO, int S,
-                                int grouped, int promo, unsigned long long* dout) {
+                                int grouped, int promo, int reps, unsigned long long* dout) {
   if (grid <= 0 || N % grid || (N / grid) % R || R > 256 || R % 8 || KO < 1 || K % (64 * KO) ||
-      S < 1 || promo < 0 || promo > 3 || N % 8)
+      S < 1 || promo < 0 || promo > 3 || N % 8 || reps < 1)
     return -10;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
@@ -201,7 +310,59 @@ extern "C" int probe_tma_stream(const void* B, int N, int K, int grid, int R, in
   if (cudaFuncSetAttribute(tma_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return -3;
-  tma_stream_kernel<<<grid, 64, smem>>>(tm, N / grid, R, KO, S, K, grouped, dout);
+  tma_stream_kernel<<<grid, 64, smem>>>(tm, N / grid, R, KO, S, K, grouped, reps, dout);
   if (cudaGetLastError() != cudaSuccess) return -4;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -5;
+}
+
+// Nanoseconds per CTA to receive `reps` passes over its cluster's rows of B
+// ([N, K] bf16) as copies of R rows x KO blocks, each issued in C pieces by the
+// C CTAs of a cluster and multicast to all of them (C = 1: no multicast), S
+// copies in flight.  Requires grid % C == 0, N % (grid / C) == 0, the cluster's
+// rows a multiple of R, R % (8 C) == 0, K % (64 KO) == 0, C in {1, 2, 4}.
+// batched: S copies at a time into distinct slots, a cluster barrier between
+// batches, instead of per-slot release (reps * passes must be a multiple of S).
+extern "C" int probe_tma_mcast(const void* B, int N, int K, int grid, int R, int KO, int S, int C,
+                               int reps, int batched, unsigned long long* dout) {
+  if (C != 1 && C != 2 && C != 4) return -10;
+  if (grid <= 0 || grid % C || N % (grid / C) || (N / (grid / C)) % R || R % (8 * C) ||
+      R / C > 256 || KO < 1 || K % (64 * KO) || S < 1 || reps < 1)
+    return -10;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return -1;
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  CUtensorMap tm;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(R / C), static_cast<cuuint32_t>(KO)};
+  cuuint32_t es[3] = {1, 1, 1};
+  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return -2;
+  const int smem = S * R * 128 * KO + 1024 + 16 * S + 64;
+  if (smem > 232448) return -12;
+  if (cudaFuncSetAttribute(tma_mcast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return -3;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(64);
+  cfg.dynamicSmemBytes = smem;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, tma_mcast_kernel, tm, N / (grid / C), R, KO, S, K, C, reps, batched,
+                         dout) !=
+      cudaSuccess)
+    return -4;
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -5;
 }
