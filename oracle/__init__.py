@@ -58,6 +58,10 @@ def _load():
             lib.oracle_gemm.argtypes = [i64, i64, i64, f64, vp, i64, ci, vp, i64, ci, ci,
                                         f64, vp, i64, ci, vp, i64, vp, vp, vp, ci]
             lib.oracle_gemm.restype = ci
+            lib.oracle_gemm_epilogue.argtypes = [i64, i64, i64, f64, vp, i64, ci, vp, i64, ci, ci,
+                                                 f64, vp, i64, ci, vp, ci, ci, vp, i64, vp, vp,
+                                                 vp, ci]
+            lib.oracle_gemm_epilogue.restype = ci
             lib.oracle_decode.argtypes = [vp, ci, i64, vp]
             lib.oracle_encode.argtypes = [vp, ci, i64, vp]
             _lib = lib
@@ -84,14 +88,21 @@ def encode(x: np.ndarray, fmt: str) -> np.ndarray:
     return out
 
 
+BIAS_KIND = {None: 0, "col": 1, "row": 2}
+
+
 def gemm(A, B, *, M, N, K, in_dtype, out_dtype, a_col=False, b_col=False,
-         alpha=1.0, beta=0.0, C=None, rows=None, nthreads=0):
+         alpha=1.0, beta=0.0, C=None, rows=None, nthreads=0, bias=None, bias_kind=None,
+         relu=False):
     """Oracle GEMM on bit-pattern operands.
 
     A: [M, K] (a_col False) or [K, M] (a_col True) array of input bit patterns;
     B: [K, N] (b_col False) or [N, K] (b_col True); the leading dimension of each
     is its second extent.  C: [M, N'] (N' >= N) output-format bit patterns, read
     only when beta != 0.  rows: optional list of row indices (default all M).
+    bias: float32 values, N of them (bias_kind "col": bias[j] added to column j) or
+    M (bias_kind "row": bias[i] added to row i), added after alpha*s + beta*c;
+    relu: then negative results become 0 (NaN stays NaN), before the rounding.
     Returns (out_bits [R, N], exact [R, N] binary64 before rounding, scale [R, N]
     = sum_k |a_ik||b_kj|).
     """
@@ -113,14 +124,20 @@ def gemm(A, B, *, M, N, K, in_dtype, out_dtype, a_col=False, b_col=False,
         Cc = np.ascontiguousarray(C, dtype=_BITS_DT[out_dtype])
         assert Cc.shape[0] == M and Cc.shape[1] >= N
         ldc = Cc.shape[1]
+    bk = BIAS_KIND[bias_kind]
+    bv = None
+    if bk:
+        bv = np.ascontiguousarray(bias, dtype=np.float32)
+        assert bv.ndim == 1 and bv.size == (N if bk == 1 else M)
     out_bits = np.empty((nr, N), dtype=_BITS_DT[out_dtype])
     exact = np.empty((nr, N), dtype=np.float64)
     scale = np.empty((nr, N), dtype=np.float64)
-    rc = _load().oracle_gemm(M, N, K, float(alpha), _ptr(A), A.shape[1], int(a_col),
-                             _ptr(B), B.shape[1], int(b_col), FMT[in_dtype],
-                             float(beta), _ptr(Cc), ldc, FMT[out_dtype],
-                             _ptr(r), nr, _ptr(out_bits), _ptr(exact), _ptr(scale),
-                             int(nthreads))
+    rc = _load().oracle_gemm_epilogue(M, N, K, float(alpha), _ptr(A), A.shape[1], int(a_col),
+                                      _ptr(B), B.shape[1], int(b_col), FMT[in_dtype],
+                                      float(beta), _ptr(Cc), ldc, FMT[out_dtype],
+                                      _ptr(bv), bk, int(bool(relu)),
+                                      _ptr(r), nr, _ptr(out_bits), _ptr(exact), _ptr(scale),
+                                      int(nthreads))
     if rc != 0:
         raise ValueError("oracle_gemm rejected its arguments")
     return out_bits, exact, scale

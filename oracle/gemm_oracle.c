@@ -17,6 +17,14 @@
  *                dropped when beta == 0 so C is not read (the same page's
  *                preamble: the alpha = 1, beta = 0 case does not read the old
  *                output buffer)
+ *   r_ij      += bias_j (per-column bias) or bias_i (per-row bias), in binary64,
+ *                when a bias is given; then r_ij = 0 if r_ij < 0 when ReLU is
+ *                asked for (NaN stays NaN).  This is the epilogue folded into the
+ *                GEMM of "A dense FP16 matrix-multiply kernel for NVIDIA Ada", its
+ *                bias + ReLU paragraph after the L2-rasterization table: the
+ *                intermediate is kept in wide precision and rounded once; the
+ *                per-row form is the one the "mma.sync and ldmatrix" page names
+ *                (an epilogue applying a per-row bias).
  *   out_ij     = round-to-nearest-even(r_ij) in the output format
  *   S_ij       = sum_k |a_ik| |b_kj|, the scale of the error bound.
  *
@@ -33,6 +41,8 @@
 #include <unistd.h>
 
 enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2 };
+enum { OR_BIAS_NONE = 0, OR_BIAS_COL = 1, OR_BIAS_ROW = 2 };
+enum { OR_ACT_NONE = 0, OR_ACT_RELU = 1 };
 
 /* ---------------------------------------------------------------- decoding */
 
@@ -150,6 +160,7 @@ typedef struct {
     int in_fmt;
     const void* C_in; int64_t ldc;
     int out_fmt;
+    const float* bias; int bias_kind; int act;
     const int64_t* rows; int64_t nrows;
     void* out_bits; double* out_exact; double* out_scale;
     int64_t r0, r1;                 /* this worker's slice of rows[] */
@@ -179,6 +190,9 @@ static void* run_rows(void* arg) {
             double r = J->alpha * acc[j];
             if (J->beta != 0.0)
                 r += J->beta * decode(J->C_in, J->out_fmt, i * J->ldc + j);
+            if (J->bias_kind == OR_BIAS_COL) r += (double)J->bias[j];
+            else if (J->bias_kind == OR_BIAS_ROW) r += (double)J->bias[i];
+            if (J->act == OR_ACT_RELU && r < 0.0) r = 0.0;
             const int64_t o = t * N + j;
             if (J->out_exact) J->out_exact[o] = r;
             if (J->out_scale) J->out_scale[o] = scl[j];
@@ -198,16 +212,22 @@ static void* run_rows(void* arg) {
  * NULL; nrows must then equal M).  Outputs are packed [nrows, N].
  * B is [K, N] row-major (b_kj at k*ldb + j) or [N, K] column-major storage
  * (b_kj at j*ldb + k).  C_in is [M, N] row-major in out_fmt with leading
- * dimension ldc; it is read only when beta != 0.  Returns 0, or -1 on bad input. */
-int oracle_gemm(int64_t M, int64_t N, int64_t K, double alpha,
-                const void* A, int64_t lda, int a_col,
-                const void* B, int64_t ldb, int b_col, int in_fmt,
-                double beta, const void* C_in, int64_t ldc, int out_fmt,
-                const int64_t* rows, int64_t nrows,
-                void* out_bits, double* out_exact, double* out_scale, int nthreads) {
+ * dimension ldc; it is read only when beta != 0.  bias: N floats (bias_kind 1,
+ * per column) or M floats (bias_kind 2, per row), unused for bias_kind 0; act 1
+ * applies ReLU.  Returns 0, or -1 on bad input. */
+int oracle_gemm_epilogue(int64_t M, int64_t N, int64_t K, double alpha,
+                         const void* A, int64_t lda, int a_col,
+                         const void* B, int64_t ldb, int b_col, int in_fmt,
+                         double beta, const void* C_in, int64_t ldc, int out_fmt,
+                         const float* bias, int bias_kind, int act,
+                         const int64_t* rows, int64_t nrows,
+                         void* out_bits, double* out_exact, double* out_scale, int nthreads) {
     if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
     if (!rows && nrows != M) return -1;
     if (beta != 0.0 && !C_in) return -1;
+    if (bias_kind < OR_BIAS_NONE || bias_kind > OR_BIAS_ROW || act < OR_ACT_NONE || act > OR_ACT_RELU)
+        return -1;
+    if (bias_kind != OR_BIAS_NONE && !bias) return -1;
     for (int64_t t = 0; rows && t < nrows; ++t)
         if (rows[t] < 0 || rows[t] >= M) return -1;
     float* Bk = (float*)malloc(sizeof(float) * (size_t)(K * N > 0 ? K * N : 1));
@@ -222,7 +242,7 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K, double alpha,
     job_t* jobs = (job_t*)malloc(sizeof(job_t) * (size_t)nthreads);
     for (int w = 0; w < nthreads; ++w) {
         job_t J = {M, N, K, alpha, beta, A, lda, a_col, Bk, in_fmt, C_in, ldc, out_fmt,
-                   rows, nrows, out_bits, out_exact, out_scale,
+                   bias, bias_kind, act, rows, nrows, out_bits, out_exact, out_scale,
                    nrows * w / nthreads, nrows * (w + 1) / nthreads};
         jobs[w] = J;
         pthread_create(&th[w], NULL, run_rows, &jobs[w]);
@@ -232,6 +252,18 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K, double alpha,
     free(jobs);
     free(Bk);
     return 0;
+}
+
+/* The plain GEMM: no bias, no activation. */
+int oracle_gemm(int64_t M, int64_t N, int64_t K, double alpha,
+                const void* A, int64_t lda, int a_col,
+                const void* B, int64_t ldb, int b_col, int in_fmt,
+                double beta, const void* C_in, int64_t ldc, int out_fmt,
+                const int64_t* rows, int64_t nrows,
+                void* out_bits, double* out_exact, double* out_scale, int nthreads) {
+    return oracle_gemm_epilogue(M, N, K, alpha, A, lda, a_col, B, ldb, b_col, in_fmt, beta, C_in,
+                                ldc, out_fmt, NULL, OR_BIAS_NONE, OR_ACT_NONE, rows, nrows,
+                                out_bits, out_exact, out_scale, nthreads);
 }
 
 /* Element-wise helpers exposed for the oracle's own pins. */
