@@ -221,7 +221,7 @@ def make_device_problem(cfg, device):
     return w, a, b, c, c0
 
 
-def time_gemm(g, w, a, b, c, c0, steps, warmup, stream, flush):
+def time_gemm(g, w, a, b, c, c0, steps, warmup, stream, flush, **epilogue):
     """Per-step CUDA-event times (ms) of the GEMM launch alone, L2 flushed before
     each step outside the event pair.  C is reset from c0 before each step when
     beta != 0 (outside the event pair) so every step computes the same result."""
@@ -237,7 +237,7 @@ def time_gemm(g, w, a, b, c, c0, steps, warmup, stream, flush):
             if i >= warmup:
                 evs[i - warmup][0].record(st)
             g.matmul(a, b, c, alpha=w["alpha"], beta=w["beta"], a_col=w["a_col"],
-                     b_col=w["b_col"], stream=st.cuda_stream)
+                     b_col=w["b_col"], stream=st.cuda_stream, **epilogue)
             if i >= warmup:
                 evs[i - warmup][1].record(st)
     torch.cuda.synchronize()
@@ -426,9 +426,15 @@ def run_suite(g, args, device, peaks, skip_cfg):
         tf = flops / (ms * 1e-3) / 1e12
         gbs = algorithmic_bytes(w) / (ms * 1e-3) / 1e9
         cub_ms = time_cublas(w, a, b, 20, 5, flush)
+        # the same GEMM with the fused epilogue (per-column fp32 bias, then ReLU)
+        bias = torch.from_numpy(si.normal(4000 + cfg, w["N"], 1.0)).to(device)
+        ftimes = time_gemm(g, w, a, b, c, c0, 20, 5, torch.cuda.current_stream(device), flush,
+                           bias=bias, relu=True)
         res[w["name"]] = {"median_ms": ms, "tflops": tf, "gbs_algorithmic": gbs, "bound": bound,
                           "frac": tf / peak_t if bound == "tensor" else gbs / hbm,
-                          "cublas_ms": cub_ms, "cublas_tflops": flops / (cub_ms * 1e-3) / 1e12}
+                          "cublas_ms": cub_ms, "cublas_tflops": flops / (cub_ms * 1e-3) / 1e12,
+                          "bias_relu_median_ms": statistics.median(ftimes),
+                          "bias_relu_mean_over_plain_mean": statistics.mean(ftimes) / statistics.mean(times)}
         del a, b, c, c0
         torch.cuda.empty_cache()
     return res

@@ -9,12 +9,13 @@ its names and raises ImportError if the CUDA library has not been built
 import importlib
 
 _BINDING_NAMES = frozenset((
-    "EXPORTS", "GEMM_A_COL", "GEMM_A_ROW", "GEMM_B_COL", "GEMM_B_ROW", "GEMM_BF16",
+    "EXPORTS", "GEMM_A_COL", "GEMM_A_ROW", "GEMM_ACT_NONE", "GEMM_ACT_RELU", "GEMM_B_COL",
+    "GEMM_B_ROW", "GEMM_BF16", "GEMM_BIAS_COL", "GEMM_BIAS_NONE", "GEMM_BIAS_ROW",
     "GEMM_ERR_ARCH", "GEMM_ERR_CUDA", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_SCRATCH",
     "GEMM_ERR_TIMEOUT", "GEMM_ERR_UNSUPPORTED", "GEMM_F16", "GEMM_F32",
     "GEMM_NOALLOC_SCRATCH_BYTES", "GEMM_OK", "LIB_PATH", "GemmError",
     "gemm", "gemm_config_t", "gemm_debug_set", "gemm_encode_idesc", "gemm_encode_sdesc",
-    "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_plan", "gemm_plan_t", "gemm_sync_status",
+    "gemm_bias_act", "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_plan", "gemm_plan_t", "gemm_sync_status",
     "gemm_tile_coord", "gemm_version", "gemm_work_items", "library", "matmul", "status_string"))
 
 

@@ -18,9 +18,11 @@ GEMM_A_ROW, GEMM_A_COL, GEMM_B_ROW, GEMM_B_COL = 0, 1, 0, 2
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ARCH, GEMM_ERR_CUDA, \
     GEMM_ERR_TIMEOUT, GEMM_ERR_SCRATCH = range(7)
 GEMM_NOALLOC_SCRATCH_BYTES = 24 * 1024 * 1024
+GEMM_BIAS_NONE, GEMM_BIAS_COL, GEMM_BIAS_ROW = 0, 1, 2
+GEMM_ACT_NONE, GEMM_ACT_RELU = 0, 1
 
 # Symbols declared in include/gemm_tcgen05.h.
-EXPORTS = ("gemm", "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_status_string",
+EXPORTS = ("gemm", "gemm_bias_act", "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_status_string",
            "gemm_sync_status",
            "gemm_debug_set", "gemm_plan", "gemm_tile_coord", "gemm_work_items",
            "gemm_encode_idesc", "gemm_encode_sdesc", "gemm_version")
@@ -61,6 +63,8 @@ def _load():
     lib.gemm.restype = ci
     lib.gemm_ex.argtypes = gemm_args + [ctypes.POINTER(gemm_config_t)]
     lib.gemm_ex.restype = ci
+    lib.gemm_bias_act.argtypes = gemm_args[:-1] + [vp, ci, ci, vp, ctypes.POINTER(gemm_config_t)]
+    lib.gemm_bias_act.restype = ci
     lib.gemm_ex_noalloc.argtypes = gemm_args + [ctypes.POINTER(gemm_config_t)]
     lib.gemm_ex_noalloc.restype = ci
     lib.gemm_host.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, ci, ci, ci,
@@ -122,6 +126,13 @@ def gemm_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, l
             cfg=None):
     return _lib.gemm_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
                         stream, _cfg(cfg))
+
+
+def gemm_bias_act(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
+                  bias, bias_kind, act, stream, cfg=None):
+    """Raw C-ABI call of the fused-epilogue GEMM (bias: device pointer or 0)."""
+    return _lib.gemm_bias_act(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype,
+                              layout, bias, bias_kind, act, stream, _cfg(cfg))
 
 
 def gemm_ex_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
@@ -197,12 +208,16 @@ def _ld(t):
     return t.stride(0) if t.size(0) > 1 else max(t.stride(0), t.size(1))
 
 
-def matmul(a, b, c, alpha=1.0, beta=0.0, a_col=False, b_col=False, stream=None, cfg=None):
-    """C <- alpha * A * B + beta * C on CUDA tensors (in place in ``c``).
+def matmul(a, b, c, alpha=1.0, beta=0.0, a_col=False, b_col=False, stream=None, cfg=None,
+           bias=None, bias_rows=False, relu=False):
+    """C <- act(alpha * A * B + beta * C + bias) on CUDA tensors (in place in ``c``).
 
     ``a`` is the stored A: [M, K] (a_col False) or [K, M] (a_col True, i.e. A
     column-major).  ``b`` is the stored B: [K, N] or [N, K] (b_col True).
     ``c`` is [M, N] with unit column stride; its dtype is the output format.
+    ``bias``: optional fp32 CUDA tensor of N values (added per column) or, with
+    ``bias_rows``, M values (added per row); ``relu`` clamps negative results to 0
+    after the bias.  Either one selects the fused-epilogue entry point.
     Runs on ``stream`` (default: torch's current stream).  Raises GemmError.
     """
     import torch
@@ -217,9 +232,24 @@ def matmul(a, b, c, alpha=1.0, beta=0.0, a_col=False, b_col=False, stream=None, 
     if stream is None:
         stream = torch.cuda.current_stream(c.device).cuda_stream
     layout = (GEMM_A_COL if a_col else 0) | (GEMM_B_COL if b_col else 0)
-    s = gemm_ex(M, N, K, float(alpha), a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), float(beta),
-                c.data_ptr(), _ld(c), _torch_dtype_code(a.dtype), _torch_dtype_code(c.dtype),
-                layout, int(stream), cfg)
+    if bias is None and not relu:
+        s = gemm_ex(M, N, K, float(alpha), a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), float(beta),
+                    c.data_ptr(), _ld(c), _torch_dtype_code(a.dtype), _torch_dtype_code(c.dtype),
+                    layout, int(stream), cfg)
+    else:
+        kind = GEMM_BIAS_NONE
+        bptr = 0
+        if bias is not None:
+            if not bias.is_cuda or bias.dtype != torch.float32 or not bias.is_contiguous():
+                raise ValueError("bias must be a contiguous fp32 CUDA tensor")
+            if bias.numel() != (M if bias_rows else N):
+                raise ValueError(f"bias has {bias.numel()} values, expected {M if bias_rows else N}")
+            kind = GEMM_BIAS_ROW if bias_rows else GEMM_BIAS_COL
+            bptr = bias.data_ptr()
+        s = gemm_bias_act(M, N, K, float(alpha), a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
+                          float(beta), c.data_ptr(), _ld(c), _torch_dtype_code(a.dtype),
+                          _torch_dtype_code(c.dtype), layout, bptr, kind,
+                          GEMM_ACT_RELU if relu else GEMM_ACT_NONE, int(stream), cfg)
     if s != GEMM_OK:
         raise GemmError(s, "gemm")
     return c

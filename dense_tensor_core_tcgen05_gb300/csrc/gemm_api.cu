@@ -404,23 +404,32 @@ CUtensorMapDataType tma_dtype(int dt) {
 }
 
 template <int OUT>
-gemm_status_t launch_scale(void* C, int64_t ldc, int64_t M, int64_t N, float beta, int num_sms,
-                           cudaStream_t stream) {
+gemm_status_t launch_scale(void* C, int64_t ldc, int64_t M, int64_t N, float beta, const float* bias,
+                           int bias_kind, int act, int num_sms, cudaStream_t stream) {
   const int64_t total = M * N;
   int64_t blocks = ceil_div(total, 256);
   if (blocks > int64_t(num_sms) * 8) blocks = int64_t(num_sms) * 8;
   scale_c_kernel<OUT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      C, ldc, static_cast<int>(M), static_cast<int>(N), beta);
+      C, ldc, static_cast<int>(M), static_cast<int>(N), beta, bias, bias_kind, act);
   return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                        const void* B, int64_t ldb, float beta, void* C, int64_t ldc, int in_dtype,
                        int out_dtype, int layout, void* stream_v, const gemm_config_t* cfg,
-                       bool fixed_scratch = false) {
+                       bool fixed_scratch = false, const float* bias = nullptr,
+                       int bias_kind = GEMM_BIAS_NONE, int act = GEMM_ACT_NONE) {
   bool quick = false;
   gemm_status_t s = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, layout, &quick);
-  if (s != GEMM_OK || quick) return s;
+  if (s != GEMM_OK) return s;
+  if (bias_kind < GEMM_BIAS_NONE || bias_kind > GEMM_BIAS_ROW || act < GEMM_ACT_NONE ||
+      act > GEMM_ACT_RELU)
+    return GEMM_ERR_INVALID_ARG;
+  if (bias_kind != GEMM_BIAS_NONE && !quick) {
+    if (bias == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(bias)) return GEMM_ERR_UNSUPPORTED;
+  }
+  if (quick) return GEMM_OK;
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
@@ -431,9 +440,12 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
 
   if (K == 0) {
     switch (out_dtype) {
-      case GEMM_F32: return launch_scale<OUT_F32>(C, ldc, M, N, beta, di->num_sms, stream);
-      case GEMM_BF16: return launch_scale<OUT_BF16>(C, ldc, M, N, beta, di->num_sms, stream);
-      default: return launch_scale<OUT_F16>(C, ldc, M, N, beta, di->num_sms, stream);
+      case GEMM_F32:
+        return launch_scale<OUT_F32>(C, ldc, M, N, beta, bias, bias_kind, act, di->num_sms, stream);
+      case GEMM_BF16:
+        return launch_scale<OUT_BF16>(C, ldc, M, N, beta, bias, bias_kind, act, di->num_sms, stream);
+      default:
+        return launch_scale<OUT_F16>(C, ldc, M, N, beta, bias, bias_kind, act, di->num_sms, stream);
     }
   }
 
@@ -502,6 +514,10 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.groups = p.groups;
   ka.dp_tiles = p.dp_tiles;
   ka.sk_iters = p.sk_iters;
+  ka.bias = bias;
+  ka.bias_kind = bias_kind;
+  ka.act = act;
+  ka.epi = (bias_kind != GEMM_BIAS_NONE || act != GEMM_ACT_NONE) ? 1 : 0;
   if (p.sk_iters) {
     s = fixed_scratch ? noalloc_scratch(dev, stream, static_cast<size_t>(p.scratch_bytes), &ka.ws,
                                         &ka.ws_flags, &ka.epoch)
@@ -556,6 +572,14 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, float alpha, const void* 
                       int out_dtype, int layout, void* stream, const gemm_config_t* cfg) {
   return run_gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
                   stream, cfg);
+}
+
+gemm_status_t gemm_bias_act(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                            int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                            int64_t ldc, int in_dtype, int out_dtype, int layout, const float* bias,
+                            int bias_kind, int act, void* stream, const gemm_config_t* cfg) {
+  return run_gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, in_dtype, out_dtype, layout,
+                  stream, cfg, /*fixed_scratch=*/false, bias, bias_kind, act);
 }
 
 gemm_status_t gemm_ex_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const void* A,

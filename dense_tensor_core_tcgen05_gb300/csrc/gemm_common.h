@@ -124,6 +124,10 @@ GEMM_HD int sk_unit_of(long long i, int units, long long sk_iters) {
   return u;
 }
 
+// Fused epilogue kinds (same values as the public GEMM_BIAS_* / GEMM_ACT_*).
+enum { EPI_BIAS_NONE = 0, EPI_BIAS_COL = 1, EPI_BIAS_ROW = 2 };
+enum { EPI_ACT_NONE = 0, EPI_ACT_RELU = 1 };
+
 // Kernel arguments (plain data, built on the host).
 struct KernelArgs {
   int M, N, K;
@@ -151,6 +155,11 @@ struct KernelArgs {
   float* ws;
   unsigned int* ws_flags;
   unsigned int epoch;
+  // Fused epilogue: out = act(alpha*acc + beta*C + bias) before the rounding.
+  const float* bias;     // N floats (EPI_BIAS_COL) or M floats (EPI_BIAS_ROW), 16-byte aligned
+  int bias_kind;         // EPI_BIAS_*
+  int act;               // EPI_ACT_*
+  int epi;               // 1 when bias_kind or act is set (selects the fused epilogue)
 };
 
 }  // namespace gemm_tc

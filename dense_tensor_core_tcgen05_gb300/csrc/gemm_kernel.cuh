@@ -199,13 +199,48 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, int out_kind) {
   return __half22float2(h);
 }
 
+// The fused epilogue of one piece (E outputs of row grow from column gcol, a
+// multiple of 4), on fp32 values that already hold alpha*acc + beta*c: add the
+// per-column or per-row bias, then ReLU (negative -> 0, NaN kept).  Bias
+// elements beyond N (or a row beyond M) read as 0; their outputs are not stored.
+template <int E>
+__device__ __forceinline__ void bias_act(float* x, const KernelArgs& args, int grow, int gcol) {
+  if (args.bias_kind == EPI_BIAS_COL) {
+#pragma unroll
+    for (int h = 0; h < E / 4; ++h) {
+      const int c = gcol + 4 * h;
+      float4 b;
+      if (c + 4 <= args.N) {
+        b = __ldg(reinterpret_cast<const float4*>(args.bias + c));
+      } else {
+        b.x = c < args.N ? __ldg(args.bias + c) : 0.0f;
+        b.y = c + 1 < args.N ? __ldg(args.bias + c + 1) : 0.0f;
+        b.z = c + 2 < args.N ? __ldg(args.bias + c + 2) : 0.0f;
+        b.w = 0.0f;
+      }
+      x[4 * h + 0] += b.x;
+      x[4 * h + 1] += b.y;
+      x[4 * h + 2] += b.z;
+      x[4 * h + 3] += b.w;
+    }
+  } else if (args.bias_kind == EPI_BIAS_ROW) {
+    const float b = grow < args.M ? __ldg(args.bias + grow) : 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] += b;
+  }
+  if (args.act == EPI_ACT_RELU) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = x[e] < 0.0f ? 0.0f : x[e];
+  }
+}
+
 // One 16-byte piece of an output row: x holds its accumulator values (4 for
 // fp32 output, 8 for 16-bit output, alpha not yet applied).  Applies
-// alpha*acc + beta*c (c read from the staged C chunk at p when read_c), casts,
-// and either writes the piece to the swizzled staging buffer (p) or, for a
-// chunk crossing the ragged right edge of C, stores its in-range elements
-// straight to global memory.
-template <int OUT>
+// alpha*acc + beta*c (c read from the staged C chunk at p when read_c), then
+// (FUSED) the bias and activation, casts, and either writes the piece to the
+// swizzled staging buffer (p) or, for a chunk crossing the ragged right edge of
+// C, stores its in-range elements straight to global memory.
+template <int OUT, bool FUSED = false>
 __device__ __forceinline__ void finish_piece(float* x, uint4* p, const KernelArgs& args,
                                              bool ragged, bool store_row, int grow, int gcol) {
   constexpr int E = OUT == OUT_F32 ? 4 : 8;
@@ -228,6 +263,7 @@ __device__ __forceinline__ void finish_piece(float* x, uint4* p, const KernelArg
       }
     }
   }
+  if (FUSED) bias_act<E>(x, args, grow, gcol);
   uint4 o;
   if (OUT == OUT_F32) {
     o = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
@@ -622,9 +658,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Write one finished tile: TMEM -> registers (+ the later units' partial
     // sums, in unit order, when ADD) -> alpha * acc + beta * C -> output.
     // Returns false if a wait gave up.
-    auto store_tile = [&](auto add_tag, uint32_t t_row, int nb, int row0, int buf, int contrib0,
-                          int ncontrib) -> bool {
+    auto store_tile = [&](auto add_tag, auto fused_tag, uint32_t t_row, int nb, int row0, int buf,
+                          int contrib0, int ncontrib) -> bool {
       constexpr bool ADD = decltype(add_tag)::value;
+      constexpr bool FUSED = decltype(fused_tag)::value;   // bias / activation
       const uint32_t first = p_issued;
       const uint32_t total = ADD ? static_cast<uint32_t>(CHUNKS * ncontrib) : 0u;
       uint64_t pol = 0;
@@ -710,8 +747,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t* src = (OUT == OUT_F32) ? (v0 + 4 * j) : ((j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4)));
 #pragma unroll
           for (int e = 0; e < E; ++e) x[e] = __uint_as_float(src[e]);
-          finish_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
-                            col0 + E * j);
+          finish_piece<OUT, FUSED>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
+                                   col0 + E * j);
         }
         end_chunk(st, stg, &tmC, row0, col0, ragged, skip_store);
       }
@@ -826,8 +863,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       const int ncontrib = contrib1 - contrib0;
-      ok = ncontrib == 0 ? store_tile(BoolC<false>{}, t_row, nb, row0, buf, 0, 0)
-                         : store_tile(BoolC<true>{}, t_row, nb, row0, buf, contrib0, ncontrib);
+      // one specialised chunk loop per case, chosen once per tile
+      if (ncontrib == 0)
+        ok = args.epi ? store_tile(BoolC<false>{}, BoolC<true>{}, t_row, nb, row0, buf, 0, 0)
+                      : store_tile(BoolC<false>{}, BoolC<false>{}, t_row, nb, row0, buf, 0, 0);
+      else
+        ok = args.epi
+                 ? store_tile(BoolC<true>{}, BoolC<true>{}, t_row, nb, row0, buf, contrib0, ncontrib)
+                 : store_tile(BoolC<true>{}, BoolC<false>{}, t_row, nb, row0, buf, contrib0, ncontrib);
     }
     if (!SPLITK) {
       if (!ok && st.pending_cload >= 0 && lane == 0)
@@ -920,8 +963,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
-          finish_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
-                            col0 + E * j);
+          if (args.epi)
+            finish_piece<OUT, true>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
+                                    col0 + E * j);
+          else
+            finish_piece<OUT, false>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
+                                     col0 + E * j);
         }
         end_chunk(st, stg, &tmC, row0, col0, ragged, skip_store);
       }
@@ -984,24 +1031,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-// C <- beta * C (or 0 when beta == 0, without reading C): the K == 0 case.
+// C <- act(beta * C + bias) (beta * C taken as 0 when beta == 0, without reading
+// C): the K == 0 case.
 template <int OUT>
-__global__ void scale_c_kernel(void* C, long long ldc, int M, int N, float beta) {
+__global__ void scale_c_kernel(void* C, long long ldc, int M, int N, float beta, const float* bias,
+                               int bias_kind, int act) {
   const long long total = static_cast<long long>(M) * N;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long r = i / N, c = i % N;
     const long long o = r * ldc + c;
-    if (OUT == OUT_F32) {
-      float* p = static_cast<float*>(C) + o;
-      *p = (beta == 0.0f) ? 0.0f : beta * *p;
-    } else if (OUT == OUT_BF16) {
-      __nv_bfloat16* p = static_cast<__nv_bfloat16*>(C) + o;
-      *p = (beta == 0.0f) ? __float2bfloat16_rn(0.0f) : __float2bfloat16_rn(beta * __bfloat162float(*p));
-    } else {
-      __half* p = static_cast<__half*>(C) + o;
-      *p = (beta == 0.0f) ? __float2half_rn(0.0f) : __float2half_rn(beta * __half2float(*p));
+    float x = 0.0f;
+    if (beta != 0.0f) {
+      if (OUT == OUT_F32)
+        x = beta * static_cast<const float*>(C)[o];
+      else if (OUT == OUT_BF16)
+        x = beta * __bfloat162float(static_cast<const __nv_bfloat16*>(C)[o]);
+      else
+        x = beta * __half2float(static_cast<const __half*>(C)[o]);
     }
+    if (bias_kind == EPI_BIAS_COL) x += bias[c];
+    else if (bias_kind == EPI_BIAS_ROW) x += bias[r];
+    if (act == EPI_ACT_RELU) x = x < 0.0f ? 0.0f : x;
+    if (OUT == OUT_F32)
+      static_cast<float*>(C)[o] = x;
+    else if (OUT == OUT_BF16)
+      static_cast<__nv_bfloat16*>(C)[o] = __float2bfloat16_rn(x);
+    else
+      static_cast<__half*>(C)[o] = __float2half_rn(x);
   }
 }
 

@@ -127,6 +127,41 @@ gemm_status_t gemm_ex(int64_t M, int64_t N, int64_t K, float alpha, const void* 
                       int out_dtype, int layout, void* stream, const gemm_config_t* cfg);
 
 /*
+ * gemm_bias_act -- the GEMM with a fused epilogue:
+ *
+ *     C <- act(alpha * A * B + beta * C + bias)
+ *
+ * The bias + ReLU epilogue that "A dense FP16 matrix-multiply kernel for NVIDIA
+ * Ada" (kd.iw.mk) folds into the GEMM (its paragraph on bias + ReLU after the
+ * L2-rasterization table): the sum stays in an fp32 register through the bias
+ * and the activation and is rounded to the output format once, with no extra
+ * pass over C.  The per-row form is the per-row bias the "mma.sync and ldmatrix"
+ * page (gpu-preview.ayushworks.com, day 73) names as coordinate-dependent
+ * epilogue work.
+ *
+ * bias      : fp32, DEVICE pointer owned by the caller, only read, 16-byte
+ *             aligned; N values (GEMM_BIAS_COL: bias[j] added to every row's
+ *             column j) or M values (GEMM_BIAS_ROW: bias[i] added to row i).
+ *             Unused (may be NULL) with GEMM_BIAS_NONE.
+ * bias_kind : GEMM_BIAS_NONE, GEMM_BIAS_COL or GEMM_BIAS_ROW.
+ * act       : GEMM_ACT_NONE or GEMM_ACT_RELU (negative results become +0; NaN
+ *             stays NaN), applied after the bias.
+ * The fp32 order is alpha*acc, then fmaf(beta, c, .), then + bias, then act,
+ * then one round to nearest even.  Everything else (arguments, layouts, K == 0
+ * -> C <- act(beta*C + bias), quick returns, determinism) is as for gemm_ex.
+ * Errors: as gemm_ex, plus GEMM_ERR_INVALID_ARG for an unknown bias_kind or act
+ * or a NULL bias that would be read, GEMM_ERR_UNSUPPORTED for a bias pointer
+ * that is not 16-byte aligned.
+ */
+enum { GEMM_BIAS_NONE = 0, GEMM_BIAS_COL = 1, GEMM_BIAS_ROW = 2 };
+enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1 };
+
+gemm_status_t gemm_bias_act(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                            int64_t lda, const void* B, int64_t ldb, float beta, void* C,
+                            int64_t ldc, int in_dtype, int out_dtype, int layout, const float* bias,
+                            int bias_kind, int act, void* stream, const gemm_config_t* cfg);
+
+/*
  * gemm_ex_noalloc -- gemm_ex that never allocates device memory.
  *
  * The pages have no counterpart: this entry point exists for callers that must

@@ -41,14 +41,18 @@ def alloc_c(M, N, ldc, fmt, init_bits=None, device="cuda"):
 
 
 def run_library(A, B, *, M, N, K, in_dtype, out_dtype, a_col, b_col, alpha=1.0, beta=0.0,
-                C=None, ldc=None, cfg=None):
-    """Run the GPU GEMM; returns (out bits [M, N], full C buffer bits [M, ldc])."""
+                C=None, ldc=None, cfg=None, bias=None, bias_kind=None, relu=False):
+    """Run the GPU GEMM; returns (out bits [M, N], full C buffer bits [M, ldc]).
+    bias (float32 numpy, N or M values) with bias_kind "col"/"row", and relu,
+    select the fused epilogue."""
     import dense_tensor_core_tcgen05_gb300 as g
     ldc = N if ldc is None else ldc
     dA = to_device(A, in_dtype)[:, :(M if a_col else K)]
     dB = to_device(B, in_dtype)[:, :(K if b_col else N)]
     full, c = alloc_c(M, N, ldc, out_dtype, C)
-    g.matmul(dA, dB, c, alpha=alpha, beta=beta, a_col=a_col, b_col=b_col, cfg=cfg)
+    dbias = None if bias is None else torch.from_numpy(np.ascontiguousarray(bias, np.float32)).cuda()
+    g.matmul(dA, dB, c, alpha=alpha, beta=beta, a_col=a_col, b_col=b_col, cfg=cfg, bias=dbias,
+             bias_rows=(bias_kind == "row"), relu=relu)
     s, site = g.gemm_sync_status(torch.cuda.current_stream().cuda_stream)
     assert s == g.GEMM_OK, f"kernel status {s} site {site}"
     fb = to_bits(full, out_dtype)
@@ -56,12 +60,14 @@ def run_library(A, B, *, M, N, K, in_dtype, out_dtype, a_col, b_col, alpha=1.0, 
 
 
 def check_against_oracle(gpu_bits, A, B, *, M, N, K, in_dtype, out_dtype, a_col, b_col,
-                         alpha=1.0, beta=0.0, C=None, rows=None, exact=False):
+                         alpha=1.0, beta=0.0, C=None, rows=None, exact=False, bias=None,
+                         bias_kind=None, relu=False):
     """Element-wise comparison on the given rows (default all).  exact=True demands
     identical bit patterns; otherwise the error bound of TOL[out_dtype]."""
     obits, oexact, oscale = oracle.gemm(A, B, M=M, N=N, K=K, in_dtype=in_dtype,
                                         out_dtype=out_dtype, a_col=a_col, b_col=b_col,
-                                        alpha=alpha, beta=beta, C=C, rows=rows)
+                                        alpha=alpha, beta=beta, C=C, rows=rows, bias=bias,
+                                        bias_kind=bias_kind, relu=relu)
     g = gpu_bits if rows is None else gpu_bits[np.asarray(rows)]
     if exact:
         bad = np.argwhere(g != obits)
@@ -76,6 +82,13 @@ def check_against_oracle(gpu_bits, A, B, *, M, N, K, in_dtype, out_dtype, a_col,
         cin = oracle.decode(np.asarray(C)[:, :N] if rows is None else np.asarray(C)[np.asarray(rows), :N],
                             out_dtype)
         bound = bound + 2.0 ** -23 * np.abs(beta * cin)
+    if bias_kind is not None:
+        # the bias is added in fp32 on the GPU: one more rounding of a value at
+        # most |alpha| S + |beta c| + |bias| in size (ReLU is 1-Lipschitz)
+        bv = np.asarray(bias, np.float64)
+        rr = np.arange(M) if rows is None else np.asarray(rows)
+        b2 = bv[None, :N] if bias_kind == "col" else bv[rr][:, None]
+        bound = bound + 2.0 ** -23 * (np.abs(b2) + abs(alpha) * oscale)
     worst = np.argmax(err - bound)
     assert np.all(np.isfinite(gv)), "non-finite output"
     assert np.all(err <= bound), (f"error bound exceeded at {np.unravel_index(worst, err.shape)}: "

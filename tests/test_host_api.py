@@ -304,3 +304,18 @@ def test_smem_descriptor_fields(g):
     assert (d >> 61) & 7 == 2
     d2 = g.gemm_encode_sdesc(0x3FFF0, 8192, 1024)
     assert d2 & 0x3FFF == 0x3FFF and (d2 >> 16) & 0x3FFF == 512
+
+
+@pytest.mark.parametrize("bias,kind,act,M,expect", [
+    (0, 1, 0, 64, 1),               # column bias without a pointer
+    (0, 2, 1, 64, 1),               # row bias without a pointer
+    (ALIGNED, 3, 0, 64, 1),         # unknown bias kind
+    (ALIGNED, 1, 2, 64, 1),         # unknown activation
+    (ALIGNED, -1, 0, 64, 1),
+    (ALIGNED + 4, 1, 0, 64, 2),     # bias not 16-byte aligned
+    (0, 1, 1, 0, 0),                # M == 0: quick return, the bias is never read
+])
+def test_bias_act_argument_checks(g, bias, kind, act, M, expect):
+    s = g.gemm_bias_act(M, 64, 64, 1.0, ALIGNED, 64, ALIGNED, 64, 0.0, ALIGNED, 64, 0, 2, 0,
+                        bias, kind, act, 0)
+    assert s == expect
