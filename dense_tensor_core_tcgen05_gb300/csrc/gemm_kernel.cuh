@@ -199,38 +199,41 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, int out_kind) {
   return __half22float2(h);
 }
 
-// The fused epilogue of one piece (E outputs of row grow from column gcol, a
-// multiple of 4), on fp32 values that already hold alpha*acc + beta*c: add the
-// per-column or per-row bias, then ReLU (negative -> 0, NaN kept).  Bias
-// elements beyond N (or a row beyond M) read as 0; their outputs are not stored.
-template <int E>
-__device__ __forceinline__ void bias_act(float* x, const KernelArgs& args, int grow, int gcol) {
+// Bias values of one output chunk, loaded before the chunk's waits: lane l holds
+// the column bias of chunk columns l and 32 + l (c0, c1; 0 without a column
+// bias) and the row bias of its row (row; 0 without a row bias); lo is the ReLU
+// floor (0, or -infinity without ReLU).  Pieces pick their columns' values by
+// shuffle, so no piece waits on memory, and the step has no branch.
+struct EpiBias {
+  float c0, c1, row, lo;
+};
+
+// Load them (every lane of the warp; columns past N and a row past M read 0).
+template <int CHUNK>
+__device__ __forceinline__ EpiBias load_epi_bias(const KernelArgs& args, int col0, int grow) {
+  const int lane = threadIdx.x & 31;
+  EpiBias b{0.0f, 0.0f, 0.0f, args.act == EPI_ACT_RELU ? 0.0f : -__int_as_float(0x7f800000)};
   if (args.bias_kind == EPI_BIAS_COL) {
-#pragma unroll
-    for (int h = 0; h < E / 4; ++h) {
-      const int c = gcol + 4 * h;
-      float4 b;
-      if (c + 4 <= args.N) {
-        b = __ldg(reinterpret_cast<const float4*>(args.bias + c));
-      } else {
-        b.x = c < args.N ? __ldg(args.bias + c) : 0.0f;
-        b.y = c + 1 < args.N ? __ldg(args.bias + c + 1) : 0.0f;
-        b.z = c + 2 < args.N ? __ldg(args.bias + c + 2) : 0.0f;
-        b.w = 0.0f;
-      }
-      x[4 * h + 0] += b.x;
-      x[4 * h + 1] += b.y;
-      x[4 * h + 2] += b.z;
-      x[4 * h + 3] += b.w;
-    }
+    if (col0 + lane < args.N) b.c0 = __ldg(args.bias + col0 + lane);
+    if (CHUNK == 64 && col0 + 32 + lane < args.N) b.c1 = __ldg(args.bias + col0 + 32 + lane);
   } else if (args.bias_kind == EPI_BIAS_ROW) {
-    const float b = grow < args.M ? __ldg(args.bias + grow) : 0.0f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) x[e] += b;
+    if (grow < args.M) b.row = __ldg(args.bias + grow);
   }
-  if (args.act == EPI_ACT_RELU) {
+  return b;
+}
+
+// The fused epilogue of one piece (E outputs from chunk column pc, a multiple of
+// 4), on fp32 values that already hold alpha*acc + beta*c: add the bias (the
+// column and row terms, at most one of them nonzero, so the sum is that bias
+// exactly), then the ReLU floor (x < lo -> +0; NaN kept).  All 32 lanes call it.
+template <int E>
+__device__ __forceinline__ void bias_act(float* x, const EpiBias& b, int pc) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) x[e] = x[e] < 0.0f ? 0.0f : x[e];
+  for (int e = 0; e < E; ++e) {
+    const int t = pc + e;
+    const float bias = __shfl_sync(0xffffffffu, t < 32 ? b.c0 : b.c1, t & 31) + b.row;
+    const float y = x[e] + bias;
+    x[e] = y < b.lo ? 0.0f : y;
   }
 }
 
@@ -240,9 +243,15 @@ __device__ __forceinline__ void bias_act(float* x, const KernelArgs& args, int g
 // (FUSED) the bias and activation, casts, and either writes the piece to the
 // swizzled staging buffer (p) or, for a chunk crossing the ragged right edge of
 // C, stores its in-range elements straight to global memory.
+template <int OUT>
+__device__ __forceinline__ void store_piece(const float* x, uint4* p, const KernelArgs& args,
+                                            bool ragged, bool store_row, int grow, int gcol);
+
 template <int OUT, bool FUSED = false>
 __device__ __forceinline__ void finish_piece(float* x, uint4* p, const KernelArgs& args,
-                                             bool ragged, bool store_row, int grow, int gcol) {
+                                             bool ragged, bool store_row, int grow, int gcol,
+                                             const EpiBias& eb = EpiBias{0.0f, 0.0f, 0.0f, 0.0f},
+                                             int pc = 0) {
   constexpr int E = OUT == OUT_F32 ? 4 : 8;
 #pragma unroll
   for (int e = 0; e < E; ++e) x[e] *= args.alpha;
@@ -263,7 +272,80 @@ __device__ __forceinline__ void finish_piece(float* x, uint4* p, const KernelArg
       }
     }
   }
-  if (FUSED) bias_act<E>(x, args, grow, gcol);
+  if (FUSED) bias_act<E>(x, eb, pc);
+  store_piece<OUT>(x, p, args, ragged, store_row, grow, gcol);
+}
+
+// The fused epilogue on a whole output chunk held in registers (this thread's
+// row, CHUNK columns from col0: v0 = columns 0..31, v1 = 32..63), before any of
+// it is stored: x = alpha*acc, + beta*c (c from the staged C chunk at rowp when
+// read_c), + bias, then ReLU (negative -> 0, NaN kept); written back into v0/v1.
+// With no store in between, the chunk's bias loads (the same addresses in every
+// lane) issue together, and the branches are taken once per chunk.
+template <int OUT, int CHUNK>
+__device__ __forceinline__ void fused_chunk(uint32_t* v0, uint32_t* v1, const uint8_t* rowp,
+                                            const KernelArgs& args, int col0, int grow, int r) {
+  constexpr int E = OUT == OUT_F32 ? 4 : 8;
+  float x[CHUNK];
+#pragma unroll
+  for (int i = 0; i < CHUNK; ++i) x[i] = __uint_as_float(i < 32 ? v0[i] : v1[i - 32]) * args.alpha;
+  if (args.read_c) {
+#pragma unroll
+    for (int j = 0; j < CHUNK / E; ++j) {
+      const uint4 ci = *reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4));
+      const uint32_t cw[4] = {ci.x, ci.y, ci.z, ci.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (OUT == OUT_F32) {
+          x[4 * j + e] = fmaf(args.beta, __uint_as_float(cw[e]), x[4 * j + e]);
+        } else {
+          const float2 f = unpack2(cw[e], OUT);
+          x[8 * j + 2 * e] = fmaf(args.beta, f.x, x[8 * j + 2 * e]);
+          x[8 * j + 2 * e + 1] = fmaf(args.beta, f.y, x[8 * j + 2 * e + 1]);
+        }
+      }
+    }
+  }
+  if (args.bias_kind == EPI_BIAS_COL) {
+    if (col0 + CHUNK <= args.N) {
+      const float4* b4 = reinterpret_cast<const float4*>(args.bias + col0);
+#pragma unroll
+      for (int q = 0; q < CHUNK / 4; ++q) {
+        const float4 b = __ldg(b4 + q);
+        x[4 * q + 0] += b.x;
+        x[4 * q + 1] += b.y;
+        x[4 * q + 2] += b.z;
+        x[4 * q + 3] += b.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < CHUNK; ++i)
+        if (col0 + i < args.N) x[i] += __ldg(args.bias + col0 + i);
+    }
+  } else if (args.bias_kind == EPI_BIAS_ROW) {
+    const float b = grow < args.M ? __ldg(args.bias + grow) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < CHUNK; ++i) x[i] += b;
+  }
+  if (args.act == EPI_ACT_RELU) {
+#pragma unroll
+    for (int i = 0; i < CHUNK; ++i) x[i] = x[i] < 0.0f ? 0.0f : x[i];
+  }
+#pragma unroll
+  for (int i = 0; i < CHUNK; ++i) {
+    if (i < 32)
+      v0[i] = __float_as_uint(x[i]);
+    else
+      v1[i - 32] = __float_as_uint(x[i]);
+  }
+}
+
+// Cast a finished piece (E fp32 values) to the output format and store it: into
+// the swizzled staging buffer (p), or for a chunk crossing the ragged right edge
+// of C, its in-range elements straight to global memory.
+template <int OUT>
+__device__ __forceinline__ void store_piece(const float* x, uint4* p, const KernelArgs& args,
+                                            bool ragged, bool store_row, int grow, int gcol) {
   uint4 o;
   if (OUT == OUT_F32) {
     o = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
@@ -739,6 +821,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         uint8_t* rowp = stg + r * SW;
+        if (FUSED) fused_chunk<OUT, CHUNK>(v0, v1, rowp, args, col0, row0 + r, r);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {   // 16-byte pieces of the 128-byte row
           uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
@@ -747,8 +830,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t* src = (OUT == OUT_F32) ? (v0 + 4 * j) : ((j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4)));
 #pragma unroll
           for (int e = 0; e < E; ++e) x[e] = __uint_as_float(src[e]);
-          finish_piece<OUT, FUSED>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
-                                   col0 + E * j);
+          if (FUSED)
+            store_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
+                             col0 + E * j);
+          else
+            finish_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
+                              col0 + E * j);
         }
         end_chunk(st, stg, &tmC, row0, col0, ragged, skip_store);
       }
@@ -762,6 +849,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tile_coord(w.tile, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
       const int buf = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
+      if (args.epi) {
+        // the tile's bias into L1 while its mainloop runs (in bounds only)
+        if (args.bias_kind == EPI_BIAS_COL) {
+          const int c = nb * BN + lane * 32;   // one 128-byte line per lane
+          if (lane < BN / 32 && c < args.N) prefetch_l1(args.bias + c);
+        } else if (args.bias_kind == EPI_BIAS_ROW && lane == 0) {
+          const int rr = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32;
+          if (rr < args.M) prefetch_l1(args.bias + rr);
+        }
+      }
       if (!wait_warp<PAIR>(&tfull[buf], aph, abort_flag, args, SITE_EPI_TMEM_FULL)) {
         ok = false;
         break;
@@ -926,6 +1023,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int c = 0; ok && c < SLICE / CHUNK; ++c) {
         const int tcol = static_cast<int>(srank) * SLICE + c * CHUNK;   // column inside the tile
         const int col0 = nb * BN + tcol;
+        EpiBias eb{0.0f, 0.0f, 0.0f, 0.0f};
+        if (args.epi) eb = load_epi_bias<CHUNK>(args, col0, row0 + r);
         uint8_t* stg;
         if (!begin_chunk<true, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args)) {
           ok = false;
@@ -965,7 +1064,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
           if (args.epi)
             finish_piece<OUT, true>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
-                                    col0 + E * j);
+                                    col0 + E * j, eb, E * j);
           else
             finish_piece<OUT, false>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
                                      col0 + E * j);

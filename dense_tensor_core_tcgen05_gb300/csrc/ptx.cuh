@@ -222,6 +222,11 @@ __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, 
       : "memory");
 }
 
+// Bring the global-memory line holding `p` into L1 (no register, no wait).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
