@@ -13,10 +13,11 @@ _BINDING_NAMES = frozenset((
     "GEMM_B_ROW", "GEMM_BF16", "GEMM_BIAS_COL", "GEMM_BIAS_NONE", "GEMM_BIAS_ROW",
     "GEMM_ERR_ARCH", "GEMM_ERR_CUDA", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_SCRATCH",
     "GEMM_ERR_TIMEOUT", "GEMM_ERR_UNSUPPORTED", "GEMM_F16", "GEMM_F32",
-    "GEMM_NOALLOC_SCRATCH_BYTES", "GEMM_OK", "LIB_PATH", "GemmError",
+    "GEMM_NOALLOC_SCRATCH_BYTES", "GEMM_OK", "GEMM_ORDER_AUTO", "GEMM_ORDER_GROUPED",
+    "GEMM_ORDER_HILBERT", "LIB_PATH", "GemmError",
     "gemm", "gemm_config_t", "gemm_debug_set", "gemm_encode_idesc", "gemm_encode_sdesc",
     "gemm_bias_act", "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_plan", "gemm_plan_t", "gemm_sync_status",
-    "gemm_tile_coord", "gemm_version", "gemm_work_items", "library", "matmul", "status_string"))
+    "gemm_tile_coord", "gemm_tile_order", "gemm_version", "gemm_work_items", "library", "matmul", "status_string"))
 
 
 def __getattr__(name):

@@ -20,11 +20,12 @@ GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ARCH, GEMM_ERR_CUD
 GEMM_NOALLOC_SCRATCH_BYTES = 24 * 1024 * 1024
 GEMM_BIAS_NONE, GEMM_BIAS_COL, GEMM_BIAS_ROW = 0, 1, 2
 GEMM_ACT_NONE, GEMM_ACT_RELU = 0, 1
+GEMM_ORDER_AUTO, GEMM_ORDER_GROUPED, GEMM_ORDER_HILBERT = 0, 1, 2
 
 # Symbols declared in include/gemm_tcgen05.h.
 EXPORTS = ("gemm", "gemm_bias_act", "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_status_string",
            "gemm_sync_status",
-           "gemm_debug_set", "gemm_plan", "gemm_tile_coord", "gemm_work_items",
+           "gemm_debug_set", "gemm_plan", "gemm_tile_coord", "gemm_tile_order", "gemm_work_items",
            "gemm_encode_idesc", "gemm_encode_sdesc", "gemm_version")
 
 
@@ -32,14 +33,15 @@ class gemm_config_t(ctypes.Structure):
     _fields_ = [("bn", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("cta_group", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("stream_k", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("order", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class gemm_plan_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "bm", "bn", "bk", "stages", "m_tiles", "n_tiles", "k_blocks", "num_tiles",
         "grid", "group_m", "threads", "smem_bytes", "tmem_cols", "a_mn", "b_mn",
-        "epi_chunk_cols", "cta_group", "split_k", "groups", "dp_tiles")] + [
+        "epi_chunk_cols", "cta_group", "split_k", "groups", "dp_tiles", "order",
+        "reserved")] + [
         ("sk_iters", ctypes.c_int64), ("scratch_bytes", ctypes.c_int64)]
 
     def as_dict(self):
@@ -81,6 +83,8 @@ def _load():
     lib.gemm_plan.restype = ci
     lib.gemm_tile_coord.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
     lib.gemm_tile_coord.restype = None
+    lib.gemm_tile_order.argtypes = [ci, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32), i32]
+    lib.gemm_tile_order.restype = i32
     lib.gemm_work_items.argtypes = [i32, i32, i32, i64, i32, ctypes.POINTER(i32), i32]
     lib.gemm_work_items.restype = i32
     lib.gemm_encode_idesc.argtypes = [ci, ci, ci, ci, ci]
@@ -113,6 +117,7 @@ def _cfg(cfg):
     c.bn, c.group_m, c.grid = int(cfg.get("bn", 0)), int(cfg.get("group_m", 0)), int(cfg.get("grid", 0))
     c.cta_group, c.split_k = int(cfg.get("cta_group", 0)), int(cfg.get("split_k", 0))
     c.stream_k = int(cfg.get("stream_k", 0))
+    c.order = int(cfg.get("order", 0))
     return ctypes.byref(c)
 
 
@@ -169,6 +174,17 @@ def gemm_tile_coord(t, m_tiles, n_tiles, group_m):
     m, n = ctypes.c_int32(0), ctypes.c_int32(0)
     _lib.gemm_tile_coord(t, m_tiles, n_tiles, group_m, ctypes.byref(m), ctypes.byref(n))
     return m.value, n.value
+
+
+def gemm_tile_order(order, m_tiles, n_tiles, group_m=1):
+    """The whole tile order as a list of (m_blk, n_blk), or None if unavailable."""
+    n = m_tiles * n_tiles
+    mb = (ctypes.c_int32 * max(n, 1))()
+    nb = (ctypes.c_int32 * max(n, 1))()
+    got = _lib.gemm_tile_order(order, m_tiles, n_tiles, group_m, mb, nb, n)
+    if got < 0:
+        return None
+    return [(mb[i], nb[i]) for i in range(got)]
 
 
 def gemm_work_items(unit, units, dp_tiles, sk_iters, groups, max_items=4096):

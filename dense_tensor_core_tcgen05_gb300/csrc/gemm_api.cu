@@ -17,7 +17,9 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
+#include <vector>
 
 #include "gemm_common.h"
 #include "gemm_kernel.cuh"
@@ -151,6 +153,53 @@ gemm_status_t noalloc_scratch(int dev, cudaStream_t st, size_t need, float** ws,
   return GEMM_OK;
 }
 
+// Tiles of an m_tiles x n_tiles grid in Hilbert-curve order: the curve over the
+// smallest power-of-two square holding the grid, keeping the cells inside it
+// (x = n block, y = m block).  False (nothing written) when the square would hold
+// more than 16 times the grid's tiles, or the grid more than 2^22 tiles.
+bool hilbert_tiles(int m_tiles, int n_tiles, std::vector<int2>* out) {
+  const int64_t tiles = int64_t(m_tiles) * n_tiles;
+  if (m_tiles <= 0 || n_tiles <= 0 || tiles > (int64_t(1) << 22)) return false;
+  int k = 0;
+  while ((int64_t(1) << k) < std::max(m_tiles, n_tiles)) ++k;
+  const int64_t cells = int64_t(1) << (2 * k);
+  if (cells > 16 * tiles) return false;
+  out->clear();
+  out->reserve(static_cast<size_t>(tiles));
+  for (int64_t d = 0; d < cells; ++d) {
+    int x, y;
+    hilbert_cell(k, d, &x, &y);
+    if (x < n_tiles && y < m_tiles) out->push_back(make_int2(y, x));
+  }
+  return true;
+}
+
+// Device copies of Hilbert tile tables, one per (device, grid shape), built on
+// first use and kept for the life of the process.
+std::mutex g_map_mu;
+std::map<std::tuple<int, int, int>, int2*> g_maps;
+
+gemm_status_t hilbert_map_for(int dev, int m_tiles, int n_tiles, const int2** table) {
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  const auto key = std::make_tuple(dev, m_tiles, n_tiles);
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *table = it->second;
+    return GEMM_OK;
+  }
+  std::vector<int2> host;
+  if (!hilbert_tiles(m_tiles, n_tiles, &host)) return GEMM_ERR_INVALID_ARG;
+  int2* d = nullptr;
+  if (cudaMalloc(&d, host.size() * sizeof(int2)) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (cudaMemcpy(d, host.data(), host.size() * sizeof(int2), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(d);
+    return GEMM_ERR_CUDA;
+  }
+  g_maps[key] = d;
+  *table = d;
+  return GEMM_OK;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   std::call_once(g_encode_once, []() {
     void* fn = nullptr;
@@ -271,7 +320,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
                         const gemm_config_t* cfg, gemm_plan_t* p) {
   if (num_sms <= 0) return GEMM_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
-  if (cfg && (cfg->reserved[0] || cfg->reserved[1])) return GEMM_ERR_INVALID_ARG;
+  if (cfg && cfg->reserved) return GEMM_ERR_INVALID_ARG;
+  if (cfg && (cfg->order < GEMM_ORDER_AUTO || cfg->order > GEMM_ORDER_HILBERT))
+    return GEMM_ERR_INVALID_ARG;
   int bn = 0;
   bool pair = false;
   choose_unit(M, N, num_sms, &bn, &pair);
@@ -311,6 +362,15 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
   if (gm < 0) return GEMM_ERR_INVALID_ARG;
   if (gm > p->m_tiles) gm = p->m_tiles > 0 ? p->m_tiles : 1;
   p->group_m = gm;
+  // tile order: grouped unless the Hilbert curve is asked for and usable here
+  p->order = GEMM_ORDER_GROUPED;
+  if (cfg && cfg->order == GEMM_ORDER_HILBERT) {
+    const int64_t cells_side = std::max(mt, nt);
+    int k = 0;
+    while ((int64_t(1) << k) < cells_side) ++k;
+    if (mt * nt <= (int64_t(1) << 22) && (int64_t(1) << (2 * k)) <= 16 * mt * nt)
+      p->order = GEMM_ORDER_HILBERT;
+  }
   const int per_unit = pair ? 2 : 1;
   int grid = (cfg && cfg->grid) ? cfg->grid : (pair ? (num_sms / 2) * 2 : num_sms);
   if (grid < 0) return GEMM_ERR_INVALID_ARG;
@@ -518,6 +578,11 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.bias_kind = bias_kind;
   ka.act = act;
   ka.epi = (bias_kind != GEMM_BIAS_NONE || act != GEMM_ACT_NONE) ? 1 : 0;
+  ka.tile_map = nullptr;
+  if (p.order == GEMM_ORDER_HILBERT && !fixed_scratch) {   // the fixed-scratch path allocates nothing
+    s = hilbert_map_for(dev, p.m_tiles, p.n_tiles, &ka.tile_map);
+    if (s != GEMM_OK) return s;
+  }
   if (p.sk_iters) {
     s = fixed_scratch ? noalloc_scratch(dev, stream, static_cast<size_t>(p.scratch_bytes), &ka.ws,
                                         &ka.ws_flags, &ka.epoch)
@@ -671,6 +736,32 @@ void gemm_tile_coord(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_
   tile_coord(t, m_tiles, n_tiles, group_m, &m, &n);
   *m_blk = m;
   *n_blk = n;
+}
+
+int32_t gemm_tile_order(int order, int32_t m_tiles, int32_t n_tiles, int32_t group_m,
+                        int32_t* m_blk, int32_t* n_blk, int32_t max_tiles) {
+  if (m_tiles <= 0 || n_tiles <= 0 || !m_blk || !n_blk || max_tiles < 0) return -1;
+  const int64_t tiles = int64_t(m_tiles) * n_tiles;
+  if (order == GEMM_ORDER_GROUPED) {
+    if (group_m <= 0) return -1;
+    for (int64_t t = 0; t < tiles && t < max_tiles; ++t) {
+      int m = 0, n = 0;
+      tile_coord(static_cast<int>(t), m_tiles, n_tiles, group_m, &m, &n);
+      m_blk[t] = m;
+      n_blk[t] = n;
+    }
+    return static_cast<int32_t>(tiles);
+  }
+  if (order == GEMM_ORDER_HILBERT) {
+    std::vector<int2> v;
+    if (!hilbert_tiles(m_tiles, n_tiles, &v)) return -1;
+    for (size_t t = 0; t < v.size() && t < static_cast<size_t>(max_tiles); ++t) {
+      m_blk[t] = v[t].x;
+      n_blk[t] = v[t].y;
+    }
+    return static_cast<int32_t>(v.size());
+  }
+  return -1;
 }
 
 int32_t gemm_work_items(int32_t unit, int32_t units, int32_t dp_tiles, int64_t sk_iters,

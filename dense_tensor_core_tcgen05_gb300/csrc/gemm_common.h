@@ -35,6 +35,35 @@ GEMM_HD void tile_coord(int t, int m_tiles, int n_tiles, int group_m, int* m_blk
   *n_blk = r / rows_in_group;
 }
 
+// Cell (x, y) at index d of the Hilbert curve over a 2^k x 2^k grid (the order the
+// lecture "The Asynchronous Kernel: Tensor Cores & TMA" compares in "Scheduling
+// is geometry": a space-filling curve whose every prefix stays compact).  Built
+// one level at a time from the lowest: two bits of d pick the quadrant, and the
+// cells placed so far are turned into that quadrant's orientation (a transpose,
+// plus a reflection in the last quadrant) so consecutive indices stay adjacent.
+GEMM_HD void hilbert_cell(int k, long long d, int* x, int* y) {
+  int cx = 0, cy = 0;
+  for (int lvl = 0; lvl < k; ++lvl) {
+    const int s = 1 << lvl;
+    const int qx = static_cast<int>((d >> 1) & 1);
+    const int qy = static_cast<int>((d ^ qx) & 1);
+    if (qy == 0) {
+      if (qx == 1) {
+        cx = s - 1 - cx;
+        cy = s - 1 - cy;
+      }
+      const int t = cx;
+      cx = cy;
+      cy = t;
+    }
+    cx += s * qx;
+    cy += s * qy;
+    d >>= 2;
+  }
+  *x = cx;
+  *y = cy;
+}
+
 // -------------------------------------------------------- tcgen05 descriptors
 //
 // Instruction descriptor of tcgen05.mma kind::f16 (32 bits, public PTX ISA):
@@ -160,6 +189,22 @@ struct KernelArgs {
   int bias_kind;         // EPI_BIAS_*
   int act;               // EPI_ACT_*
   int epi;               // 1 when bias_kind or act is set (selects the fused epilogue)
+  // Tile order: NULL = grouped (tile_coord), else (m block, n block) of tile t
+  // in Hilbert-curve order, num_tiles entries.
+  const int2* tile_map;
 };
+
+#if defined(__CUDACC__)
+// Output block (m_blk, n_blk) of tile index t in the launch's tile order.
+__device__ __forceinline__ void tile_of(const KernelArgs& a, int t, int* m_blk, int* n_blk) {
+  if (a.tile_map) {
+    const int2 v = __ldg(a.tile_map + t);
+    *m_blk = v.x;
+    *n_blk = v.y;
+  } else {
+    tile_coord(t, a.m_tiles, a.n_tiles, a.group_m, m_blk, n_blk);
+  }
+}
+#endif
 
 }  // namespace gemm_tc

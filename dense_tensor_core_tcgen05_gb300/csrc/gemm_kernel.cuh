@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       work_begin(wi);
       while (ok && wi.next(&w)) {
         int mb, nb, kb_begin, kb_end;
-        tile_coord(w.tile, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
+        tile_of(args, w.tile, &mb, &nb);
         kb_range(w, &kb_begin, &kb_end);
         const int a_row = mb * TILE_M + static_cast<int>(rank) * BM;
         const int b_col = nb * BN + static_cast<int>(rank) * L::B_COLS;
@@ -846,7 +846,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     work_begin(wi);
     for (; ok && wi.next(&w); ++tl) {
       int mb, nb;
-      tile_coord(w.tile, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
+      tile_of(args, w.tile, &mb, &nb);
       const int buf = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
       if (args.epi) {
@@ -1012,7 +1012,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       EpiState st{smem + L::off_epi + ew * EPI_BUFS * L::EPI_BUF_BYTES, &cload[ew * EPI_BUFS], 0,
                   -1, 0};
       int mb, nb;
-      tile_coord(unit0, args.m_tiles, args.n_tiles, args.group_m, &mb, &nb);
+      tile_of(args, unit0, &mb, &nb);
       const int row0 = mb * BM + quarter * 32;
       const int prow = quarter * 32 + r;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);

@@ -108,7 +108,21 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *             tiles data-parallel and splits the remaining tiles' k-groups evenly
  *             over all CTAs (or CTA pairs); a tile's partial sums are added by the
  *             CTA that finishes it, in a fixed order, through a scratch buffer the
- *             library keeps per device and stream.  Ignored with split_k > 1. */
+ *             library keeps per device and stream.  Ignored with split_k > 1.
+ *   order     tile order of the persistent scheduler: 1 grouped (group_m
+ *             tile-rows at a time, column-major inside the group; the default),
+ *             2 Hilbert curve (the order the lecture "The Asynchronous Kernel:
+ *             Tensor Cores & TMA", section "Scheduling is geometry", compares
+ *             with the grouped one: every prefix of the walk stays compact).
+ *             The Hilbert order walks the curve over the smallest power-of-two
+ *             square holding the tile grid and keeps the cells inside the grid;
+ *             when that square is more than 16 times the grid (a very elongated
+ *             grid) or the grid has more than 2^22 tiles the grouped order is
+ *             used.  Its table (8 bytes per tile) is built on the host and kept
+ *             on the device per grid shape by the library (gemm_ex_noalloc
+ *             always uses the grouped order). */
+enum { GEMM_ORDER_AUTO = 0, GEMM_ORDER_GROUPED = 1, GEMM_ORDER_HILBERT = 2 };
+
 typedef struct {
   int32_t bn;
   int32_t group_m;
@@ -116,7 +130,8 @@ typedef struct {
   int32_t cta_group;
   int32_t split_k;
   int32_t stream_k;
-  int32_t reserved[2];  /* must be zero */
+  int32_t order;
+  int32_t reserved;  /* must be zero */
 } gemm_config_t;
 
 /* gemm with an explicit configuration (cfg may be NULL = gemm()).  Same
@@ -243,6 +258,8 @@ typedef struct {
   int32_t cta_group, split_k;
   int32_t groups;      /* k-groups (ring stages) per tile */
   int32_t dp_tiles;    /* tiles of the data-parallel phase */
+  int32_t order;       /* GEMM_ORDER_GROUPED or GEMM_ORDER_HILBERT */
+  int32_t reserved;
   int64_t sk_iters;    /* stream-K iterations (tile k-groups) after it; 0 = none */
   int64_t scratch_bytes; /* stream-K scratch the launch uses (0 = none) */
 } gemm_plan_t;
@@ -255,6 +272,13 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
  * for t in [0, m_tiles * n_tiles). */
 void gemm_tile_coord(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_m,
                      int32_t* m_blk, int32_t* n_blk);
+
+/* A whole tile order on the host: order GEMM_ORDER_GROUPED (with group_m) or
+ * GEMM_ORDER_HILBERT; writes the (m_blk, n_blk) of tiles 0 .. m_tiles*n_tiles-1
+ * (at most max_tiles of them) and returns the tile count, or -1 when the order
+ * is unknown or (Hilbert) not used for this grid shape. */
+int32_t gemm_tile_order(int order, int32_t m_tiles, int32_t n_tiles, int32_t group_m,
+                        int32_t* m_blk, int32_t* n_blk, int32_t max_tiles);
 
 /* The work split of one unit (a CTA, or a CTA pair) for a plan, computed on the
  * host exactly as the kernel walks it: whole tiles unit, unit + units, ... below

@@ -178,10 +178,11 @@ def test_plan_split_k_overrides(g):
     # reserved fields must be zero
     import ctypes
     cfg = g.gemm_config_t()
-    cfg.reserved[1] = 7
+    cfg.reserved = 7
     p = g.gemm_plan_t()
     lib = g.library()
     assert lib.gemm_plan(256, 256, 256, 1, 1, 0, 152, ctypes.byref(cfg), ctypes.byref(p)) == 1
+    assert g.gemm_plan(256, 256, 256, 1, 1, 0, 152, {"order": 3})[0] == g.GEMM_ERR_INVALID_ARG
 
 
 def test_stream_k_override(g):
@@ -319,3 +320,70 @@ def test_bias_act_argument_checks(g, bias, kind, act, M, expect):
     s = g.gemm_bias_act(M, 64, 64, 1.0, ALIGNED, 64, ALIGNED, 64, 0.0, ALIGNED, 64, 0, 2, 0,
                         bias, kind, act, 0)
     assert s == expect
+
+
+# ------------------------------------------------------------ tile orders
+
+def _panel_counts(golden):
+    out = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", golden)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, v = line.split()
+            out[k] = float(v) if "." in v else int(v)
+    return out
+
+
+def _avg_panels_sliding(order, window):
+    """Mean over every run of `window` consecutive tiles of the A panels plus B
+    panels it touches (distinct tile rows + distinct tile columns)."""
+    tot = 0
+    for s0 in range(len(order) - window + 1):
+        w = order[s0:s0 + window]
+        tot += len({m for m, _ in w}) + len({n for _, n in w})
+    return tot / (len(order) - window + 1)
+
+
+def test_tile_orders_match_the_lectures_panel_counts(g):
+    """The lecture's "Scheduling is geometry" counts panels of 8 tiles in flight:
+    9.86 row by row, 7.02 grouped, 6.67 along a Hilbert curve (8 x 8 tile grid,
+    groups of 4 tile-rows, as in its 4 x 2 block example)."""
+    pc = _panel_counts("panel_counts.txt")
+    mt = nt = pc["grid"]
+    w = pc["window"]
+    row = g.gemm_tile_order(g.GEMM_ORDER_GROUPED, mt, nt, 1)
+    grp = g.gemm_tile_order(g.GEMM_ORDER_GROUPED, mt, nt, pc["group_rows"])
+    hil = g.gemm_tile_order(g.GEMM_ORDER_HILBERT, mt, nt)
+    assert round(_avg_panels_sliding(row, w), 2) == pc["row_major"]
+    assert round(_avg_panels_sliding(grp, w), 2) == pc["grouped"]
+    assert round(_avg_panels_sliding(hil, w), 2) == pc["hilbert"]
+
+
+@pytest.mark.parametrize("mt,nt", [(1, 1), (8, 8), (32, 32), (24, 24), (28, 20), (3, 17), (17, 3),
+                                   (64, 5), (5, 64), (1, 16), (33, 40)])
+def test_hilbert_order_covers_each_tile_once(g, mt, nt):
+    hil = g.gemm_tile_order(g.GEMM_ORDER_HILBERT, mt, nt)
+    if hil is None:   # too elongated for the enclosing square: the planner keeps grouped
+        side = 1 << max(0, (max(mt, nt) - 1).bit_length())
+        assert side * side > 16 * mt * nt
+        s, p = g.gemm_plan(mt * 128, nt * 256, 512, 1, 1, 0, 152,
+                           {"order": 2, "cta_group": 1, "bn": 256})
+        assert s == 0 and p.order == g.GEMM_ORDER_GROUPED
+        return
+    assert sorted(hil) == [(m, n) for m in range(mt) for n in range(nt)]
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 5])
+def test_hilbert_steps_are_adjacent_on_power_of_two_squares(g, k):
+    n = 1 << k
+    hil = g.gemm_tile_order(g.GEMM_ORDER_HILBERT, n, n)
+    assert hil[0] == (0, 0)
+    for (a, b), (c, d) in zip(hil, hil[1:]):
+        assert abs(a - c) + abs(b - d) == 1
+
+
+def test_plan_reports_the_order(g):
+    s, p = g.gemm_plan(8192, 8192, 8192, 1, 2, 2, 152, {"order": 2})
+    assert s == 0 and p.order == g.GEMM_ORDER_HILBERT
+    s, p = g.gemm_plan(8192, 8192, 8192, 1, 2, 2, 152)
+    assert s == 0 and p.order == g.GEMM_ORDER_GROUPED
