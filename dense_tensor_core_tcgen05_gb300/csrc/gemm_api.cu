@@ -304,16 +304,25 @@ void choose_unit(int64_t M, int64_t N, int num_sms, int* bn_out, bool* pair_out)
 int choose_split(int64_t M, int64_t N, int64_t K, int num_sms, int* bn_out) {
   if (M > BM) return 1;
   const int64_t kb = ceil_div(K, BK);
-  const struct { int bn, s; } cands[3] = {{128, 2}, {256, 4}, {256, 2}};
-  for (const auto& c : cands) {
-    const int64_t nt = ceil_div(N, c.bn);
-    if (nt * c.s <= num_sms && kb >= 8 * c.s &&
-        nt * c.s >= std::min<int64_t>(ceil_div(N, 64), num_sms / 2)) {
-      *bn_out = c.bn;
-      return c.s;
+  // The most CTAs that fit one wave, each with at least 8 k-blocks; on a tie the
+  // fewer splits (less partial-sum exchange), then the wider tile.  Listed in
+  // that order of preference.
+  const struct { int bn, s; } cands[7] = {{256, 2}, {128, 2}, {64, 2}, {256, 4},
+                                          {128, 4}, {64, 4}, {128, 8}};
+  int best = -1;
+  int64_t best_ctas = 0;
+  for (int i = 0; i < 7; ++i) {
+    const int64_t ctas = ceil_div(N, cands[i].bn) * cands[i].s;
+    if (ctas <= num_sms && kb >= 8 * cands[i].s && ctas > best_ctas) {
+      best = i;
+      best_ctas = ctas;
     }
   }
-  return 1;
+  // worth splitting only when it reaches half the SMs or more than the
+  // unsplit 64-wide tiles would
+  if (best < 0 || best_ctas < std::min<int64_t>(ceil_div(N, 64), num_sms / 2)) return 1;
+  *bn_out = cands[best].bn;
+  return cands[best].s;
 }
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layout, int num_sms,
@@ -519,8 +528,15 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   const bool pair = p.cta_group == 2;
   const int ko = ko_for(p.bn, pair);
   const int b_cols = b_cols_per_cta(p.bn, pair);
+  // A single row of tiles with M < BM (K-major A): copy only the first
+  // ceil8(M) rows of A per k-block (a box of whole 8-row swizzle atoms); the
+  // smem rows beyond feed only accumulator rows >= M, which are never stored.
+  // Saves the zero-fill of the other rows, and TMA is slow on a box whose first
+  // swizzle atom is only partly inside the tensor.
+  const int a_box_rows = (!pair && !a_col && p.m_tiles == 1 && M < BM)
+                             ? static_cast<int>((M + 7) / 8 * 8) : BM;
   bool ok = a_col ? encode_2d(&mp.a, din, A, M, K, lda * 2, ATOM_MN, BK)
-                  : encode_2d(&mp.a, din, A, K, M, lda * 2, BK, BM);
+                  : encode_2d(&mp.a, din, A, K, M, lda * 2, BK, a_box_rows);
   ok = ok && (b_col ? encode_2d(&mp.b, din, B, K, N, ldb * 2, BK, b_cols)
                     : encode_2d(&mp.b, din, B, N, K, ldb * 2, ATOM_MN, BK));
   ok = ok && encode_2d(&mp.c, tma_dtype(out_dtype), C, N, M, ldc * out_size(out_dtype),
@@ -531,7 +547,8 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   const int64_t a_full = a_col ? M / ATOM_MN : K / BK;
   const int64_t b_full = b_col ? K / BK : N / ATOM_MN;
   int a_full3d = 0, b_full3d = 0;
-  if (a_full > 0 && (a_col ? encode_3d(&mp.a3, din, A, K, a_full, lda * 2, ko * BK, BM / ATOM_MN)
+  if (a_full > 0 && a_box_rows == BM &&
+      (a_col ? encode_3d(&mp.a3, din, A, K, a_full, lda * 2, ko * BK, BM / ATOM_MN)
                            : encode_3d(&mp.a3, din, A, M, a_full, lda * 2, BM, ko)))
     a_full3d = static_cast<int>(a_full);
   else
@@ -570,6 +587,7 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.a_hint = p.m_tiles == 1 && p.n_tiles > 1 ? 2 : (p.n_tiles == 1 && p.m_tiles > 1 ? 1 : 0);
   ka.b_hint = p.m_tiles == 1 && p.n_tiles > 1 ? 1 : (p.n_tiles == 1 && p.m_tiles > 1 ? 2 : 0);
   ka.a_full3d = a_full3d;
+  ka.a_box_rows = a_box_rows;
   ka.b_full3d = b_full3d;
   ka.groups = p.groups;
   ka.dp_tiles = p.dp_tiles;

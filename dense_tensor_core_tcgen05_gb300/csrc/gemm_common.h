@@ -189,6 +189,10 @@ struct KernelArgs {
   int bias_kind;         // EPI_BIAS_*
   int act;               // EPI_ACT_*
   int epi;               // 1 when bias_kind or act is set (selects the fused epilogue)
+  // Rows of A each k-block copy brings (BM, or fewer for a single row of tiles
+  // with M < BM: the rows of smem beyond them only feed accumulator rows >= M,
+  // which are never stored).
+  int a_box_rows;
   // Tile order: NULL = grouped (tile_coord), else (m block, n block) of tile t
   // in Hilbert-curve order, num_tiles entries.
   const int2* tile_map;

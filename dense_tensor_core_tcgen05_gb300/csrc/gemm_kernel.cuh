@@ -426,11 +426,14 @@ __device__ __forceinline__ void end_chunk(EpiState& st, const uint8_t* stg, cons
 }
 
 // Shared-memory address of 16-byte piece `piece` of row `row` in a split-K
-// slice block (128 rows of SLICE floats; pieces XOR-swizzled by row, so the 32
-// rows of a warp touch every bank once per 8 rows).
+// slice block (128 rows of SLICE floats; pieces XOR-swizzled by row so that the
+// 8 rows sharing a 1 KB span use all 8 bank groups: by row & 7 with 8 or more
+// pieces per row, by (row / (8 / P)) & (P - 1) with P < 8 pieces per row).
 template <int SLICE>
 __device__ __forceinline__ uint32_t slice_addr(uint32_t base, int row, int piece) {
-  return base + static_cast<uint32_t>(row * (SLICE * 4) + ((piece ^ (row & 7)) << 4));
+  constexpr int P = SLICE / 4;
+  const int sw = P >= 8 ? (row & 7) : ((row / (8 / P)) & (P - 1));
+  return base + static_cast<uint32_t>(row * (SLICE * 4) + ((piece ^ sw) << 4));
 }
 
 // Stream-K hand-off: a CTA publishes its partial tile with a release store of
@@ -473,7 +476,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   static_assert(BN % CHUNK == 0, "tile width must be a whole number of epilogue chunks");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N must be in [16,256], N%16==0");
   static_assert(!(PAIR && SPLITK), "pair and split-K modes are exclusive");
-  static_assert(!SPLITK || SLICE % CHUNK == 0, "each split CTA reduces whole epilogue chunks");
+  static_assert(!SPLITK || (SLICE >= 16 && (SLICE % CHUNK == 0 || CHUNK % SLICE == 0)),
+                "a split CTA finishes whole epilogue chunks or one narrower slice");
   // split-K: the fp32 slices a CTA sends to its SPLIT-1 peers and the ones it
   // receives from them share the (idle) ring
   constexpr int SLICE_BYTES = BM * SLICE * 4;
@@ -591,7 +595,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (args.inject_skip != 0 && it + 1 == static_cast<uint32_t>(args.inject_skip)) continue;
           // the leader's full[s] counts the bytes of both CTAs of a pair
-          if (leader) mbar_arrive_expect_tx(&full[s], (PAIR ? 2 : 1) * nkb * L::KB_BYTES);
+          if (leader)
+            mbar_arrive_expect_tx(&full[s], PAIR ? 2 * nkb * L::KB_BYTES
+                                                 : nkb * (args.a_box_rows * BK * 2 + L::KB_B_BYTES));
           uint8_t* sa = smem + L::off_a + s * L::A_BYTES;
           uint8_t* sb = smem + L::off_b + s * L::B_BYTES;
           const uint32_t bar_c = PAIR ? map_to_rank(&full[s], 0) : 0;
@@ -878,13 +884,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int qi = 0; qi < SPLIT - 1; ++qi) {
           const int q = qi < static_cast<int>(srank) ? qi : qi + 1;
           const uint32_t sbase = smem_u32(smem) + static_cast<uint32_t>(qi * SLICE_BYTES);
+          // 32 columns per TMEM load; a 16-column slice takes the first half of
+          // one (the load stays inside the 2 x BN allocated columns)
+          constexpr int LOADS = SLICE >= 32 ? SLICE / 32 : 1;
+          constexpr int PIECES = SLICE >= 32 ? 8 : SLICE / 4;
 #pragma unroll 1
-          for (int c = 0; c < SLICE / 32; ++c) {
+          for (int c = 0; c < LOADS; ++c) {
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_row, v, q * SLICE + c * 32);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < PIECES; ++j)
               st_shared_v4(slice_addr<SLICE>(sbase, prow, c * 8 + j),
                            make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
           }
@@ -1019,9 +1029,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t rbase = smem_u32(smem) + RECV0;
       bool ok = wait_warp<true>(rfull, 0, abort_flag, args, SITE_SPLITK_SLICES);
       received = ok;
+      // chunks of PCH columns: whole epilogue chunks, or one slice narrower than a
+      // chunk, finished through the predicated direct stores of a ragged edge
+      constexpr int PCH = SLICE < CHUNK ? SLICE : CHUNK;
+      constexpr bool NARROW = PCH < CHUNK;
+      constexpr int PIECES = PCH * (OUT == OUT_F32 ? 4 : 2) / 16;   // 16-byte pieces per row
 #pragma unroll 1
-      for (int c = 0; ok && c < SLICE / CHUNK; ++c) {
-        const int tcol = static_cast<int>(srank) * SLICE + c * CHUNK;   // column inside the tile
+      for (int c = 0; ok && c < SLICE / PCH; ++c) {
+        const int tcol = static_cast<int>(srank) * SLICE + c * PCH;   // column inside the tile
         const int col0 = nb * BN + tcol;
         EpiBias eb{0.0f, 0.0f, 0.0f, 0.0f};
         if (args.epi) eb = load_epi_bias<CHUNK>(args, col0, row0 + r);
@@ -1030,16 +1045,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
-        const bool ragged = args.n_ragged && (col0 + CHUNK > args.N);
+        const bool ragged = NARROW || (args.n_ragged && (col0 + CHUNK > args.N));
         const bool skip_store = col0 >= args.N || row0 >= args.M;
         uint32_t v0[32], v1[32];
         tmem_ld_32x32b_x32(t_row, v0, tcol);
-        if (CHUNK == 64) tmem_ld_32x32b_x32(t_row, v1, tcol + 32);
+        if (PCH == 64) tmem_ld_32x32b_x32(t_row, v1, tcol + 32);
         tmem_ld_wait();
         uint8_t* rowp = stg + r * SW;
         constexpr int E = OUT == OUT_F32 ? 4 : 8;   // outputs per 16-byte piece
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < PIECES; ++j) {
           const uint32_t* own = (OUT == OUT_F32) ? (v0 + 4 * j) : ((j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4)));
           float x[E];
 #pragma unroll
@@ -1053,7 +1068,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const uint32_t blk = rbase + static_cast<uint32_t>((q < static_cast<int>(srank) ? q : q - 1) * SLICE_BYTES);
 #pragma unroll
               for (int h = 0; h < E / 4; ++h) {
-                const uint4 pv = ld_shared_v4(slice_addr<SLICE>(blk, prow, (c * CHUNK + E * j) / 4 + h));
+                const uint4 pv = ld_shared_v4(slice_addr<SLICE>(blk, prow, (c * PCH + E * j) / 4 + h));
                 x[4 * h + 0] += __uint_as_float(pv.x);
                 x[4 * h + 1] += __uint_as_float(pv.y);
                 x[4 * h + 2] += __uint_as_float(pv.z);

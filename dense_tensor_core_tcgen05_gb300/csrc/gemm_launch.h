@@ -46,7 +46,9 @@ cudaError_t launch_gemm_f16(int bn, bool pair, int split, const OperandMaps& m,
 
 // Split-K cluster shapes that have kernel instances: (bn, split).
 constexpr bool split_supported(int bn, int split) {
-  return (bn == 256 && (split == 2 || split == 4)) || (bn == 128 && split == 2);
+  return (bn == 256 && (split == 2 || split == 4)) ||
+         (bn == 128 && (split == 2 || split == 4 || split == 8)) ||
+         (bn == 64 && (split == 2 || split == 4));
 }
 
 }  // namespace gemm_tc

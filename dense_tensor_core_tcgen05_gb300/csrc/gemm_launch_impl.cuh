@@ -69,6 +69,10 @@ cudaError_t GEMM_LAUNCH_NAME(int bn, bool pair, int split, const OperandMaps& m,
     if (bn == 256 && split == 2) return launch_inst<256, false, 2>(m, args, grid, stream, dev);
     if (bn == 256 && split == 4) return launch_inst<256, false, 4>(m, args, grid, stream, dev);
     if (bn == 128 && split == 2) return launch_inst<128, false, 2>(m, args, grid, stream, dev);
+    if (bn == 128 && split == 4) return launch_inst<128, false, 4>(m, args, grid, stream, dev);
+    if (bn == 128 && split == 8) return launch_inst<128, false, 8>(m, args, grid, stream, dev);
+    if (bn == 64 && split == 2) return launch_inst<64, false, 2>(m, args, grid, stream, dev);
+    if (bn == 64 && split == 4) return launch_inst<64, false, 4>(m, args, grid, stream, dev);
     return cudaErrorInvalidValue;
   }
   if (pair) {

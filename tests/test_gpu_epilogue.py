@@ -12,9 +12,10 @@ from gpu_util import check_against_oracle, operands, pad8, run_library, sample_r
 pytestmark = pytest.mark.gpu
 
 MODES = [{"cta_group": 1, "bn": 256}, {"cta_group": 1, "bn": 64}, {"cta_group": 2},
-         {"split_k": 2}, {"split_k": 4}, {"cta_group": 1, "stream_k": 2},
-         {"cta_group": 2, "stream_k": 2}]
-MODE_IDS = ["cta1", "cta1-bn64", "pair", "splitk2", "splitk4", "streamk1", "streamk2"]
+         {"split_k": 2}, {"split_k": 4}, {"split_k": 4, "bn": 64}, {"split_k": 8, "bn": 128},
+         {"cta_group": 1, "stream_k": 2}, {"cta_group": 2, "stream_k": 2}]
+MODE_IDS = ["cta1", "cta1-bn64", "pair", "splitk2", "splitk4", "splitk4-bn64", "splitk8-bn128",
+            "streamk1", "streamk2"]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -64,7 +64,8 @@ def test_probe_identity_left(a_col, b_col, in_dtype, mode):
 
 PROBE_CFGS = [{"bn": 64}, {"bn": 128}, {"bn": 256}, {"bn": 128, "cta_group": 2},
               {"bn": 256, "cta_group": 2}, {"bn": 128, "split_k": 2}, {"bn": 256, "split_k": 2},
-              {"bn": 256, "split_k": 4}]
+              {"bn": 256, "split_k": 4}, {"bn": 128, "split_k": 4}, {"bn": 128, "split_k": 8},
+              {"bn": 64, "split_k": 2}, {"bn": 64, "split_k": 4}]
 
 
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
@@ -192,6 +193,8 @@ def test_odd_shapes_integer_exact(shape, a_col, b_col, mode):
 @pytest.mark.parametrize("cfg", PROBE_CFGS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
 def test_formats_and_tile_widths(out_dtype, in_dtype, cfg):
     M, N, K = 300, 520, 333
+    if not _mode_fits(cfg, K):
+        K = 64 * cfg["split_k"] + 13   # enough k-blocks for every split, still ragged
     A, B = operands(M, N, K, in_dtype, False, False, dist="uniform", seed=cfg["bn"], pad=True)
     out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype=in_dtype, out_dtype=out_dtype,
                          a_col=False, b_col=False, cfg=cfg, ldc=pad8(N))

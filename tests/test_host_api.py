@@ -164,9 +164,17 @@ def test_plan_split_k_overrides(g):
     assert s == 0 and (p.split_k, p.bn, p.grid, p.num_tiles) == (2, 256, 32, 16)
     s, p = g.gemm_plan(128, 4096, 4096, 1, 1, 2, 152, {"split_k": 2, "bn": 128})
     assert s == 0 and (p.split_k, p.bn, p.grid) == (2, 128, 64)
-    for bad in ({"split_k": 3}, {"split_k": 4, "bn": 128}, {"split_k": 2, "cta_group": 2},
-                {"split_k": 2, "bn": 64}):
+    for bad in ({"split_k": 3}, {"split_k": 8, "bn": 256}, {"split_k": 2, "cta_group": 2},
+                {"split_k": 8, "bn": 64}, {"split_k": 16, "bn": 128}):
         assert g.gemm_plan(256, 4096, 4096, 1, 1, 2, 152, bad)[0] == g.GEMM_ERR_INVALID_ARG, bad
+    # narrower slices: 128-wide split 4 / 8, 64-wide split 2 / 4
+    for good, grid in (({"split_k": 4, "bn": 128}, 128), ({"split_k": 8, "bn": 128}, 256),
+                       ({"split_k": 2, "bn": 64}, 128), ({"split_k": 4, "bn": 64}, 256)):
+        s, p = g.gemm_plan(128, 4096, 4096, 1, 1, 2, 152, good)
+        assert s == 0 and (p.split_k, p.bn, p.grid) == (good["split_k"], good["bn"], grid), good
+    # small-N decode shapes: as many CTAs as fit one wave (128 for N = 2048)
+    s, p = g.gemm_plan(16, 2048, 8192, 1, 1, 2, 152)
+    assert s == 0 and (p.bn, p.split_k, p.grid) == (64, 4, 128)
     # a manual tile setting turns the automatic split off
     s, p = g.gemm_plan(128, 8192, 8192, 1, 1, 2, 152, {"cta_group": 1, "bn": 64})
     assert s == 0 and (p.split_k, p.bn, p.num_tiles) == (1, 64, 128)
