@@ -383,6 +383,7 @@ def run_ours(args, rank, world, device):
                       "entry_point": "gemm_host (pinned host operands)"}
         if not args.no_suite:
             out["suite"] = run_suite(g, args, device, peaks, cfg)
+            out["odd_tail"] = run_odd_tail(g, device, peaks)
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(w)
         out["kernel_hash"] = kernel_source_hash()
@@ -437,6 +438,67 @@ def run_suite(g, args, device, peaks, skip_cfg):
                           "bias_relu_mean_over_plain_mean": statistics.mean(ftimes) / statistics.mean(times)}
         del a, b, c, c0
         torch.cuda.empty_cache()
+    return res
+
+
+# Second workload: odd and tail shapes ("GEMM From Naive CUDA to Tensor Cores":
+# its default 257 x 263 x 251 and the index-check fixtures 73 x 61 x 67,
+# 31 x 29 x 37, 17 x 65 x 19; its M = N = 64 sweep over K = 32, 256, 4096) and
+# decode-like shapes with a few rows against a wide, deep B (column-major), the
+# split-K shapes beyond the 128-row skinny workload.  Timed like the suite; the
+# inputs are seeded normal draws made on the device (their parity is covered by
+# the GPU tests on the same shapes).
+ODD_TAIL = [
+    # name, M, N, K, in, out, B column-major
+    ("lab_257x263x251", 257, 263, 251, "f16", "f32", False),
+    ("lab_73x61x67", 73, 61, 67, "f16", "f32", False),
+    ("lab_31x29x37", 31, 29, 37, "f16", "f32", False),
+    ("lab_17x65x19", 17, 65, 19, "f16", "f32", False),
+    ("ksweep_64x64x32", 64, 64, 32, "f16", "f32", False),
+    ("ksweep_64x64x256", 64, 64, 256, "f16", "f32", False),
+    ("ksweep_64x64x4096", 64, 64, 4096, "f16", "f32", False),
+    ("decode_1x8192x8192", 1, 8192, 8192, "bf16", "bf16", True),
+    ("decode_16x4096x8192", 16, 4096, 8192, "bf16", "bf16", True),
+    ("decode_32x2048x8192", 32, 2048, 8192, "bf16", "bf16", True),
+    ("decode_64x8192x2048", 64, 8192, 2048, "bf16", "bf16", True),
+    ("decode_8x14336x4096", 8, 14336, 4096, "bf16", "bf16", True),
+]
+
+
+def run_odd_tail(g, device, peaks):
+    import torch
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    flush = L2Flush(device)
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    gen = torch.Generator(device=device)
+    res = {}
+    for i, (name, M, N, K, din, dout, b_col) in enumerate(ODD_TAIL):
+        gen.manual_seed(5000 + i)
+        pad = lambda n: (n + 7) // 8 * 8   # noqa: E731  (16-byte row pitches)
+        a = torch.randn(M, pad(K), device=device, generator=gen).to(tdt[din])[:, :K]
+        b = (torch.randn(N, pad(K), device=device, generator=gen).to(tdt[din])[:, :K] if b_col
+             else torch.randn(K, pad(N), device=device, generator=gen).to(tdt[din])[:, :N])
+        c = torch.empty(M, pad(N), device=device, dtype=tdt[dout])[:, :N]
+        w = {"alpha": 1.0, "beta": 0.0, "a_col": False, "b_col": b_col}
+        times = time_gemm(g, w, a, b, c, None, 20, 5, torch.cuda.current_stream(device), flush)
+        ms = statistics.median(times)
+        bt = b.t() if b_col else b
+        ctimes = []
+        for _ in range(25):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, bt)
+            e1.record()
+            torch.cuda.synchronize()
+            ctimes.append(e0.elapsed_time(e1))
+        cub = statistics.median(ctimes[5:])
+        byts = 2 * (M * K + K * N) + (4 if dout == "f32" else 2) * M * N
+        res[name] = {"M": M, "N": N, "K": K, "median_ms": ms,
+                     "tflops": 2 * M * N * K / (ms * 1e-3) / 1e12,
+                     "gbs_algorithmic": byts / (ms * 1e-3) / 1e9,
+                     "frac_hbm": byts / (ms * 1e-3) / 1e9 / hbm,
+                     "cublas_ms": cub}
     return res
 
 

@@ -227,6 +227,27 @@ def test_k_sweep_64x64(K):
                          a_col=False, b_col=False)
 
 
+@pytest.mark.parametrize("K", [32, 256, 4096])
+def test_k_sweep_64x64_against_both_references(K):
+    """The lab's K-sweep against its two references ("The two-reference testing
+    protocol"): the rounded-input oracle (the gate) and the original fp32 draws.
+    The second differs from the first by the fp16 rounding of the inputs, at most
+    (2u + u^2) sum_k |a_ik||b_kj| with u = 2^-11, whatever K is."""
+    M = N = 64
+    A, B = operands(M, N, K, "f16", False, False, dist="uniform", seed=K)
+    a0 = si.draw("uniform", 1000 + K, M * K, 1.0).reshape(M, K).astype(np.float64)
+    b0 = si.draw("uniform", 2000 + K, K * N, 1.0).reshape(K, N).astype(np.float64)
+    out, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="f16", out_dtype="f32",
+                         a_col=False, b_col=False)
+    gv = oracle.decode(out, "f32")
+    _, exact, scale = oracle.gemm(A, B, M=M, N=N, K=K, in_dtype="f16", out_dtype="f32")
+    err_rounded = np.abs(gv - exact)
+    assert np.all(err_rounded <= 1e-3 * scale + 1e-6)
+    err_original = np.abs(gv - a0 @ b0)
+    u = 2.0 ** -11
+    assert np.all(err_original <= err_rounded + (2 * u + u * u) * (np.abs(a0) @ np.abs(b0)) + 1e-9)
+
+
 # ------------------------------------------------------------ stream-K
 
 SK_CASES = [
