@@ -32,8 +32,9 @@ _LIB = os.path.join(_BUILD, "liboracle_gemm.so")
 _lock = threading.Lock()
 _lib = None
 
-FMT = {"f16": 0, "bf16": 1, "f32": 2}
-_BITS_DT = {"f16": np.uint16, "bf16": np.uint16, "f32": np.uint32}
+FMT = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4}
+_BITS_DT = {"f16": np.uint16, "bf16": np.uint16, "f32": np.uint32, "e4m3": np.uint8,
+            "e5m2": np.uint8}
 
 
 def build(force: bool = False) -> str:

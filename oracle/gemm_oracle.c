@@ -40,7 +40,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2 };
+enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2, OR_E4M3 = 3, OR_E5M2 = 4 };
 enum { OR_BIAS_NONE = 0, OR_BIAS_COL = 1, OR_BIAS_ROW = 2 };
 enum { OR_ACT_NONE = 0, OR_ACT_RELU = 1 };
 
@@ -70,6 +70,36 @@ static double decode_bf16(uint16_t h) {
     return s ? -v : v;
 }
 
+/* The two 8-bit formats of the OCP FP8 definition (the FP8 variant the Ada GEMM
+ * page lists as written but untested):
+ *   E4M3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits; no infinities, the
+ *         pattern S.1111.111 is NaN, the largest finite value is 448.
+ *   E5M2: 1 sign, 5 exponent bits (bias 15), 2 mantissa bits; IEEE-style
+ *         infinities (exponent 31, mantissa 0) and NaNs. */
+static double decode_e4m3(uint8_t b) {
+    int s = (b >> 7) & 1, e = (b >> 3) & 0xF, m = b & 0x7;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -9);                  /* m/8 * 2^(1-7) */
+    else if (e == 15 && m == 7)
+        v = NAN;
+    else
+        v = ldexp((double)(8 + m), e - 10);         /* (1 + m/8) 2^(e-7) */
+    return s ? -v : v;
+}
+
+static double decode_e5m2(uint8_t b) {
+    int s = (b >> 7) & 1, e = (b >> 2) & 0x1F, m = b & 0x3;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -16);                 /* m/4 * 2^(1-15) */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(4 + m), e - 17);         /* (1 + m/4) 2^(e-15) */
+    return s ? -v : v;
+}
+
 static double decode_f32(uint32_t w) {
     int s = (w >> 31) & 1, e = (w >> 23) & 0xFF;
     uint32_t m = w & 0x7FFFFF;
@@ -84,9 +114,11 @@ static double decode_f32(uint32_t w) {
 }
 
 static double decode(const void* base, int fmt, int64_t idx) {
-    if (fmt == OR_F16) return decode_f16(((const uint16_t*)base)[idx]);
+    if (fmt == OR_F32) return decode_f32(((const uint32_t*)base)[idx]);
     if (fmt == OR_BF16) return decode_bf16(((const uint16_t*)base)[idx]);
-    return decode_f32(((const uint32_t*)base)[idx]);
+    if (fmt == OR_E4M3) return decode_e4m3(((const uint8_t*)base)[idx]);
+    if (fmt == OR_E5M2) return decode_e5m2(((const uint8_t*)base)[idx]);
+    return decode_f16(((const uint16_t*)base)[idx]);
 }
 
 /* ----------------------------------------------- rounding (nearest, ties even) */

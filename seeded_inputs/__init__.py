@@ -35,6 +35,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 F16, BF16, F32 = "f16", "bf16", "f32"
+E4M3, E5M2 = "e4m3", "e5m2"
 
 
 _CHUNK = 1 << 22
@@ -131,12 +132,50 @@ def f32_to_bf16_bits(v: np.ndarray) -> np.ndarray:
     return r
 
 
+def _fp8_positive_values(exp_bits: int, man_bits: int) -> np.ndarray:
+    """Values of the 128 non-negative codes of an OCP FP8 format (NaN where the
+    code is not a finite number): E4M3 (4, 3) has no infinities and S.1111.111 as
+    NaN; E5M2 (5, 2) has IEEE-style infinities and NaNs."""
+    bias = (1 << (exp_bits - 1)) - 1
+    vals = np.empty(128, dtype=np.float64)
+    for code in range(128):
+        e, m = code >> man_bits, code & ((1 << man_bits) - 1)
+        if e == 0:
+            vals[code] = m / (1 << man_bits) * 2.0 ** (1 - bias)
+        elif e == (1 << exp_bits) - 1 and (exp_bits == 5 or m == (1 << man_bits) - 1):
+            vals[code] = np.nan
+        else:
+            vals[code] = (1 + m / (1 << man_bits)) * 2.0 ** (e - bias)
+    return vals
+
+
+def f32_to_fp8_bits(v: np.ndarray, dtype: str) -> np.ndarray:
+    """binary32 -> E4M3 / E5M2 (round to nearest, ties to the even code), uint8
+    bit patterns.  Inputs must be finite and within the format's range."""
+    pos = _fp8_positive_values(4, 3) if dtype == E4M3 else _fp8_positive_values(5, 2)
+    finite = np.flatnonzero(np.isfinite(pos))     # codes in increasing value order
+    table = pos[finite]
+    x = np.asarray(v, dtype=np.float64)
+    a = np.abs(x)
+    if np.any(~np.isfinite(a)) or np.any(a > table[-1]):
+        raise ValueError("value outside the FP8 format's finite range")
+    hi = np.clip(np.searchsorted(table, a, side="left"), 0, table.size - 1)
+    lo = np.clip(hi - 1, 0, table.size - 1)
+    dlo, dhi = a - table[lo], table[hi] - a
+    code_lo, code_hi = finite[lo], finite[hi]
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (code_hi % 2 == 0) & (code_lo % 2 == 1))
+    code = np.where(pick_hi, code_hi, code_lo).astype(np.uint8)
+    return np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
+
+
 def to_bits(v: np.ndarray, dtype: str) -> np.ndarray:
     """Round binary32 values to the stored input format; returns the bit patterns."""
     if dtype == F16:
         return f32_to_f16_bits(v)
     if dtype == BF16:
         return f32_to_bf16_bits(v)
+    if dtype in (E4M3, E5M2):
+        return f32_to_fp8_bits(v, dtype)
     if dtype == F32:
         return np.ascontiguousarray(v, dtype=np.float32).view(np.uint32)
     raise ValueError(dtype)
