@@ -384,6 +384,7 @@ def run_ours(args, rank, world, device):
         if not args.no_suite:
             out["suite"] = run_suite(g, args, device, peaks, cfg)
             out["odd_tail"] = run_odd_tail(g, device, peaks)
+            out["fp8"] = run_fp8(g, device, peaks)
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(w)
         out["kernel_hash"] = kernel_source_hash()
@@ -499,6 +500,60 @@ def run_odd_tail(g, device, peaks):
                      "gbs_algorithmic": byts / (ms * 1e-3) / 1e9,
                      "frac_hbm": byts / (ms * 1e-3) / 1e9 / hbm,
                      "cublas_ms": cub}
+    return res
+
+
+# FP8 operands (tcgen05.mma kind::f8f6f4, fp32 accumulation), K-major A and B.
+# The roofline peak is the measured bf16 dense rate times 2, the nominal FP8/BF16
+# ratio of the part (4.5 / 2.25 PFLOP/s); cuBLASLt's FP8 GEMM (torch._scaled_mm
+# with unit scales) is timed beside it.
+FP8_SHAPES = [
+    ("fp8_2048_e4m3_f32", 2048, 2048, 2048, "e4m3", "f32"),
+    ("fp8_4096_e4m3_bf16", 4096, 4096, 4096, "e4m3", "bf16"),
+    ("fp8_8192_e4m3_f32", 8192, 8192, 8192, "e4m3", "f32"),
+    ("fp8_8192_e5m2_bf16", 8192, 8192, 8192, "e5m2", "bf16"),
+]
+
+
+def run_fp8(g, device, peaks):
+    import torch
+    tdt = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2, "f32": torch.float32,
+           "bf16": torch.bfloat16}
+    flush = L2Flush(device)
+    peak8 = 2.0 * peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    gen = torch.Generator(device=device)
+    res = {}
+    for i, (name, M, N, K, din, dout) in enumerate(FP8_SHAPES):
+        gen.manual_seed(6000 + i)
+        a = torch.randn(M, K, device=device, generator=gen).to(tdt[din])
+        b = torch.randn(N, K, device=device, generator=gen).to(tdt[din])   # B column-major
+        c = torch.empty(M, N, device=device, dtype=tdt[dout])
+        w = {"alpha": 1.0, "beta": 0.0, "a_col": False, "b_col": True}
+        steps = 10 if M >= 8192 else 20
+        times = time_gemm(g, w, a, b, c, None, steps, 5, torch.cuda.current_stream(device), flush)
+        ms = statistics.median(times)
+        tf = 2 * M * N * K / (ms * 1e-3) / 1e12
+        entry = {"M": M, "N": N, "K": K, "in": din, "out": dout, "median_ms": ms, "tflops": tf,
+                 "peak_tflops": peak8, "frac": tf / peak8}
+        try:
+            one = torch.ones((), device=device)
+            odt = torch.float32 if dout == "f32" else torch.bfloat16
+            ctimes = []
+            for _ in range(steps + 5):
+                flush()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=odt)
+                e1.record()
+                torch.cuda.synchronize()
+                ctimes.append(e0.elapsed_time(e1))
+            entry["cublaslt_ms"] = statistics.median(ctimes[5:])
+        except (RuntimeError, TypeError) as e:   # an FP8 format the library rejects
+            entry["cublaslt_ms"] = None
+            entry["cublaslt_note"] = str(e).splitlines()[0][:120]
+        res[name] = entry
+        del a, b, c
+        torch.cuda.empty_cache()
     return res
 
 

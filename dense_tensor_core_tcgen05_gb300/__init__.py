@@ -11,6 +11,7 @@ import importlib
 _BINDING_NAMES = frozenset((
     "EXPORTS", "GEMM_A_COL", "GEMM_A_ROW", "GEMM_ACT_NONE", "GEMM_ACT_RELU", "GEMM_B_COL",
     "GEMM_B_ROW", "GEMM_BF16", "GEMM_BIAS_COL", "GEMM_BIAS_NONE", "GEMM_BIAS_ROW",
+    "GEMM_E4M3", "GEMM_E5M2",
     "GEMM_ERR_ARCH", "GEMM_ERR_CUDA", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_SCRATCH",
     "GEMM_ERR_TIMEOUT", "GEMM_ERR_UNSUPPORTED", "GEMM_F16", "GEMM_F32",
     "GEMM_NOALLOC_SCRATCH_BYTES", "GEMM_OK", "GEMM_ORDER_AUTO", "GEMM_ORDER_GROUPED",

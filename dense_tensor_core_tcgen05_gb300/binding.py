@@ -13,7 +13,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgemm_tcgen05.so")
 
-GEMM_F16, GEMM_BF16, GEMM_F32 = 0, 1, 2
+GEMM_F16, GEMM_BF16, GEMM_F32, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3, 4
 GEMM_A_ROW, GEMM_A_COL, GEMM_B_ROW, GEMM_B_COL = 0, 1, 0, 2
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ARCH, GEMM_ERR_CUDA, \
     GEMM_ERR_TIMEOUT, GEMM_ERR_SCRATCH = range(7)
@@ -215,6 +215,10 @@ def _torch_dtype_code(dt):
         return GEMM_BF16
     if dt == torch.float32:
         return GEMM_F32
+    if dt == getattr(torch, "float8_e4m3fn", None):
+        return GEMM_E4M3
+    if dt == getattr(torch, "float8_e5m2", None):
+        return GEMM_E5M2
     raise TypeError(f"unsupported dtype {dt}")
 
 

@@ -214,6 +214,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 int out_size(int out_dtype) { return out_dtype == GEMM_F32 ? 4 : 2; }
 
+bool is_fp8(int in_dtype) { return in_dtype == GEMM_E4M3 || in_dtype == GEMM_E5M2; }
+
+// Bytes per input element, and K elements per k-block (one 128-byte swizzled row).
+int in_size(int in_dtype) { return is_fp8(in_dtype) ? 1 : 2; }
+int kblock_elems(int in_dtype) { return is_fp8(in_dtype) ? 2 * BK : BK; }
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Checks on sizes, formats and layout only (no pointers): shared by gemm() and
@@ -223,7 +229,10 @@ gemm_status_t check_shape(int64_t M, int64_t N, int64_t K, int in_dtype, int out
   *quick = false;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   if (layout & ~(GEMM_A_COL | GEMM_B_COL)) return GEMM_ERR_INVALID_ARG;
-  if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16) return GEMM_ERR_UNSUPPORTED;
+  if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16 && !is_fp8(in_dtype))
+    return GEMM_ERR_UNSUPPORTED;
+  // 8-bit operands: K-major only (A row-major, B column-major)
+  if (is_fp8(in_dtype) && layout != (GEMM_A_ROW | GEMM_B_COL)) return GEMM_ERR_UNSUPPORTED;
   if (out_dtype != GEMM_F32 && out_dtype != GEMM_BF16 && out_dtype != GEMM_F16)
     return GEMM_ERR_UNSUPPORTED;
   // tile indices and TMA coordinates are 32-bit signed on the device
@@ -253,9 +262,10 @@ gemm_status_t check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t
     if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
     if (lda > (int64_t(1) << 36) || ldb > (int64_t(1) << 36)) return GEMM_ERR_INVALID_ARG;
     const int64_t a_rows = a_col ? K : M, b_rows = b_col ? N : K;
-    if (a_rows > (int64_t(1) << 62) / (lda * 2 + 1) || b_rows > (int64_t(1) << 62) / (ldb * 2 + 1))
+    const int isz = in_size(in_dtype);
+    if (a_rows > (int64_t(1) << 62) / (lda * isz + 1) || b_rows > (int64_t(1) << 62) / (ldb * isz + 1))
       return GEMM_ERR_INVALID_ARG;
-    if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0)
+    if (!aligned16(A) || !aligned16(B) || (lda * isz) % 16 != 0 || (ldb * isz) % 16 != 0)
       return GEMM_ERR_UNSUPPORTED;
   }
   return GEMM_OK;
@@ -301,9 +311,9 @@ void choose_unit(int64_t M, int64_t N, int num_sms, int* bn_out, bool* pair_out)
 // 128-wide tiles come first: their 3-stage ring hid HBM latency best on the
 // 128 x 8192 x 8192 stream (36.9 us vs 45 us for 256-wide tiles split 4).
 // Returns 1 (no split) otherwise.
-int choose_split(int64_t M, int64_t N, int64_t K, int num_sms, int* bn_out) {
+int choose_split(int64_t M, int64_t N, int64_t K, int kbe, int num_sms, int* bn_out) {
   if (M > BM) return 1;
-  const int64_t kb = ceil_div(K, BK);
+  const int64_t kb = ceil_div(K, kbe);
   // The most CTAs that fit one wave, each with at least 8 k-blocks; on a tie the
   // fewer splits (less partial-sum exchange), then the wider tile.  Listed in
   // that order of preference.
@@ -325,8 +335,9 @@ int choose_split(int64_t M, int64_t N, int64_t K, int num_sms, int* bn_out) {
   return cands[best].s;
 }
 
-gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layout, int num_sms,
-                        const gemm_config_t* cfg, gemm_plan_t* p) {
+gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int layout,
+                        int num_sms, const gemm_config_t* cfg, gemm_plan_t* p) {
+  const int kbe = kblock_elems(in_dtype);
   if (num_sms <= 0) return GEMM_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
   if (cfg && cfg->reserved) return GEMM_ERR_INVALID_ARG;
@@ -335,7 +346,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
   int bn = 0;
   bool pair = false;
   choose_unit(M, N, num_sms, &bn, &pair);
-  int split = choose_split(M, N, K, num_sms, &bn);
+  int split = choose_split(M, N, K, kbe, num_sms, &bn);
   if (split > 1) pair = false;
   // a manual tile setting without an explicit split_k turns the automatic split off
   if (cfg && (cfg->cta_group || cfg->bn) && !cfg->split_k) split = 1;
@@ -353,14 +364,14 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int out_dtype, int layo
   if (cfg && cfg->bn) bn = cfg->bn;
   if (pair ? (bn != 128 && bn != 256) : (bn != 64 && bn != 128 && bn != 256))
     return GEMM_ERR_INVALID_ARG;
-  if (split > 1 && (pair || !split_supported(bn, split) || ceil_div(K, BK) < split))
+  if (split > 1 && (pair || !split_supported(bn, split) || ceil_div(K, kbe) < split))
     return GEMM_ERR_INVALID_ARG;
   const int rows = pair ? 2 * BM : BM;
   p->bm = rows;
   p->bn = bn;
-  p->bk = BK * ko_for(bn, pair);   // K per ring stage
+  p->bk = kbe * ko_for(bn, pair);   // K elements per ring stage
   p->stages = stages_for(bn, pair);
-  const int64_t mt = ceil_div(M, rows), nt = ceil_div(N, bn), kb = ceil_div(K, BK);
+  const int64_t mt = ceil_div(M, rows), nt = ceil_div(N, bn), kb = ceil_div(K, kbe);
   if (mt * nt >= (int64_t(1) << 30)) return GEMM_ERR_UNSUPPORTED;
   p->m_tiles = static_cast<int32_t>(mt);
   p->n_tiles = static_cast<int32_t>(nt);
@@ -450,13 +461,15 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
 // blocks 128 B apart along the row, so one box {64, box1, box2} covers box2
 // consecutive blocks of each of its rows.  Only whole blocks are mapped: the
 // kernel uses it for copies that stay inside them and the 2-D map otherwise.
+// 3-D map (block, d1, d2): `inner` elements make the 128-byte block (64 16-bit or
+// 128 8-bit elements), whole blocks 128 B apart along d2.
 bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d1, uint64_t d2,
-               uint64_t row_bytes, uint32_t box1, uint32_t box2) {
+               uint64_t row_bytes, uint32_t box1, uint32_t box2, uint32_t inner = 64) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
-  cuuint64_t dims[3] = {64, d1, d2};
+  cuuint64_t dims[3] = {inner, d1, d2};
   cuuint64_t strides[2] = {row_bytes, 128};
-  cuuint32_t box[3] = {64, box1, box2};
+  cuuint32_t box[3] = {inner, box1, box2};
   cuuint32_t elem_strides[3] = {1, 1, 1};
   CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, elem_strides,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -468,6 +481,8 @@ CUtensorMapDataType tma_dtype(int dt) {
   switch (dt) {
     case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    case GEMM_E4M3:
+    case GEMM_E5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // raw bytes; the MMA knows the format
     default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   }
 }
@@ -519,7 +534,7 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   }
 
   gemm_plan_t p;
-  s = make_plan(M, N, K, out_dtype, layout, di->num_sms, cfg, &p);
+  s = make_plan(M, N, K, in_dtype, out_dtype, layout, di->num_sms, cfg, &p);
   if (s != GEMM_OK) return s;
 
   OperandMaps mp;
@@ -535,26 +550,27 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   // swizzle atom is only partly inside the tensor.
   const int a_box_rows = (!pair && !a_col && p.m_tiles == 1 && M < BM)
                              ? static_cast<int>((M + 7) / 8 * 8) : BM;
-  bool ok = a_col ? encode_2d(&mp.a, din, A, M, K, lda * 2, ATOM_MN, BK)
-                  : encode_2d(&mp.a, din, A, K, M, lda * 2, BK, a_box_rows);
-  ok = ok && (b_col ? encode_2d(&mp.b, din, B, K, N, ldb * 2, BK, b_cols)
-                    : encode_2d(&mp.b, din, B, N, K, ldb * 2, ATOM_MN, BK));
+  const int isz = in_size(in_dtype), kbe = kblock_elems(in_dtype);   // MN-major: 16-bit only
+  bool ok = a_col ? encode_2d(&mp.a, din, A, M, K, lda * isz, ATOM_MN, BK)
+                  : encode_2d(&mp.a, din, A, K, M, lda * isz, kbe, a_box_rows);
+  ok = ok && (b_col ? encode_2d(&mp.b, din, B, K, N, ldb * isz, kbe, b_cols)
+                    : encode_2d(&mp.b, din, B, N, K, ldb * isz, ATOM_MN, BK));
   ok = ok && encode_2d(&mp.c, tma_dtype(out_dtype), C, N, M, ldc * out_size(out_dtype),
                        p.epi_chunk_cols, EPI_ROWS);
   if (!ok) return GEMM_ERR_CUDA;
   // 3-D maps over whole 64-element blocks: K-major (A row-major, B column-major)
   // -> blocks along K; MN-major (A column-major, B row-major) -> 64-wide atoms.
-  const int64_t a_full = a_col ? M / ATOM_MN : K / BK;
-  const int64_t b_full = b_col ? K / BK : N / ATOM_MN;
+  const int64_t a_full = a_col ? M / ATOM_MN : K / kbe;
+  const int64_t b_full = b_col ? K / kbe : N / ATOM_MN;
   int a_full3d = 0, b_full3d = 0;
   if (a_full > 0 && a_box_rows == BM &&
-      (a_col ? encode_3d(&mp.a3, din, A, K, a_full, lda * 2, ko * BK, BM / ATOM_MN)
-                           : encode_3d(&mp.a3, din, A, M, a_full, lda * 2, BM, ko)))
+      (a_col ? encode_3d(&mp.a3, din, A, K, a_full, lda * isz, ko * BK, BM / ATOM_MN)
+             : encode_3d(&mp.a3, din, A, M, a_full, lda * isz, BM, ko, kbe)))
     a_full3d = static_cast<int>(a_full);
   else
     mp.a3 = mp.a;
-  if (b_full > 0 && (b_col ? encode_3d(&mp.b3, din, B, N, b_full, ldb * 2, b_cols, ko)
-                           : encode_3d(&mp.b3, din, B, K, b_full, ldb * 2, ko * BK, b_cols / ATOM_MN)))
+  if (b_full > 0 && (b_col ? encode_3d(&mp.b3, din, B, N, b_full, ldb * isz, b_cols, ko, kbe)
+                           : encode_3d(&mp.b3, din, B, K, b_full, ldb * isz, ko * BK, b_cols / ATOM_MN)))
     b_full3d = static_cast<int>(b_full);
   else
     mp.b3 = mp.b;
@@ -571,7 +587,10 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.group_m = p.group_m;
   ka.alpha = alpha;
   ka.beta = beta;
-  ka.idesc = make_idesc_f16(in_dtype == GEMM_BF16 ? 1 : 0, p.a_mn, p.b_mn, p.bm, p.bn);
+  // format code 1: bf16 (kind::f16) or E5M2 (kind::f8f6f4); 0: f16 or E4M3
+  ka.idesc = make_idesc_f16((in_dtype == GEMM_BF16 || in_dtype == GEMM_E5M2) ? 1 : 0, p.a_mn,
+                            p.b_mn, p.bm, p.bn);
+  ka.kblock_elems = kblock_elems(in_dtype);
   ka.a_mn = p.a_mn;
   ka.b_mn = p.b_mn;
   ka.read_c = beta != 0.0f ? 1 : 0;
@@ -611,9 +630,18 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
 
   cudaError_t e;
   switch (out_dtype) {
-    case GEMM_F32: e = launch_gemm_f32(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev); break;
-    case GEMM_BF16: e = launch_gemm_bf16(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev); break;
-    default: e = launch_gemm_f16(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev); break;
+    case GEMM_F32:
+      e = is_fp8(in_dtype) ? launch_gemm_f8_f32(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev)
+                           : launch_gemm_f32(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev);
+      break;
+    case GEMM_BF16:
+      e = is_fp8(in_dtype) ? launch_gemm_f8_bf16(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev)
+                           : launch_gemm_bf16(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev);
+      break;
+    default:
+      e = is_fp8(in_dtype) ? launch_gemm_f8_f16(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev)
+                           : launch_gemm_f16(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev);
+      break;
   }
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -689,10 +717,11 @@ gemm_status_t gemm_host(int64_t M, int64_t N, int64_t K, float alpha, const void
   if (K > 0) {
     const int64_t a_rows = a_col ? K : M, a_cols = a_col ? M : K;
     const int64_t b_rows = b_col ? N : K, b_cols = b_col ? K : N;
-    if (cudaMemcpy2DAsync(dA, lda * 2, hA, lda * 2, a_cols * 2, a_rows, cudaMemcpyHostToDevice,
-                          st) != cudaSuccess ||
-        cudaMemcpy2DAsync(dB, ldb * 2, hB, ldb * 2, b_cols * 2, b_rows, cudaMemcpyHostToDevice,
-                          st) != cudaSuccess)
+    const int64_t isz = in_size(in_dtype);
+    if (cudaMemcpy2DAsync(dA, lda * isz, hA, lda * isz, a_cols * isz, a_rows,
+                          cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpy2DAsync(dB, ldb * isz, hB, ldb * isz, b_cols * isz, b_rows,
+                          cudaMemcpyHostToDevice, st) != cudaSuccess)
       return GEMM_ERR_CUDA;
   }
   if (beta != 0.0f &&
@@ -745,7 +774,7 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   bool quick = false;
   gemm_status_t s = check_shape(M, N, K, in_dtype, out_dtype, layout, &quick);
   if (s != GEMM_OK) return s;
-  return make_plan(M, N, K, out_dtype, layout, num_sms, cfg, plan);
+  return make_plan(M, N, K, in_dtype, out_dtype, layout, num_sms, cfg, plan);
 }
 
 void gemm_tile_coord(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_m, int32_t* m_blk,

@@ -66,8 +66,10 @@ GEMM_HD void hilbert_cell(int k, long long d, int* x, int* y) {
 
 // -------------------------------------------------------- tcgen05 descriptors
 //
-// Instruction descriptor of tcgen05.mma kind::f16 (32 bits, public PTX ISA):
-//   [4,6) D format (1 = f32)   [7,10) A format   [10,13) B format (0 = f16, 1 = bf16)
+// Instruction descriptor of tcgen05.mma kind::f16 and kind::f8f6f4 (32 bits, public
+// PTX ISA; the same layout for both kinds):
+//   [4,6) D format (1 = f32)   [7,10) A format   [10,13) B format (kind::f16: 0 = f16,
+//   1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2; in_is_bf16 carries that code)
 //   [15] A major   [16] B major (0 = K-major, 1 = MN-major)
 //   [17,23) N >> 3   [24,29) M >> 4     (everything else 0: dense, no negate)
 GEMM_HD uint32_t make_idesc_f16(int in_is_bf16, int a_mn, int b_mn, int m, int n) {
@@ -189,6 +191,9 @@ struct KernelArgs {
   int bias_kind;         // EPI_BIAS_*
   int act;               // EPI_ACT_*
   int epi;               // 1 when bias_kind or act is set (selects the fused epilogue)
+  // K elements of one k-block (64 for 16-bit operands, 128 for 8-bit ones: one
+  // 128-byte swizzled row either way).
+  int kblock_elems;
   // Rows of A each k-block copy brings (BM, or fewer for a single row of tiles
   // with M < BM: the rows of smem beyond them only feed accumulator rows >= M,
   // which are never stored).

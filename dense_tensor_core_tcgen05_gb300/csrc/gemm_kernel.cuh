@@ -459,7 +459,9 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 // SPLIT CTAs shares one 128-row tile, each accumulating 1/SPLIT of the K range;
 // the partial sums meet in distributed shared memory (split-K without a global
 // workspace; one tile per cluster).
-template <int BN, int STAGES, int OUT, bool PAIR, int SPLIT, int KO>
+// F8: 8-bit operands (tcgen05.mma kind::f8f6f4) instead of 16-bit ones; a
+// compile-time choice, as a branch between MMA kinds in the issue loop slows it.
+template <int BN, int STAGES, int OUT, bool PAIR, int SPLIT, int KO, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -627,7 +629,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (nkb == KO && kb0 + KO <= full3d) {
                 load3(dst, m3, row0, kb0, hint, pol);
               } else {
-                for (int j = 0; j < nkb; ++j) load2(dst + j * rows * SW, m2, (kb0 + j) * BK, row0, hint, pol);
+                for (int j = 0; j < nkb; ++j)
+                  load2(dst + j * rows * SW, m2, (kb0 + j) * args.kblock_elems, row0, hint, pol);
               }
             } else {
               const int atoms = rows / ATOM_MN;
@@ -693,14 +696,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const uint64_t da0 = make_sdesc_sw128(sa + j * a_kb, a_lbo, 8 * SW);
               const uint64_t db0 = make_sdesc_sw128(sb + j * b_kb, b_lbo, 8 * SW);
 #pragma unroll
-              for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              for (int kk = 0; kk < BK / UMMA_K; ++kk) {   // 4 x 32 bytes of each row
                 const uint64_t da = da0 + static_cast<uint64_t>(kk) * a_step;
                 const uint64_t db = db0 + static_cast<uint64_t>(kk) * b_step;
                 const uint32_t acc = (kb0 != kb_begin || j != 0 || kk != 0) ? 1u : 0u;
-                if (PAIR)
-                  umma_f16_pair(d_tmem, da, db, args.idesc, acc);
-                else
-                  umma_f16(d_tmem, da, db, args.idesc, acc);
+                if (F8) {
+                  if (PAIR)
+                    umma_f8_pair(d_tmem, da, db, args.idesc, acc);
+                  else
+                    umma_f8(d_tmem, da, db, args.idesc, acc);
+                } else {
+                  if (PAIR)
+                    umma_f16_pair(d_tmem, da, db, args.idesc, acc);
+                  else
+                    umma_f16(d_tmem, da, db, args.idesc, acc);
+                }
               }
             }
           }

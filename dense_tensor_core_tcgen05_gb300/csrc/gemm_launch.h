@@ -43,6 +43,12 @@ cudaError_t launch_gemm_bf16(int bn, bool pair, int split, const OperandMaps& m,
                              const KernelArgs& args, int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_f16(int bn, bool pair, int split, const OperandMaps& m,
                             const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_f8_f32(int bn, bool pair, int split, const OperandMaps& m,
+                            const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_f8_bf16(int bn, bool pair, int split, const OperandMaps& m,
+                             const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_f8_f16(int bn, bool pair, int split, const OperandMaps& m,
+                            const KernelArgs& args, int grid, cudaStream_t stream, int dev);
 
 // Split-K cluster shapes that have kernel instances: (bn, split).
 constexpr bool split_supported(int bn, int split) {

@@ -1,5 +1,8 @@
 // Body of one launcher translation unit; GEMM_OUT_KIND and GEMM_LAUNCH_NAME are
-// defined by the including file.
+// defined by the including file, and GEMM_F8 (8-bit operands) when it is set.
+#ifndef GEMM_F8
+#define GEMM_F8 false
+#endif
 #include "gemm_kernel.cuh"
 #include "gemm_launch.h"
 
@@ -14,7 +17,7 @@ cudaError_t launch_inst(const OperandMaps& m, const KernelArgs& args, int grid,
   constexpr int ST = stages_for(BN, PAIR);
   constexpr int KO = ko_for(BN, PAIR);
   using L = SmemLayout<BN, ST, PAIR, KO>;
-  auto kern = gemm_tcgen05_kernel<BN, ST, GEMM_OUT_KIND, PAIR, SPLIT, KO>;
+  auto kern = gemm_tcgen05_kernel<BN, ST, GEMM_OUT_KIND, PAIR, SPLIT, KO, GEMM_F8>;
   static volatile bool attr_set[kMaxDevices] = {};
   static volatile int max_clusters[kMaxDevices] = {};
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;

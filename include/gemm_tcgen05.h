@@ -38,7 +38,16 @@ extern "C" {
 typedef enum {
   GEMM_F16 = 0,  /* IEEE binary16 */
   GEMM_BF16 = 1, /* bfloat16 (8-bit exponent, 7-bit mantissa) */
-  GEMM_F32 = 2   /* IEEE binary32 (output only) */
+  GEMM_F32 = 2,  /* IEEE binary32 (output only) */
+  GEMM_E4M3 = 3, /* OCP FP8 E4M3 (4-bit exponent, bias 7, 3-bit mantissa, no
+                    infinities, max 448; input only) */
+  GEMM_E5M2 = 4  /* OCP FP8 E5M2 (5-bit exponent, bias 15, 2-bit mantissa; input
+                    only).  FP8 is the variant "A dense FP16 matrix-multiply kernel
+                    for NVIDIA Ada" lists as written but untested; here the tensor
+                    core multiplies it with tcgen05.mma kind::f8f6f4, fp32
+                    accumulation.  FP8 operands must be K-major: layout
+                    GEMM_A_ROW | GEMM_B_COL (other layouts: GEMM_ERR_UNSUPPORTED),
+                    and lda, ldb multiples of 16 elements. */
 } gemm_dtype_t;
 
 /* Storage order of A and B (bit mask, OR one A flag with one B flag).  C is
@@ -72,11 +81,11 @@ typedef enum {
 /*
  * gemm -- C <- alpha * A * B + beta * C on the current device.
  *
- * in_dtype  : GEMM_F16 or GEMM_BF16 (A and B share it).
+ * in_dtype  : GEMM_F16, GEMM_BF16, GEMM_E4M3 or GEMM_E5M2 (A and B share it).
  * out_dtype : GEMM_F32, GEMM_BF16 or GEMM_F16 (C in and C out share it).
  * layout    : GEMM_A_ROW|GEMM_A_COL combined with GEMM_B_ROW|GEMM_B_COL.
- * Requirements: A, B, C 16-byte aligned; lda*2, ldb*2 and ldc*sizeof(out)
- * multiples of 16 bytes.  Any M, N, K >= 0 (ragged edges are handled by the
+ * Requirements: A, B, C 16-byte aligned; lda*sizeof(in), ldb*sizeof(in) and
+ * ldc*sizeof(out) multiples of 16 bytes.  Any M, N, K >= 0 (ragged edges are handled by the
  * copy engine's zero fill on loads and clipping on stores).
  * Quick returns: M == 0 or N == 0 -> GEMM_OK, nothing touched.  K == 0 ->
  * C <- beta * C (C is not read when beta == 0), A and B not read.

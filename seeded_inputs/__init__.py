@@ -204,7 +204,8 @@ def matrix(dist: str, seed: int, rows: int, cols: int, dtype: str,
     if ld == cols:
         return np.ascontiguousarray(bits)
     out = np.empty((rows, ld), dtype=bits.dtype)
-    out[:] = bits.dtype.type(0x7E00 if bits.dtype == np.uint16 else 0x7FC00000)
+    guard = {np.dtype(np.uint8): 0x7F, np.dtype(np.uint16): 0x7E00, np.dtype(np.uint32): 0x7FC00000}
+    out[:] = bits.dtype.type(guard[bits.dtype])   # a NaN of the format
     out[:, :cols] = bits
     return out
 

@@ -6,8 +6,10 @@ import torch
 import oracle
 import seeded_inputs as si
 
-TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
-BITS_DT = {"f16": np.uint16, "bf16": np.uint16, "f32": np.uint32}
+TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+            "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+BITS_DT = {"f16": np.uint16, "bf16": np.uint16, "f32": np.uint32, "e4m3": np.uint8,
+           "e5m2": np.uint8}
 # Error bound |C_gpu - C_oracle| <= TOL * sum_k |a_ik||b_kj| + 1e-6 per output format.
 TOL = {"f32": 1e-3, "bf16": 8e-3, "f16": 8e-3}
 NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "f32": 0x7FC00000}
@@ -18,6 +20,8 @@ def to_device(bits: np.ndarray, fmt: str, device="cuda") -> torch.Tensor:
     b = np.ascontiguousarray(bits)
     if fmt == "f32":
         t = torch.from_numpy(b.view(np.int32).copy()).view(torch.float32)
+    elif fmt in ("e4m3", "e5m2"):
+        t = torch.from_numpy(b.view(np.uint8).copy()).view(TORCH_DT[fmt])
     else:
         t = torch.from_numpy(b.view(np.int16).copy()).view(TORCH_DT[fmt])
     return t.to(device)

@@ -395,3 +395,21 @@ def test_plan_reports_the_order(g):
     assert s == 0 and p.order == g.GEMM_ORDER_HILBERT
     s, p = g.gemm_plan(8192, 8192, 8192, 1, 2, 2, 152)
     assert s == 0 and p.order == g.GEMM_ORDER_GROUPED
+
+
+@pytest.mark.parametrize("layout,lda,ldb,expect", [
+    (2, 64, 64, 0), (0, 64, 64, 2), (1, 64, 64, 2), (3, 64, 64, 2),   # K-major (A row, B col) only
+    (2, 56, 64, 2), (2, 64, 72, 2),                                   # 16-byte pitch: 16 elements
+])
+def test_fp8_layout_and_pitch_rules(g, layout, lda, ldb, expect):
+    for fmt in (g.GEMM_E4M3, g.GEMM_E5M2):
+        s = g.gemm(64, 64, 48, 1.0, ALIGNED, lda, ALIGNED, ldb, 0.0, ALIGNED, 64, fmt, 2, layout, 0)
+        if expect == 0:
+            assert s in (g.GEMM_ERR_CUDA, g.GEMM_ERR_ARCH, g.GEMM_OK)
+        else:
+            assert s == expect
+
+
+def test_fp8_plan_uses_128_element_k_blocks(g):
+    s, p = g.gemm_plan(4096, 4096, 4096, g.GEMM_E4M3, 1, 2, 152)
+    assert s == 0 and p.k_blocks == 32 and p.bk == 256 and p.groups == 16
