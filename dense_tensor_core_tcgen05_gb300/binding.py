@@ -33,7 +33,7 @@ class gemm_config_t(ctypes.Structure):
     _fields_ = [("bn", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("cta_group", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("stream_k", ctypes.c_int32),
-                ("order", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("order", ctypes.c_int32), ("general", ctypes.c_int32)]
 
 
 class gemm_plan_t(ctypes.Structure):
@@ -41,7 +41,7 @@ class gemm_plan_t(ctypes.Structure):
         "bm", "bn", "bk", "stages", "m_tiles", "n_tiles", "k_blocks", "num_tiles",
         "grid", "group_m", "threads", "smem_bytes", "tmem_cols", "a_mn", "b_mn",
         "epi_chunk_cols", "cta_group", "split_k", "groups", "dp_tiles", "order",
-        "reserved")] + [
+        "specialised")] + [
         ("sk_iters", ctypes.c_int64), ("scratch_bytes", ctypes.c_int64)]
 
     def as_dict(self):
@@ -118,6 +118,7 @@ def _cfg(cfg):
     c.cta_group, c.split_k = int(cfg.get("cta_group", 0)), int(cfg.get("split_k", 0))
     c.stream_k = int(cfg.get("stream_k", 0))
     c.order = int(cfg.get("order", 0))
+    c.general = int(cfg.get("general", 0))
     return ctypes.byref(c)
 
 

@@ -340,7 +340,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   const int kbe = kblock_elems(in_dtype);
   if (num_sms <= 0) return GEMM_ERR_INVALID_ARG;
   std::memset(p, 0, sizeof(*p));
-  if (cfg && cfg->reserved) return GEMM_ERR_INVALID_ARG;
+  if (cfg && (cfg->general < 0 || cfg->general > 1)) return GEMM_ERR_INVALID_ARG;
   if (cfg && (cfg->order < GEMM_ORDER_AUTO || cfg->order > GEMM_ORDER_HILBERT))
     return GEMM_ERR_INVALID_ARG;
   int bn = 0;
@@ -440,6 +440,12 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   p->b_mn = (layout & GEMM_B_COL) ? 0 : 1;
   p->epi_chunk_cols = out_dtype == GEMM_F32 ? 32 : 64;
   p->cta_group = pair ? 2 : 1;
+  // the conditions of run_gemm's plain path that the plan itself fixes
+  p->specialised = (p->sk_iters == 0 && p->order == GEMM_ORDER_GROUPED && !(cfg && cfg->general) &&
+                    (N * out_size(out_dtype)) % 16 == 0 &&
+                    spec_supported(bn, pair, split, layout, is_fp8(in_dtype)))
+                       ? 1
+                       : 0;
   return GEMM_OK;
 }
 
@@ -628,7 +634,29 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
     if (s != GEMM_OK) return s;
   }
 
-  cudaError_t e;
+  // A call on the plain path takes the specialised instance of its
+  // configuration and layout when there is one (cfg->general = 1 forbids it).
+  const bool plain = !(cfg && cfg->general) && !ka.read_c && !ka.epi && !ka.n_ragged &&
+                     ka.sk_iters == 0 && ka.inject_skip == 0 && ka.tile_map == nullptr;
+  cudaError_t e = cudaErrorNotSupported;
+  if (plain) {
+    const bool f8 = is_fp8(in_dtype);
+    switch (out_dtype) {
+      case GEMM_F32:
+        e = f8 ? launch_gemm_f8_spec_f32(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev)
+               : launch_gemm_spec_f32(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev);
+        break;
+      case GEMM_BF16:
+        e = f8 ? launch_gemm_f8_spec_bf16(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev)
+               : launch_gemm_spec_bf16(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev);
+        break;
+      default:
+        e = f8 ? launch_gemm_f8_spec_f16(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev)
+               : launch_gemm_spec_f16(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev);
+        break;
+    }
+    if (e != cudaErrorNotSupported) return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  }
   switch (out_dtype) {
     case GEMM_F32:
       e = is_fp8(in_dtype) ? launch_gemm_f8_f32(p.bn, pair, p.split_k, mp, ka, p.grid, stream, dev)

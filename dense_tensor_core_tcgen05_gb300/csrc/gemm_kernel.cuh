@@ -449,10 +449,74 @@ __device__ __forceinline__ unsigned int flag_acquire(const unsigned int* f) {
 }
 
 
+// Specialised instances.  Most launches take the plain path: no C read, no
+// bias or activation, N * sizeof(out) a multiple of 16 bytes, data-parallel
+// tiles in grouped order, no fault injection; and each operand's major-ness is
+// fixed by the call's layout.  Folding those parameters into constants drops
+// the code of the other paths from the kernel, which roughly halves its
+// instruction-cache misses and shortens the one-off start-up and epilogue code
+// (2048^3: about 10% of the launch).  The host launches a specialised instance
+// only for a call that matches it; every other call takes the general kernel.
+enum : int {
+  SPEC_PLAIN = 1,          // plain epilogue and scheduling (see above)
+  SPEC_LAYOUT = 2,         // operand layout fixed: bits 2..3 hold GEMM_A_* | GEMM_B_*
+  SPEC_LAYOUT_SHIFT = 2,
+};
+constexpr int spec_bits(int layout) {   // the specialisation of a plain call with `layout`
+  return SPEC_PLAIN | SPEC_LAYOUT | (layout << SPEC_LAYOUT_SHIFT);
+}
+template <int SPEC, bool F8>
+__device__ __forceinline__ KernelArgs specialise_args(const KernelArgs& in) {
+  KernelArgs a = in;
+  if (SPEC & SPEC_PLAIN) {
+    a.read_c = 0;
+    a.epi = 0;
+    a.bias_kind = EPI_BIAS_NONE;
+    a.act = EPI_ACT_NONE;
+    a.n_ragged = 0;
+    a.sk_iters = 0;
+    a.inject_skip = 0;
+    a.tile_map = nullptr;
+  }
+  if (SPEC & SPEC_LAYOUT) {
+    constexpr int layout = SPEC >> SPEC_LAYOUT_SHIFT;
+    a.a_mn = (layout & 1) ? 1 : 0;   // A column-major: M-major
+    a.b_mn = (layout & 2) ? 0 : 1;   // B row-major: N-major
+    a.kblock_elems = F8 ? 128 : 64;
+  }
+  return a;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+// Stage one output chunk row (this thread's row r, registers v0 = columns 0..31,
+// v1 = 32..63) as alpha * acc cast to the output format, into the swizzled
+// staging row at shared address `row`: 16-byte piece j at (j ^ (r & 7)) * 16.
+template <int OUT>
+__device__ __forceinline__ void stage_chunk_scaled(const uint32_t* v0, const uint32_t* v1,
+                                                   uint32_t row, float alpha, int r) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint4 o;
+    if (OUT == OUT_F32) {
+      const uint32_t* s = v0 + 4 * j;
+      o = make_uint4(__float_as_uint(__uint_as_float(s[0]) * alpha),
+                     __float_as_uint(__uint_as_float(s[1]) * alpha),
+                     __float_as_uint(__uint_as_float(s[2]) * alpha),
+                     __float_as_uint(__uint_as_float(s[3]) * alpha));
+    } else {
+      const uint32_t* s = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+      o = make_uint4(pack2(__uint_as_float(s[0]) * alpha, __uint_as_float(s[1]) * alpha, OUT),
+                     pack2(__uint_as_float(s[2]) * alpha, __uint_as_float(s[3]) * alpha, OUT),
+                     pack2(__uint_as_float(s[4]) * alpha, __uint_as_float(s[5]) * alpha, OUT),
+                     pack2(__uint_as_float(s[6]) * alpha, __uint_as_float(s[7]) * alpha, OUT));
+    }
+    st_shared_v4(row + ((j ^ (r & 7)) << 4), o);
+  }
 }
 
 // PAIR: two CTAs per 256-row tile (cta_group::2).  SPLIT > 1: a cluster of
@@ -461,13 +525,16 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 // workspace; one tile per cluster).
 // F8: 8-bit operands (tcgen05.mma kind::f8f6f4) instead of 16-bit ones; a
 // compile-time choice, as a branch between MMA kinds in the issue loop slows it.
-template <int BN, int STAGES, int OUT, bool PAIR, int SPLIT, int KO, bool F8 = false>
+// SPEC: SPEC_* bits folding run-time parameters into constants (see
+// specialise_args); 0 for the general kernel.
+template <int BN, int STAGES, int OUT, bool PAIR, int SPLIT, int KO, bool F8 = false, int SPEC = 0>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmA3,
                         const __grid_constant__ CUtensorMap tmB3,
-                        const __grid_constant__ CUtensorMap tmC, const KernelArgs args) {
+                        const __grid_constant__ CUtensorMap tmC, const KernelArgs args_in) {
+  const KernelArgs args = specialise_args<SPEC, F8>(args_in);
   using L = SmemLayout<BN, STAGES, PAIR, KO>;
   constexpr int CHUNK = OutTraits<OUT>::CHUNK_COLS;
   constexpr int CHUNKS = BN / CHUNK;
@@ -531,27 +598,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   };
   uint32_t producer_iters = 0;  // ring iterations armed (producer thread only)
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+  // Start-up.  The lanes of warp 0 initialise the barriers (one each) and
+  // prefetch the tensor maps while warp 1 allocates TMEM.  The start-up barrier
+  // is split: warp 0 arrives, works out the producer's first work item and L2
+  // policies, and waits only where it must (pair mode: the odd CTA's copies
+  // signal the leader's barrier), so the first copies go out as soon as it opens.
+  if (warp == 0) {
+    for (int i = lane; i < L::NUM_BARS; i += 32) {
+      const uint64_t* b = bars + i;
+      const uint32_t count = (b == tempty || b == tempty + 1) ? (PAIR ? 2 * EPI_WARPS : EPI_WARPS)
+                             : b == esync                    ? EPI_WARPS
+                                                             : 1;
+      mbar_init(bars + i, count);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
-    }
-    for (int i = 0; i < EPI_WARPS * EPI_BUFS; ++i) mbar_init(&cload[i], 1);
-    mbar_init(drain, 1);
-    mbar_init(esync, EPI_WARPS);
-    for (int i = 0; i < EPI_WARPS * PSLOTS_MAX; ++i) mbar_init(&pfull[i], 1);
-    mbar_init(rfull, 1);
-    *abort_flag = 0;
+    if (lane == 0) *abort_flag = 0;
+    if (lane == 1) prefetch_tensormap(&tmA);
+    if (lane == 2) prefetch_tensormap(&tmB);
+    if (lane == 3 && args.a_full3d) prefetch_tensormap(&tmA3);
+    if (lane == 4 && args.b_full3d) prefetch_tensormap(&tmB3);
+    if (lane == 5) prefetch_tensormap(&tmC);
     fence_barrier_init();
-    prefetch_tensormap(&tmA);
-    prefetch_tensormap(&tmB);
-    if (args.a_full3d) prefetch_tensormap(&tmA3);
-    if (args.b_full3d) prefetch_tensormap(&tmB3);
-    prefetch_tensormap(&tmC);
+    __syncwarp();
   }
   if (warp == 1) {
     if (PAIR) {
@@ -562,28 +629,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tmem_relinquish();
     }
   }
+  __syncwarp();
   tc_fence_before();
-  if (PAIR)
-    cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
-  else
-    __syncthreads();
+  // both CTAs' barriers exist before any cross-CTA signal (pair mode); the
+  // barriers and the TMEM address are visible to every role
+  if (PAIR) {
+    cluster_arrive();
+    if (warp != 0) cluster_wait();
+  } else if (warp == 0) {
+    named_bar_arrive(1, NUM_THREADS);
+  } else {
+    named_bar_sync(1, NUM_THREADS);
+  }
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tmem_base = warp == 0 ? 0u : *tmem_slot;   // warp 0 never touches TMEM
 
   if (warp == 0) {
+    // L2 policies: 0 = default, 1 = evict first (streamed once), 2 = evict last (reused)
+    uint64_t pol_a = 0, pol_b = 0;
+    WorkIter wi;
+    WorkItem w;
+    bool have = false;
+    int mb = 0, nb = 0;
+    if (lane == 0) {
+      pol_a = args.a_hint == 1 ? policy_evict_first() : policy_evict_last();
+      pol_b = args.b_hint == 1 ? policy_evict_first() : policy_evict_last();
+      work_begin(wi);
+      have = wi.next(&w);
+      if (have) tile_of(args, w.tile, &mb, &nb);
+    }
+    if (PAIR) {
+      __syncwarp();
+      cluster_wait();
+    }
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer
       uint32_t it = 0;
       bool ok = true;
-      // L2 policies: 0 = default, 1 = evict first (streamed once), 2 = evict last (reused)
-      const uint64_t pol_a = args.a_hint == 1 ? policy_evict_first() : policy_evict_last();
-      const uint64_t pol_b = args.b_hint == 1 ? policy_evict_first() : policy_evict_last();
-      WorkIter wi;
-      WorkItem w;
-      work_begin(wi);
-      while (ok && wi.next(&w)) {
-        int mb, nb, kb_begin, kb_end;
-        tile_of(args, w.tile, &mb, &nb);
+      while (ok && have) {
+        int kb_begin, kb_end;
         kb_range(w, &kb_begin, &kb_end);
         const int a_row = mb * TILE_M + static_cast<int>(rank) * BM;
         const int b_col = nb * BN + static_cast<int>(rank) * L::B_COLS;
@@ -648,6 +732,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           load_operand(sb, &tmB, &tmB3, args.b_mn, L::B_COLS, b_col, args.b_full3d, args.b_hint,
                        pol_b);
         }
+        have = wi.next(&w);
+        if (have) tile_of(args, w.tile, &mb, &nb);
       }
       producer_iters = it;
     }
@@ -756,8 +842,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Write one finished tile: TMEM -> registers (+ the later units' partial
     // sums, in unit order, when ADD) -> alpha * acc + beta * C -> output.
     // Returns false if a wait gave up.
-    auto store_tile = [&](auto add_tag, auto fused_tag, uint32_t t_row, int nb, int row0, int buf,
-                          int contrib0, int ncontrib) -> bool {
+    auto store_tile = [&](auto add_tag, auto fused_tag, uint32_t t_row, int nb,
+                          int row0, int buf, int contrib0, int ncontrib) -> bool {
       constexpr bool ADD = decltype(add_tag)::value;
       constexpr bool FUSED = decltype(fused_tag)::value;   // bias / activation
       const uint32_t first = p_issued;
@@ -838,6 +924,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         uint8_t* rowp = stg + r * SW;
         if (FUSED) fused_chunk<OUT, CHUNK>(v0, v1, rowp, args, col0, row0 + r, r);
+        if (!FUSED && !ADD && !ragged && !args.read_c) {
+          // the common case, branch-free: alpha * acc, cast, one 16-byte
+          // shared store per piece (per-piece branches slowed the stores ~1.6x)
+          stage_chunk_scaled<OUT>(v0, v1, smem_u32(rowp), args.alpha, r);
+        } else
 #pragma unroll
         for (int j = 0; j < 8; ++j) {   // 16-byte pieces of the 128-byte row
           uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
@@ -981,13 +1072,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       const int ncontrib = contrib1 - contrib0;
       // one specialised chunk loop per case, chosen once per tile
+      const BoolC<false> no;
+      const BoolC<true> yes;
       if (ncontrib == 0)
-        ok = args.epi ? store_tile(BoolC<false>{}, BoolC<true>{}, t_row, nb, row0, buf, 0, 0)
-                      : store_tile(BoolC<false>{}, BoolC<false>{}, t_row, nb, row0, buf, 0, 0);
+        ok = args.epi ? store_tile(no, yes, t_row, nb, row0, buf, 0, 0)
+                      : store_tile(no, no, t_row, nb, row0, buf, 0, 0);
       else
-        ok = args.epi
-                 ? store_tile(BoolC<true>{}, BoolC<true>{}, t_row, nb, row0, buf, contrib0, ncontrib)
-                 : store_tile(BoolC<true>{}, BoolC<false>{}, t_row, nb, row0, buf, contrib0, ncontrib);
+        ok = args.epi ? store_tile(yes, yes, t_row, nb, row0, buf, contrib0, ncontrib)
+                      : store_tile(yes, no, t_row, nb, row0, buf, contrib0, ncontrib);
     }
     if (!SPLITK) {
       if (!ok && st.pending_cload >= 0 && lane == 0)

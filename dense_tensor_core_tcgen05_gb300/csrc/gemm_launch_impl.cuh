@@ -1,5 +1,7 @@
-// Body of one launcher translation unit; GEMM_OUT_KIND and GEMM_LAUNCH_NAME are
-// defined by the including file, and GEMM_F8 (8-bit operands) when it is set.
+// Body of one launcher translation unit.  The including file defines
+// GEMM_OUT_KIND; GEMM_LAUNCH_NAME (the general instances) unless GEMM_SPEC_ONLY
+// is set; GEMM_LAUNCH_SPEC_NAME for the specialised instances it holds; and
+// GEMM_F8 (8-bit operands) when it is set.
 #ifndef GEMM_F8
 #define GEMM_F8 false
 #endif
@@ -11,13 +13,13 @@ namespace gemm_tc {
 namespace {
 constexpr int kMaxDevices = 64;
 
-template <int BN, bool PAIR, int SPLIT>
+template <int BN, bool PAIR, int SPLIT, int SPEC = 0>
 cudaError_t launch_inst(const OperandMaps& m, const KernelArgs& args, int grid,
                         cudaStream_t stream, int dev) {
   constexpr int ST = stages_for(BN, PAIR);
   constexpr int KO = ko_for(BN, PAIR);
   using L = SmemLayout<BN, ST, PAIR, KO>;
-  auto kern = gemm_tcgen05_kernel<BN, ST, GEMM_OUT_KIND, PAIR, SPLIT, KO, GEMM_F8>;
+  auto kern = gemm_tcgen05_kernel<BN, ST, GEMM_OUT_KIND, PAIR, SPLIT, KO, GEMM_F8, SPEC>;
   static volatile bool attr_set[kMaxDevices] = {};
   static volatile int max_clusters[kMaxDevices] = {};
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
@@ -65,6 +67,40 @@ cudaError_t launch_inst(const OperandMaps& m, const KernelArgs& args, int grid,
 }
 }  // namespace
 
+#ifdef GEMM_LAUNCH_SPEC_NAME
+namespace {
+// The specialised instances of one layout: the configurations most plans use
+// (the 256-wide CTA pair of large GEMMs, the 2-way split-K clusters of small-M
+// ones, the single 64-wide CTA of small ones).
+template <int LAYOUT>
+cudaError_t launch_spec_layout(int bn, bool pair, int split, const OperandMaps& m,
+                               const KernelArgs& args, int grid, cudaStream_t stream, int dev) {
+  constexpr int S = spec_bits(LAYOUT);
+  if (pair) return launch_inst<256, true, 1, S>(m, args, grid, stream, dev);
+  if (split == 2 && bn == 128) return launch_inst<128, false, 2, S>(m, args, grid, stream, dev);
+  if (split == 2) return launch_inst<64, false, 2, S>(m, args, grid, stream, dev);
+  return launch_inst<64, false, 1, S>(m, args, grid, stream, dev);
+}
+}  // namespace
+
+cudaError_t GEMM_LAUNCH_SPEC_NAME(int bn, bool pair, int split, int layout, const OperandMaps& m,
+                                  const KernelArgs& args, int grid, cudaStream_t stream, int dev) {
+  if (!spec_supported(bn, pair, split, layout, GEMM_F8)) return cudaErrorNotSupported;
+  if constexpr (GEMM_F8) {   // 8-bit operands are K-major only
+    return launch_spec_layout<2>(bn, pair, split, m, args, grid, stream, dev);
+  } else {
+    switch (layout) {
+      case 0: return launch_spec_layout<0>(bn, pair, split, m, args, grid, stream, dev);
+      case 1: return launch_spec_layout<1>(bn, pair, split, m, args, grid, stream, dev);
+      case 2: return launch_spec_layout<2>(bn, pair, split, m, args, grid, stream, dev);
+      case 3: return launch_spec_layout<3>(bn, pair, split, m, args, grid, stream, dev);
+      default: return cudaErrorNotSupported;
+    }
+  }
+}
+#endif
+
+#ifndef GEMM_SPEC_ONLY
 cudaError_t GEMM_LAUNCH_NAME(int bn, bool pair, int split, const OperandMaps& m,
                              const KernelArgs& args, int grid, cudaStream_t stream, int dev) {
   if (split > 1) {
@@ -92,5 +128,6 @@ cudaError_t GEMM_LAUNCH_NAME(int bn, bool pair, int split, const OperandMaps& m,
     default: return cudaErrorInvalidValue;
   }
 }
+#endif
 
 }  // namespace gemm_tc

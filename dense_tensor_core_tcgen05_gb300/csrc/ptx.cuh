@@ -329,6 +329,23 @@ __device__ __forceinline__ void cluster_sync() {
                    "memory");
 }
 
+// The two halves of cluster_sync, for work in between (whole warps, converged).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Named CTA barrier `id` over `threads` threads (whole warps, converged): arrive
+// without waiting, or arrive and wait.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // shared::cluster address of the variable at the same offset in CTA `rank`.
 __device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
   uint32_t out;

@@ -129,7 +129,15 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *             grid) or the grid has more than 2^22 tiles the grouped order is
  *             used.  Its table (8 bytes per tile) is built on the host and kept
  *             on the device per grid shape by the library (gemm_ex_noalloc
- *             always uses the grouped order). */
+ *             always uses the grouped order).
+ *   general   1: always launch the general kernel.  0 (the default): a call on
+ *             the plain path -- beta == 0, no bias or activation, N times the
+ *             output element size a multiple of 16 bytes, no stream-K work,
+ *             the grouped tile order -- runs a kernel instance specialised
+ *             for its layout when the plan's configuration has one (the
+ *             256-wide CTA pair, the 2-way split-K clusters of width 128 and
+ *             64, the single 64-wide CTA); both compute the same result bit
+ *             for bit.  Other values: GEMM_ERR_INVALID_ARG. */
 enum { GEMM_ORDER_AUTO = 0, GEMM_ORDER_GROUPED = 1, GEMM_ORDER_HILBERT = 2 };
 
 typedef struct {
@@ -140,7 +148,7 @@ typedef struct {
   int32_t split_k;
   int32_t stream_k;
   int32_t order;
-  int32_t reserved;  /* must be zero */
+  int32_t general;
 } gemm_config_t;
 
 /* gemm with an explicit configuration (cfg may be NULL = gemm()).  Same
@@ -268,7 +276,9 @@ typedef struct {
   int32_t groups;      /* k-groups (ring stages) per tile */
   int32_t dp_tiles;    /* tiles of the data-parallel phase */
   int32_t order;       /* GEMM_ORDER_GROUPED or GEMM_ORDER_HILBERT */
-  int32_t reserved;
+  int32_t specialised; /* 1: a call under this plan with beta == 0 and no bias or
+                          activation runs a specialised instance (see
+                          gemm_config_t.general) */
   int64_t sk_iters;    /* stream-K iterations (tile k-groups) after it; 0 = none */
   int64_t scratch_bytes; /* stream-K scratch the launch uses (0 = none) */
 } gemm_plan_t;

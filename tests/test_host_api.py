@@ -183,10 +183,10 @@ def test_plan_split_k_overrides(g):
     assert s == 0 and (p.cta_group, p.split_k, p.bm) == (1, 2, 128)
     # fewer k-blocks than splits
     assert g.gemm_plan(128, 4096, 128, 1, 1, 2, 152, {"split_k": 4})[0] == g.GEMM_ERR_INVALID_ARG
-    # reserved fields must be zero
+    # general is 0 or 1
     import ctypes
     cfg = g.gemm_config_t()
-    cfg.reserved = 7
+    cfg.general = 7
     p = g.gemm_plan_t()
     lib = g.library()
     assert lib.gemm_plan(256, 256, 256, 1, 1, 0, 152, ctypes.byref(cfg), ctypes.byref(p)) == 1
@@ -413,3 +413,29 @@ def test_fp8_layout_and_pitch_rules(g, layout, lda, ldb, expect):
 def test_fp8_plan_uses_128_element_k_blocks(g):
     s, p = g.gemm_plan(4096, 4096, 4096, g.GEMM_E4M3, 1, 2, 152)
     assert s == 0 and p.k_blocks == 32 and p.bk == 256 and p.groups == 16
+
+
+def test_plan_specialised_flag():
+    """gemm_plan_t.specialised: 1 exactly when the plan's configuration has a
+    specialised instance for the layout and the plan keeps the plain path."""
+    import dense_tensor_core_tcgen05_gb300 as g
+    plan = lambda *a, **k: g.gemm_plan(*a, **k)[1].specialised
+    # 2048^3 fp16 -> fp32 row/row: the 256-wide CTA pair, every layout
+    for layout in range(4):
+        assert plan(2048, 2048, 2048, 0, 2, layout, 152) == 1
+        assert plan(2048, 2048, 2048, 0, 2, layout, 152, {"general": 1}) == 0
+    # stream-K work (4096^3 plans a stream-K tail) is not on the plain path
+    s, p = g.gemm_plan(4096, 4096, 4096, 1, 1, 0, 152)
+    assert s == 0 and p.sk_iters > 0 and p.specialised == 0
+    # skinny and decode shapes: 2-way split-K clusters
+    assert plan(128, 8192, 8192, 1, 1, 2, 152) == 1
+    # N * sizeof(out) not a multiple of 16 bytes: ragged right edge
+    assert plan(256, 203, 256, 1, 2, 0, 152, {"cta_group": 2}) == 0
+    # the Hilbert order reads a tile table
+    assert plan(2048, 2048, 2048, 1, 1, 0, 152, {"order": 2}) == 0
+    # configurations without specialised instances
+    assert plan(2048, 2048, 2048, 1, 1, 0, 152, {"cta_group": 1, "bn": 256}) == 0
+    assert plan(128, 8192, 8192, 1, 1, 2, 152, {"split_k": 4, "bn": 128}) == 0
+    assert plan(512, 512, 512, 0, 2, 0, 152) == 1   # the single 64-wide CTA
+    # 8-bit operands: A row-major with B column-major only
+    assert plan(2048, 2048, 2048, 3, 2, 2, 152) == 1
