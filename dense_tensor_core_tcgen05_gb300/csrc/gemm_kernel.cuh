@@ -552,6 +552,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int SLICE_BYTES = BM * SLICE * 4;
   static_assert(!SPLITK || 2 * (SPLIT - 1) * SLICE_BYTES <= STAGES * L::STAGE_BYTES,
                 "the split-K slices must fit in the ring's shared memory");
+  // Two-CTA split-K whose peer slice fits the epilogue staging area (unused by a
+  // split-K CTA until its final chunks): each epilogue warp pushes its rows of
+  // the peer's slice into that area as soon as they are staged, with no cluster
+  // barrier in between; the final chunks then stage in the idle ring, after
+  // the send area.  Wider slices and more peers meet in the ring after a
+  // cluster barrier instead.
+  constexpr bool EARLY = SPLIT == 2 && SLICE_BYTES <= L::off_bar - L::off_epi;
+  static_assert(!EARLY || SLICE_BYTES + EPI_WARPS * EPI_BUFS * L::EPI_BUF_BYTES <= L::RING_BYTES,
+                "final-chunk staging must fit in the ring after the send area");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -619,6 +628,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 5) prefetch_tensormap(&tmC);
     fence_barrier_init();
     __syncwarp();
+    // early split-K exchange: the peer's block is expected from the start; the
+    // cluster barrier below orders this before the peer's copy
+    if (EARLY && lane == 0) mbar_arrive_expect_tx(rfull, SLICE_BYTES);
   }
   if (warp == 1) {
     if (PAIR) {
@@ -641,6 +653,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     named_bar_sync(1, NUM_THREADS);
   }
+  // early split-K exchange: every CTA's barriers exist before a peer copies into
+  // it (waited for by the epilogue warps before their copies, by the others at
+  // the end)
+  if (EARLY) cluster_arrive();
   tc_fence_after();
   const uint32_t tmem_base = warp == 0 ? 0u : *tmem_slot;   // warp 0 never touches TMEM
 
@@ -816,6 +832,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // -------------------------------------------------------- epilogue
     const int ew = warp - EPI_WARP0;     // 0..3
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
+    if (EARLY) cluster_wait();           // the peer's barriers exist (long before it is needed)
+    bool pushed = false;                 // early split-K: this warp's rows were sent
+    // early split-K: copy this warp's 32 rows of the staged peer slice (ring
+    // offset 0) into the peer's staging area, counted on the peer's rfull
+    auto push_rows = [&]() {
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t peer = 1u - srank;
+        const uint32_t part = static_cast<uint32_t>(quarter * 32 * SLICE * 4);
+        bulk_copy_s2cluster(map_addr_to_rank(smem_u32(smem + L::off_epi) + part, peer),
+                            smem_u32(smem) + part, 32 * SLICE * 4,
+                            map_addr_to_rank(smem_u32(rfull), peer));
+      }
+      pushed = true;
+    };
     EpiState st{smem + L::off_epi + ew * EPI_BUFS * L::EPI_BUF_BYTES, &cload[ew * EPI_BUFS], 0,
                 -1, 0};
     uint32_t tl = 0, esync_uses = 0;
@@ -979,7 +1010,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // this CTA's ring (idle: every MMA that read it has completed), one
         // contiguous [128 rows][SLICE] block per peer, 16-byte pieces
         // XOR-swizzled by row; the blocks are bulk-copied to the peers after
-        // the cluster barrier.  The CTA's own slice stays in TMEM.
+        // the cluster barrier (early exchange: each warp sends its rows at
+        // once).  The CTA's own slice stays in TMEM.
         const int prow = quarter * 32 + r;
 #pragma unroll 1
         for (int qi = 0; qi < SPLIT - 1; ++qi) {
@@ -1001,7 +1033,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         fence_proxy_async_smem();   // read next by the bulk copies
-        continue;   // one tile per split-K cluster; phase 2 runs after the cluster barrier
+        if (EARLY) push_rows();
+        continue;   // one tile per split-K cluster; phase 2 follows
       }
       if (w.g0 > 0) {
         // Stream-K segment that does not hold its tile's first k-groups: publish
@@ -1081,6 +1114,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = args.epi ? store_tile(yes, yes, t_row, nb, row0, buf, contrib0, ncontrib)
                       : store_tile(yes, no, t_row, nb, row0, buf, contrib0, ncontrib);
     }
+    // after an abort the rows are sent all the same, so the peer never waits
+    // for a block that will not come
+    if (EARLY && !pushed) push_rows();
     if (!SPLITK) {
       if (!ok && st.pending_cload >= 0 && lane == 0)
         wait_drain<PAIR>(&st.cload[st.pending_cload], st.pending_phase, args);
@@ -1093,6 +1129,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
 
+  if (EARLY && warp < EPI_WARP0) {   // the start-up cluster barrier, for the other roles
+    __syncwarp();
+    cluster_wait();
+  }
   tc_fence_before();
   __syncthreads();
   if (SPLITK) {
@@ -1103,10 +1143,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // (from TMEM) and the received ones in rank order (deterministic) and
     // finishes them like the plain epilogue.  The copies are sent even after an
     // abort, so a peer never waits for a block that will not come.
-    constexpr uint32_t RECV0 = (SPLIT - 1) * SLICE_BYTES;   // receive area, after the send area
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(rfull, (SPLIT - 1) * SLICE_BYTES);
-    cluster_sync();
-    if (threadIdx.x == 0) {
+    // (The early exchange has sent its block already: its receive area is the
+    // staging area, and the final chunks stage in the ring after the send area.)
+    constexpr uint32_t RECV0 = EARLY ? static_cast<uint32_t>(L::off_epi)
+                                     : (SPLIT - 1) * SLICE_BYTES;   // receive area
+    if (!EARLY && threadIdx.x == 0) mbar_arrive_expect_tx(rfull, (SPLIT - 1) * SLICE_BYTES);
+    if (!EARLY) cluster_sync();
+    if (!EARLY && threadIdx.x == 0) {
       const uint32_t base = smem_u32(smem);
       for (int qi = 0; qi < SPLIT - 1; ++qi) {
         const uint32_t q = qi < static_cast<int>(srank) ? qi : qi + 1;
@@ -1121,8 +1164,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int ew = warp - EPI_WARP0;
       const int quarter = warp & 3;
       const int r = lane;
-      EpiState st{smem + L::off_epi + ew * EPI_BUFS * L::EPI_BUF_BYTES, &cload[ew * EPI_BUFS], 0,
-                  -1, 0};
+      uint8_t* const stage0 = EARLY ? smem + SLICE_BYTES : smem + L::off_epi;
+      EpiState st{stage0 + ew * EPI_BUFS * L::EPI_BUF_BYTES, &cload[ew * EPI_BUFS], 0, -1, 0};
       int mb, nb;
       tile_of(args, unit0, &mb, &nb);
       const int row0 = mb * BM + quarter * 32;
