@@ -441,9 +441,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   p->epi_chunk_cols = out_dtype == GEMM_F32 ? 32 : 64;
   p->cta_group = pair ? 2 : 1;
   // the conditions of run_gemm's plain path that the plan itself fixes
-  p->specialised = (p->sk_iters == 0 && p->order == GEMM_ORDER_GROUPED && !(cfg && cfg->general) &&
+  p->specialised = (p->order == GEMM_ORDER_GROUPED && !(cfg && cfg->general) &&
                     (N * out_size(out_dtype)) % 16 == 0 &&
-                    spec_supported(bn, pair, split, layout, is_fp8(in_dtype)))
+                    spec_supported(bn, pair, split, layout, is_fp8(in_dtype), p->sk_iters != 0))
                        ? 1
                        : 0;
   return GEMM_OK;
@@ -637,22 +637,23 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   // A call on the plain path takes the specialised instance of its
   // configuration and layout when there is one (cfg->general = 1 forbids it).
   const bool plain = !(cfg && cfg->general) && !ka.read_c && !ka.epi && !ka.n_ragged &&
-                     ka.sk_iters == 0 && ka.inject_skip == 0 && ka.tile_map == nullptr;
+                     ka.inject_skip == 0 && ka.tile_map == nullptr;
+  const bool sk = ka.sk_iters != 0;
   cudaError_t e = cudaErrorNotSupported;
   if (plain) {
     const bool f8 = is_fp8(in_dtype);
     switch (out_dtype) {
       case GEMM_F32:
-        e = f8 ? launch_gemm_f8_spec_f32(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev)
-               : launch_gemm_spec_f32(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev);
+        e = f8 ? launch_gemm_f8_spec_f32(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev)
+               : launch_gemm_spec_f32(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev);
         break;
       case GEMM_BF16:
-        e = f8 ? launch_gemm_f8_spec_bf16(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev)
-               : launch_gemm_spec_bf16(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev);
+        e = f8 ? launch_gemm_f8_spec_bf16(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev)
+               : launch_gemm_spec_bf16(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev);
         break;
       default:
-        e = f8 ? launch_gemm_f8_spec_f16(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev)
-               : launch_gemm_spec_f16(p.bn, pair, p.split_k, layout, mp, ka, p.grid, stream, dev);
+        e = f8 ? launch_gemm_f8_spec_f16(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev)
+               : launch_gemm_spec_f16(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev);
         break;
     }
     if (e != cudaErrorNotSupported) return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

@@ -450,8 +450,9 @@ __device__ __forceinline__ unsigned int flag_acquire(const unsigned int* f) {
 
 
 // Specialised instances.  Most launches take the plain path: no C read, no
-// bias or activation, N * sizeof(out) a multiple of 16 bytes, data-parallel
-// tiles in grouped order, no fault injection; and each operand's major-ness is
+// bias or activation, N * sizeof(out) a multiple of 16 bytes, tiles in grouped
+// order, no fault injection, and data-parallel tiles only (or, with
+// SPEC_STREAMK, a stream-K tail as well); and each operand's major-ness is
 // fixed by the call's layout.  Folding those parameters into constants drops
 // the code of the other paths from the kernel, which roughly halves its
 // instruction-cache misses and shortens the one-off start-up and epilogue code
@@ -461,9 +462,11 @@ enum : int {
   SPEC_PLAIN = 1,          // plain epilogue and scheduling (see above)
   SPEC_LAYOUT = 2,         // operand layout fixed: bits 2..3 hold GEMM_A_* | GEMM_B_*
   SPEC_LAYOUT_SHIFT = 2,
+  SPEC_STREAMK = 16,       // with SPEC_PLAIN: stream-K work stays a run-time choice
 };
-constexpr int spec_bits(int layout) {   // the specialisation of a plain call with `layout`
-  return SPEC_PLAIN | SPEC_LAYOUT | (layout << SPEC_LAYOUT_SHIFT);
+// the specialisation of a plain call with `layout` (and stream-K work when sk)
+constexpr int spec_bits(int layout, bool sk) {
+  return SPEC_PLAIN | SPEC_LAYOUT | (layout << SPEC_LAYOUT_SHIFT) | (sk ? SPEC_STREAMK : 0);
 }
 template <int SPEC, bool F8>
 __device__ __forceinline__ KernelArgs specialise_args(const KernelArgs& in) {
@@ -474,7 +477,7 @@ __device__ __forceinline__ KernelArgs specialise_args(const KernelArgs& in) {
     a.bias_kind = EPI_BIAS_NONE;
     a.act = EPI_ACT_NONE;
     a.n_ragged = 0;
-    a.sk_iters = 0;
+    if (!(SPEC & SPEC_STREAMK)) a.sk_iters = 0;
     a.inject_skip = 0;
     a.tile_map = nullptr;
   }

@@ -1,6 +1,7 @@
 """Specialised kernel instances (the plain path -- beta == 0, no bias or activation,
-no ragged right edge, data-parallel grouped tiles -- with the operand layout fixed
-at compile time) against the general kernel and the oracle.  The same call with
+no ragged right edge, grouped tiles, data-parallel or with a stream-K tail on the
+CTA pair -- with the operand layout fixed at compile time) against the general
+kernel and the oracle.  The same call with
 gemm_config_t.general = 0 and = 1 must give identical bits, and integer inputs
 must match the oracle exactly, in every layout and every configuration that has
 specialised instances."""
@@ -17,10 +18,11 @@ LAYOUTS = [(False, False), (False, True), (True, False), (True, True)]
 # (config, M, N, K): several tiles, ragged M and K (N * 4 and N * 2 bytes stay
 # multiples of 16, so the calls stay on the plain path)
 CASES = [({"cta_group": 2, "bn": 256}, 520, 776, 456),
+         ({"cta_group": 2, "bn": 256, "stream_k": 2}, 1032, 1288, 1000),
          ({"cta_group": 1, "split_k": 2, "bn": 128}, 200, 392, 648),
          ({"cta_group": 1, "split_k": 2, "bn": 64}, 136, 328, 520),
          ({"cta_group": 1, "bn": 64}, 300, 200, 200)]
-CASE_IDS = ["pair256", "splitk2-bn128", "splitk2-bn64", "cta1-bn64"]
+CASE_IDS = ["pair256", "pair256-streamk", "splitk2-bn128", "splitk2-bn64", "cta1-bn64"]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -424,8 +424,11 @@ def test_plan_specialised_flag():
     for layout in range(4):
         assert plan(2048, 2048, 2048, 0, 2, layout, 152) == 1
         assert plan(2048, 2048, 2048, 0, 2, layout, 152, {"general": 1}) == 0
-    # stream-K work (4096^3 plans a stream-K tail) is not on the plain path
+    # 4096^3 plans a stream-K tail: the pair has stream-K instances, the single
+    # CTA does not
     s, p = g.gemm_plan(4096, 4096, 4096, 1, 1, 0, 152)
+    assert s == 0 and p.sk_iters > 0 and p.specialised == 1
+    s, p = g.gemm_plan(4096, 4096, 4096, 1, 1, 0, 152, {"cta_group": 1, "bn": 64, "stream_k": 2})
     assert s == 0 and p.sk_iters > 0 and p.specialised == 0
     # skinny and decode shapes: 2-way split-K clusters
     assert plan(128, 8192, 8192, 1, 1, 2, 152) == 1
