@@ -443,7 +443,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   // the conditions of run_gemm's plain path that the plan itself fixes
   p->specialised = (p->order == GEMM_ORDER_GROUPED && !(cfg && cfg->general) &&
                     (N * out_size(out_dtype)) % 16 == 0 &&
-                    spec_supported(bn, pair, split, layout, is_fp8(in_dtype), p->sk_iters != 0))
+                    spec_supported(bn, pair, split, layout, is_fp8(in_dtype), p->sk_iters != 0,
+                                   false))
                        ? 1
                        : 0;
   return GEMM_OK;
@@ -636,26 +637,19 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
 
   // A call on the plain path takes the specialised instance of its
   // configuration and layout when there is one (cfg->general = 1 forbids it).
-  const bool plain = !(cfg && cfg->general) && !ka.read_c && !ka.epi && !ka.n_ragged &&
-                     ka.inject_skip == 0 && ka.tile_map == nullptr;
-  const bool sk = ka.sk_iters != 0;
+  const bool plain = !(cfg && cfg->general) && !ka.epi && !ka.n_ragged && ka.inject_skip == 0 &&
+                     ka.tile_map == nullptr;
+  const bool sk = ka.sk_iters != 0, readc = ka.read_c != 0;
   cudaError_t e = cudaErrorNotSupported;
   if (plain) {
+    using SpecLaunch = cudaError_t (*)(int, bool, int, int, bool, bool, const OperandMaps&,
+                                       const KernelArgs&, int, cudaStream_t, int);
     const bool f8 = is_fp8(in_dtype);
-    switch (out_dtype) {
-      case GEMM_F32:
-        e = f8 ? launch_gemm_f8_spec_f32(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev)
-               : launch_gemm_spec_f32(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev);
-        break;
-      case GEMM_BF16:
-        e = f8 ? launch_gemm_f8_spec_bf16(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev)
-               : launch_gemm_spec_bf16(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev);
-        break;
-      default:
-        e = f8 ? launch_gemm_f8_spec_f16(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev)
-               : launch_gemm_spec_f16(p.bn, pair, p.split_k, layout, sk, mp, ka, p.grid, stream, dev);
-        break;
-    }
+    const SpecLaunch launch =
+        out_dtype == GEMM_F32    ? (f8 ? launch_gemm_f8_spec_f32 : launch_gemm_spec_f32)
+        : out_dtype == GEMM_BF16 ? (f8 ? launch_gemm_f8_spec_bf16 : launch_gemm_spec_bf16)
+                                 : (f8 ? launch_gemm_f8_spec_f16 : launch_gemm_spec_f16);
+    e = launch(p.bn, pair, p.split_k, layout, sk, readc, mp, ka, p.grid, stream, dev);
     if (e != cudaErrorNotSupported) return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
   switch (out_dtype) {

@@ -449,11 +449,11 @@ __device__ __forceinline__ unsigned int flag_acquire(const unsigned int* f) {
 }
 
 
-// Specialised instances.  Most launches take the plain path: no C read, no
-// bias or activation, N * sizeof(out) a multiple of 16 bytes, tiles in grouped
-// order, no fault injection, and data-parallel tiles only (or, with
-// SPEC_STREAMK, a stream-K tail as well); and each operand's major-ness is
-// fixed by the call's layout.  Folding those parameters into constants drops
+// Specialised instances.  Most launches take the plain path: no C read (or,
+// with SPEC_READC, always a C read), no bias or activation, N * sizeof(out) a
+// multiple of 16 bytes, tiles in grouped order, no fault injection, and
+// data-parallel tiles only (or, with SPEC_STREAMK, a stream-K tail as well);
+// and each operand's major-ness is fixed by the call's layout.  Folding those parameters into constants drops
 // the code of the other paths from the kernel, which roughly halves its
 // instruction-cache misses and shortens the one-off start-up and epilogue code
 // (2048^3: about 10% of the launch).  The host launches a specialised instance
@@ -463,16 +463,19 @@ enum : int {
   SPEC_LAYOUT = 2,         // operand layout fixed: bits 2..3 hold GEMM_A_* | GEMM_B_*
   SPEC_LAYOUT_SHIFT = 2,
   SPEC_STREAMK = 16,       // with SPEC_PLAIN: stream-K work stays a run-time choice
+  SPEC_READC = 32,         // with SPEC_PLAIN: C is read (beta != 0)
 };
-// the specialisation of a plain call with `layout` (and stream-K work when sk)
-constexpr int spec_bits(int layout, bool sk) {
-  return SPEC_PLAIN | SPEC_LAYOUT | (layout << SPEC_LAYOUT_SHIFT) | (sk ? SPEC_STREAMK : 0);
+// the specialisation of a plain call with `layout` (stream-K work when sk, a C
+// read when readc)
+constexpr int spec_bits(int layout, bool sk, bool readc) {
+  return SPEC_PLAIN | SPEC_LAYOUT | (layout << SPEC_LAYOUT_SHIFT) | (sk ? SPEC_STREAMK : 0) |
+         (readc ? SPEC_READC : 0);
 }
 template <int SPEC, bool F8>
 __device__ __forceinline__ KernelArgs specialise_args(const KernelArgs& in) {
   KernelArgs a = in;
   if (SPEC & SPEC_PLAIN) {
-    a.read_c = 0;
+    a.read_c = (SPEC & SPEC_READC) ? 1 : 0;
     a.epi = 0;
     a.bias_kind = EPI_BIAS_NONE;
     a.act = EPI_ACT_NONE;

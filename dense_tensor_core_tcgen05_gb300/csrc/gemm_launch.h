@@ -51,30 +51,38 @@ cudaError_t launch_gemm_f8_f16(int bn, bool pair, int split, const OperandMaps& 
                             const KernelArgs& args, int grid, cudaStream_t stream, int dev);
 
 // Configurations with specialised instances (plain path, fixed layout; see
-// specialise_args): the 256-wide CTA pair (with and without a stream-K tail,
-// sk), the 2-way split-K clusters of width 128 and 64 and the single 64-wide
-// CTA, in every layout (8-bit operands: A row-major with B column-major only).
-constexpr bool spec_supported(int bn, bool pair, int split, int layout, bool fp8, bool sk) {
+// specialise_args): the 256-wide CTA pair (with a stream-K tail, sk, or with a
+// C read, readc, or neither), the 2-way split-K clusters of width 128 and 64
+// and the single 64-wide CTA, in every layout (8-bit operands: A row-major with
+// B column-major only).
+constexpr bool spec_supported(int bn, bool pair, int split, int layout, bool fp8, bool sk,
+                              bool readc) {
   if (layout < 0 || layout > 3 || (fp8 && layout != 2)) return false;
-  if (pair) return bn == 256 && split == 1;
-  if (sk) return false;
+  if (pair) return bn == 256 && split == 1 && !(sk && readc);
+  if (sk || readc) return false;
   return (split == 2 && (bn == 128 || bn == 64)) || (split == 1 && bn == 64);
 }
 
-// Launch the specialised instance of (bn, pair, split, layout, sk), or return
+// Launch the specialised instance of (bn, pair, split, layout, sk, readc), or return
 // cudaErrorNotSupported when spec_supported() says there is none.  Only for
 // calls on the plain path.
-cudaError_t launch_gemm_spec_f32(int bn, bool pair, int split, int layout, bool sk, const OperandMaps& m,
+cudaError_t launch_gemm_spec_f32(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                 const OperandMaps& m,
                                  const KernelArgs& args, int grid, cudaStream_t stream, int dev);
-cudaError_t launch_gemm_spec_bf16(int bn, bool pair, int split, int layout, bool sk, const OperandMaps& m,
+cudaError_t launch_gemm_spec_bf16(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                 const OperandMaps& m,
                                   const KernelArgs& args, int grid, cudaStream_t stream, int dev);
-cudaError_t launch_gemm_spec_f16(int bn, bool pair, int split, int layout, bool sk, const OperandMaps& m,
+cudaError_t launch_gemm_spec_f16(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                 const OperandMaps& m,
                                  const KernelArgs& args, int grid, cudaStream_t stream, int dev);
-cudaError_t launch_gemm_f8_spec_f32(int bn, bool pair, int split, int layout, bool sk, const OperandMaps& m,
+cudaError_t launch_gemm_f8_spec_f32(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                 const OperandMaps& m,
                                     const KernelArgs& args, int grid, cudaStream_t stream, int dev);
-cudaError_t launch_gemm_f8_spec_bf16(int bn, bool pair, int split, int layout, bool sk, const OperandMaps& m,
+cudaError_t launch_gemm_f8_spec_bf16(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                 const OperandMaps& m,
                                      const KernelArgs& args, int grid, cudaStream_t stream, int dev);
-cudaError_t launch_gemm_f8_spec_f16(int bn, bool pair, int split, int layout, bool sk, const OperandMaps& m,
+cudaError_t launch_gemm_f8_spec_f16(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                 const OperandMaps& m,
                                     const KernelArgs& args, int grid, cudaStream_t stream, int dev);
 
 // Split-K cluster shapes that have kernel instances: (bn, split).

@@ -70,33 +70,36 @@ cudaError_t launch_inst(const OperandMaps& m, const KernelArgs& args, int grid,
 #ifdef GEMM_LAUNCH_SPEC_NAME
 namespace {
 // The specialised instances of one layout: the configurations most plans use
-// (the 256-wide CTA pair of large GEMMs, with or without a stream-K tail; the
+// (the 256-wide CTA pair of large GEMMs, with a stream-K tail or a C read; the
 // 2-way split-K clusters of small-M ones; the single 64-wide CTA of small ones).
 template <int LAYOUT>
-cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, const OperandMaps& m,
-                               const KernelArgs& args, int grid, cudaStream_t stream, int dev) {
-  constexpr int S = spec_bits(LAYOUT, false);
-  if (pair)
-    return sk ? launch_inst<256, true, 1, spec_bits(LAYOUT, true)>(m, args, grid, stream, dev)
-              : launch_inst<256, true, 1, S>(m, args, grid, stream, dev);
+cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc,
+                               const OperandMaps& m, const KernelArgs& args, int grid,
+                               cudaStream_t stream, int dev) {
+  constexpr int S = spec_bits(LAYOUT, false, false);
+  if (pair) {
+    if (sk) return launch_inst<256, true, 1, spec_bits(LAYOUT, true, false)>(m, args, grid, stream, dev);
+    if (readc) return launch_inst<256, true, 1, spec_bits(LAYOUT, false, true)>(m, args, grid, stream, dev);
+    return launch_inst<256, true, 1, S>(m, args, grid, stream, dev);
+  }
   if (split == 2 && bn == 128) return launch_inst<128, false, 2, S>(m, args, grid, stream, dev);
   if (split == 2) return launch_inst<64, false, 2, S>(m, args, grid, stream, dev);
   return launch_inst<64, false, 1, S>(m, args, grid, stream, dev);
 }
 }  // namespace
 
-cudaError_t GEMM_LAUNCH_SPEC_NAME(int bn, bool pair, int split, int layout, bool sk,
+cudaError_t GEMM_LAUNCH_SPEC_NAME(int bn, bool pair, int split, int layout, bool sk, bool readc,
                                   const OperandMaps& m, const KernelArgs& args, int grid,
                                   cudaStream_t stream, int dev) {
-  if (!spec_supported(bn, pair, split, layout, GEMM_F8, sk)) return cudaErrorNotSupported;
+  if (!spec_supported(bn, pair, split, layout, GEMM_F8, sk, readc)) return cudaErrorNotSupported;
   if constexpr (GEMM_F8) {   // 8-bit operands are K-major only
-    return launch_spec_layout<2>(bn, pair, split, sk, m, args, grid, stream, dev);
+    return launch_spec_layout<2>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
   } else {
     switch (layout) {
-      case 0: return launch_spec_layout<0>(bn, pair, split, sk, m, args, grid, stream, dev);
-      case 1: return launch_spec_layout<1>(bn, pair, split, sk, m, args, grid, stream, dev);
-      case 2: return launch_spec_layout<2>(bn, pair, split, sk, m, args, grid, stream, dev);
-      case 3: return launch_spec_layout<3>(bn, pair, split, sk, m, args, grid, stream, dev);
+      case 0: return launch_spec_layout<0>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
+      case 1: return launch_spec_layout<1>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
+      case 2: return launch_spec_layout<2>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
+      case 3: return launch_spec_layout<3>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
       default: return cudaErrorNotSupported;
     }
   }

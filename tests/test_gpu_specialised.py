@@ -99,6 +99,26 @@ def test_specialised_fp8(_lib, fmt, case):
                          b_col=True, exact=True)
 
 
+@pytest.mark.parametrize("a_col,b_col", LAYOUTS)
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_specialised_beta(_lib, a_col, b_col, out_dtype):
+    """The CTA pair's C-reading instances: beta * C exact on integers, and the
+    same bits as the general kernel."""
+    M, N, K = 520, 776, 456
+    cfg = {"cta_group": 2, "bn": 256}
+    A, B = operands(M, N, K, "bf16", a_col, b_col, dist="int", seed=N + K, pad=True)
+    C = si.matrix("int", 77, M, pad8(N), out_dtype)
+    for beta in (1.0, -2.0):
+        spec, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype=out_dtype,
+                              a_col=a_col, b_col=b_col, beta=beta, C=C, cfg=cfg, ldc=pad8(N))
+        gen, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype=out_dtype,
+                             a_col=a_col, b_col=b_col, beta=beta, C=C, cfg=dict(cfg, general=1),
+                             ldc=pad8(N))
+        np.testing.assert_array_equal(spec, gen)
+        check_against_oracle(spec, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype=out_dtype,
+                             a_col=a_col, b_col=b_col, beta=beta, C=C, exact=True)
+
+
 def test_workload_2048_specialised(_lib):
     """The 2048^3 fp16 -> fp32 workload runs a specialised instance; same bits as
     the general kernel."""
