@@ -304,33 +304,35 @@ void choose_unit(int64_t M, int64_t N, int num_sms, int* bn_out, bool* pair_out)
   }
 }
 
-// Split-K choice for a single 128-row panel (M <= 128), where output tiles alone
-// cannot occupy the GPU: tiles of 128 (split 2) or 256 columns (split 4, then 2)
-// over a cluster of CTAs, the first that fits in one wave, keeps at least 8
-// k-blocks per CTA and reaches the parallelism of 64-wide unsplit tiles.
-// 128-wide tiles come first: their 3-stage ring hid HBM latency best on the
-// 128 x 8192 x 8192 stream (36.9 us vs 45 us for 256-wide tiles split 4).
-// Returns 1 (no split) otherwise.
+// Tile and split-K choice for a single 128-row panel (M <= 128), where output
+// tiles alone cannot occupy the GPU: a tile width and a cluster of `split` CTAs
+// per tile, each accumulating 1/split of K.  The choice that puts the most CTAs
+// in one wave, each with at least 8 k-blocks; on a tie the earlier of this list:
+// 128-wide tiles first (their 3-stage ring hides HBM latency better than the
+// 2-stage ring of 256-wide ones: 8 x 14336 x 4096 runs 30.7 us unsplit at 128
+// against 35.4 us split 2 at 256; 128 x 8192 x 8192 36.9 vs 45 us split 4),
+// fewer splits first (less partial-sum exchange), 64-wide before 256-wide.
+// Unsplit tiles only for panels of at most 32 rows: each CTA then reads all of
+// A's K, which for taller panels outweighs the exchange a split saves.
+// Returns 0 (no opinion: the general unit choice applies) when M > 128 or when
+// no choice reaches the parallelism of 64-wide unsplit tiles; otherwise the
+// split (1 = unsplit) with the tile width in *bn_out.
 int choose_split(int64_t M, int64_t N, int64_t K, int kbe, int num_sms, int* bn_out) {
-  if (M > BM) return 1;
+  if (M > BM) return 0;
   const int64_t kb = ceil_div(K, kbe);
-  // The most CTAs that fit one wave, each with at least 8 k-blocks; on a tie the
-  // fewer splits (less partial-sum exchange), then the wider tile.  Listed in
-  // that order of preference.
-  const struct { int bn, s; } cands[7] = {{256, 2}, {128, 2}, {64, 2}, {256, 4},
-                                          {128, 4}, {64, 4}, {128, 8}};
+  const struct { int bn, s; } cands[] = {{128, 1}, {128, 2}, {64, 2}, {256, 2},
+                                         {128, 4}, {64, 4}, {256, 4}, {128, 8}};
   int best = -1;
   int64_t best_ctas = 0;
-  for (int i = 0; i < 7; ++i) {
+  for (int i = 0; i < static_cast<int>(sizeof(cands) / sizeof(cands[0])); ++i) {
     const int64_t ctas = ceil_div(N, cands[i].bn) * cands[i].s;
+    if (cands[i].s == 1 && M > 32) continue;
     if (ctas <= num_sms && kb >= 8 * cands[i].s && ctas > best_ctas) {
       best = i;
       best_ctas = ctas;
     }
   }
-  // worth splitting only when it reaches half the SMs or more than the
-  // unsplit 64-wide tiles would
-  if (best < 0 || best_ctas < std::min<int64_t>(ceil_div(N, 64), num_sms / 2)) return 1;
+  if (best < 0 || best_ctas < std::min<int64_t>(ceil_div(N, 64), num_sms / 2)) return 0;
   *bn_out = cands[best].bn;
   return cands[best].s;
 }
@@ -347,7 +349,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   bool pair = false;
   choose_unit(M, N, num_sms, &bn, &pair);
   int split = choose_split(M, N, K, kbe, num_sms, &bn);
-  if (split > 1) pair = false;
+  if (split > 0) pair = false;   // the single panel's choice: single-CTA tiles
+  if (split == 0) split = 1;
   // a manual tile setting without an explicit split_k turns the automatic split off
   if (cfg && (cfg->cta_group || cfg->bn) && !cfg->split_k) split = 1;
   if (cfg && cfg->cta_group) {
@@ -645,10 +648,17 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
     using SpecLaunch = cudaError_t (*)(int, bool, int, int, bool, bool, const OperandMaps&,
                                        const KernelArgs&, int, cudaStream_t, int);
     const bool f8 = is_fp8(in_dtype);
+    const bool set2 = spec_set(p.bn, pair, p.split_k, sk, readc) == 2;
     const SpecLaunch launch =
-        out_dtype == GEMM_F32    ? (f8 ? launch_gemm_f8_spec_f32 : launch_gemm_spec_f32)
-        : out_dtype == GEMM_BF16 ? (f8 ? launch_gemm_f8_spec_bf16 : launch_gemm_spec_bf16)
-                                 : (f8 ? launch_gemm_f8_spec_f16 : launch_gemm_spec_f16);
+        f8 ? (out_dtype == GEMM_F32    ? launch_gemm_f8_spec_f32
+              : out_dtype == GEMM_BF16 ? launch_gemm_f8_spec_bf16
+                                       : launch_gemm_f8_spec_f16)
+        : set2 ? (out_dtype == GEMM_F32    ? launch_gemm_spec2_f32
+                  : out_dtype == GEMM_BF16 ? launch_gemm_spec2_bf16
+                                           : launch_gemm_spec2_f16)
+               : (out_dtype == GEMM_F32    ? launch_gemm_spec_f32
+                  : out_dtype == GEMM_BF16 ? launch_gemm_spec_bf16
+                                           : launch_gemm_spec_f16);
     e = launch(p.bn, pair, p.split_k, layout, sk, readc, mp, ka, p.grid, stream, dev);
     if (e != cudaErrorNotSupported) return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }

@@ -51,16 +51,27 @@ cudaError_t launch_gemm_f8_f16(int bn, bool pair, int split, const OperandMaps& 
                             const KernelArgs& args, int grid, cudaStream_t stream, int dev);
 
 // Configurations with specialised instances (plain path, fixed layout; see
-// specialise_args): the 256-wide CTA pair (with a stream-K tail, sk, or with a
-// C read, readc, or neither), the 2-way split-K clusters of width 128 and 64
-// and the single 64-wide CTA, in every layout (8-bit operands: A row-major with
-// B column-major only).
+// specialise_args), by the set of translation units that holds them (0: none):
+// set 1, the 256-wide CTA pair (with a stream-K tail, sk, or with a C read,
+// readc, or neither), the 2-way split-K clusters of width 128 and 64 and the
+// single 64-wide CTA; set 2, the other single-panel choices (the single
+// 128-wide CTA, 4-way clusters of width 64 and 128, 2-way clusters of width
+// 256).  8-bit operands keep both sets in their own units.
+constexpr int spec_set(int bn, bool pair, int split, bool sk, bool readc) {
+  if (pair) return (bn == 256 && split == 1 && !(sk && readc)) ? 1 : 0;
+  if (sk || readc) return 0;
+  if ((split == 2 && (bn == 128 || bn == 64)) || (split == 1 && bn == 64)) return 1;
+  if ((split == 1 && bn == 128) || (split == 4 && (bn == 128 || bn == 64)) ||
+      (split == 2 && bn == 256))
+    return 2;
+  return 0;
+}
+
+// Every layout has them (8-bit operands: A row-major with B column-major only).
 constexpr bool spec_supported(int bn, bool pair, int split, int layout, bool fp8, bool sk,
                               bool readc) {
   if (layout < 0 || layout > 3 || (fp8 && layout != 2)) return false;
-  if (pair) return bn == 256 && split == 1 && !(sk && readc);
-  if (sk || readc) return false;
-  return (split == 2 && (bn == 128 || bn == 64)) || (split == 1 && bn == 64);
+  return spec_set(bn, pair, split, sk, readc) != 0;
 }
 
 // Launch the specialised instance of (bn, pair, split, layout, sk, readc), or return
@@ -75,6 +86,15 @@ cudaError_t launch_gemm_spec_bf16(int bn, bool pair, int split, int layout, bool
 cudaError_t launch_gemm_spec_f16(int bn, bool pair, int split, int layout, bool sk, bool readc,
                                  const OperandMaps& m,
                                  const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_spec2_f32(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                  const OperandMaps& m, const KernelArgs& args, int grid,
+                                  cudaStream_t stream, int dev);
+cudaError_t launch_gemm_spec2_bf16(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                   const OperandMaps& m, const KernelArgs& args, int grid,
+                                   cudaStream_t stream, int dev);
+cudaError_t launch_gemm_spec2_f16(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                  const OperandMaps& m, const KernelArgs& args, int grid,
+                                  cudaStream_t stream, int dev);
 cudaError_t launch_gemm_f8_spec_f32(int bn, bool pair, int split, int layout, bool sk, bool readc,
                                  const OperandMaps& m,
                                     const KernelArgs& args, int grid, cudaStream_t stream, int dev);

@@ -1,9 +1,13 @@
 // Body of one launcher translation unit.  The including file defines
 // GEMM_OUT_KIND; GEMM_LAUNCH_NAME (the general instances) unless GEMM_SPEC_ONLY
-// is set; GEMM_LAUNCH_SPEC_NAME for the specialised instances it holds; and
-// GEMM_F8 (8-bit operands) when it is set.
+// is set; GEMM_LAUNCH_SPEC_NAME for the specialised instances it holds, of set
+// GEMM_SPEC_SET (see spec_set; 0 = all sets); and GEMM_F8 (8-bit operands) when
+// it is set.
 #ifndef GEMM_F8
 #define GEMM_F8 false
+#endif
+#ifndef GEMM_SPEC_SET
+#define GEMM_SPEC_SET 0
 #endif
 #include "gemm_kernel.cuh"
 #include "gemm_launch.h"
@@ -69,22 +73,29 @@ cudaError_t launch_inst(const OperandMaps& m, const KernelArgs& args, int grid,
 
 #ifdef GEMM_LAUNCH_SPEC_NAME
 namespace {
-// The specialised instances of one layout: the configurations most plans use
-// (the 256-wide CTA pair of large GEMMs, with a stream-K tail or a C read; the
-// 2-way split-K clusters of small-M ones; the single 64-wide CTA of small ones).
+// The specialised instances of one layout in this unit's set (see spec_set).
 template <int LAYOUT>
 cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc,
                                const OperandMaps& m, const KernelArgs& args, int grid,
                                cudaStream_t stream, int dev) {
   constexpr int S = spec_bits(LAYOUT, false, false);
+#if GEMM_SPEC_SET != 2
   if (pair) {
     if (sk) return launch_inst<256, true, 1, spec_bits(LAYOUT, true, false)>(m, args, grid, stream, dev);
     if (readc) return launch_inst<256, true, 1, spec_bits(LAYOUT, false, true)>(m, args, grid, stream, dev);
     return launch_inst<256, true, 1, S>(m, args, grid, stream, dev);
   }
   if (split == 2 && bn == 128) return launch_inst<128, false, 2, S>(m, args, grid, stream, dev);
-  if (split == 2) return launch_inst<64, false, 2, S>(m, args, grid, stream, dev);
-  return launch_inst<64, false, 1, S>(m, args, grid, stream, dev);
+  if (split == 2 && bn == 64) return launch_inst<64, false, 2, S>(m, args, grid, stream, dev);
+  if (split == 1 && bn == 64) return launch_inst<64, false, 1, S>(m, args, grid, stream, dev);
+#endif
+#if GEMM_SPEC_SET != 1
+  if (split == 1 && bn == 128) return launch_inst<128, false, 1, S>(m, args, grid, stream, dev);
+  if (split == 4 && bn == 128) return launch_inst<128, false, 4, S>(m, args, grid, stream, dev);
+  if (split == 4 && bn == 64) return launch_inst<64, false, 4, S>(m, args, grid, stream, dev);
+  if (split == 2 && bn == 256) return launch_inst<256, false, 2, S>(m, args, grid, stream, dev);
+#endif
+  return cudaErrorNotSupported;
 }
 }  // namespace
 
@@ -92,6 +103,8 @@ cudaError_t GEMM_LAUNCH_SPEC_NAME(int bn, bool pair, int split, int layout, bool
                                   const OperandMaps& m, const KernelArgs& args, int grid,
                                   cudaStream_t stream, int dev) {
   if (!spec_supported(bn, pair, split, layout, GEMM_F8, sk, readc)) return cudaErrorNotSupported;
+  if (GEMM_SPEC_SET != 0 && spec_set(bn, pair, split, sk, readc) != GEMM_SPEC_SET)
+    return cudaErrorNotSupported;
   if constexpr (GEMM_F8) {   // 8-bit operands are K-major only
     return launch_spec_layout<2>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
   } else {

@@ -2,5 +2,6 @@
 // with bf16 output.
 #define GEMM_OUT_KIND OUT_BF16
 #define GEMM_SPEC_ONLY
+#define GEMM_SPEC_SET 1
 #define GEMM_LAUNCH_SPEC_NAME launch_gemm_spec_bf16
 #include "gemm_launch_impl.cuh"

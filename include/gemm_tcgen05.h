@@ -136,10 +136,10 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *             runs a kernel instance specialised for its layout when the
  *             plan's configuration has one: the 256-wide CTA pair (beta == 0
  *             with or without stream-K work, beta != 0 without it), and with
- *             beta == 0 and no stream-K work the 2-way split-K clusters of
- *             width 128 and 64 and the single 64-wide CTA.  Both kernels
- *             compute the same result bit for bit.  Other values:
- *             GEMM_ERR_INVALID_ARG. */
+ *             beta == 0 and no stream-K work the single CTA of width 64 or
+ *             128 and the split-K clusters of 2 CTAs (width 64, 128 or 256)
+ *             and of 4 CTAs (width 64 or 128).  Both kernels compute the same
+ *             result bit for bit.  Other values: GEMM_ERR_INVALID_ARG. */
 enum { GEMM_ORDER_AUTO = 0, GEMM_ORDER_GROUPED = 1, GEMM_ORDER_HILBERT = 2 };
 
 typedef struct {

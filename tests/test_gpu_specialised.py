@@ -21,8 +21,13 @@ CASES = [({"cta_group": 2, "bn": 256}, 520, 776, 456),
          ({"cta_group": 2, "bn": 256, "stream_k": 2}, 1032, 1288, 1000),
          ({"cta_group": 1, "split_k": 2, "bn": 128}, 200, 392, 648),
          ({"cta_group": 1, "split_k": 2, "bn": 64}, 136, 328, 520),
-         ({"cta_group": 1, "bn": 64}, 300, 200, 200)]
-CASE_IDS = ["pair256", "pair256-streamk", "splitk2-bn128", "splitk2-bn64", "cta1-bn64"]
+         ({"cta_group": 1, "bn": 64}, 300, 200, 200),
+         ({"cta_group": 1, "bn": 128}, 136, 520, 392),
+         ({"cta_group": 1, "split_k": 4, "bn": 128}, 120, 392, 1096),
+         ({"cta_group": 1, "split_k": 4, "bn": 64}, 72, 200, 1096),
+         ({"cta_group": 1, "split_k": 2, "bn": 256}, 130, 776, 648)]
+CASE_IDS = ["pair256", "pair256-streamk", "splitk2-bn128", "splitk2-bn64", "cta1-bn64", "cta1-bn128",
+            "splitk4-bn128", "splitk4-bn64", "splitk2-bn256"]
 
 
 @pytest.fixture(scope="module", autouse=True)
