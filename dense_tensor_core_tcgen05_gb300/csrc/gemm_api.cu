@@ -447,7 +447,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   p->specialised = (p->order == GEMM_ORDER_GROUPED && !(cfg && cfg->general) &&
                     (N * out_size(out_dtype)) % 16 == 0 &&
                     spec_supported(bn, pair, split, layout, is_fp8(in_dtype), p->sk_iters != 0,
-                                   false))
+                                   false, false))
                        ? 1
                        : 0;
   return GEMM_OK;
@@ -640,15 +640,15 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
 
   // A call on the plain path takes the specialised instance of its
   // configuration and layout when there is one (cfg->general = 1 forbids it).
-  const bool plain = !(cfg && cfg->general) && !ka.epi && !ka.n_ragged && ka.inject_skip == 0 &&
+  const bool plain = !(cfg && cfg->general) && !ka.n_ragged && ka.inject_skip == 0 &&
                      ka.tile_map == nullptr;
-  const bool sk = ka.sk_iters != 0, readc = ka.read_c != 0;
+  const bool sk = ka.sk_iters != 0, readc = ka.read_c != 0, epi = ka.epi != 0;
   cudaError_t e = cudaErrorNotSupported;
   if (plain) {
-    using SpecLaunch = cudaError_t (*)(int, bool, int, int, bool, bool, const OperandMaps&,
+    using SpecLaunch = cudaError_t (*)(int, bool, int, int, bool, bool, bool, const OperandMaps&,
                                        const KernelArgs&, int, cudaStream_t, int);
     const bool f8 = is_fp8(in_dtype);
-    const bool set2 = spec_set(p.bn, pair, p.split_k, sk, readc) == 2;
+    const bool set2 = spec_set(p.bn, pair, p.split_k, sk, readc, epi) == 2;
     const SpecLaunch launch =
         f8 ? (out_dtype == GEMM_F32    ? launch_gemm_f8_spec_f32
               : out_dtype == GEMM_BF16 ? launch_gemm_f8_spec_bf16
@@ -659,7 +659,7 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
                : (out_dtype == GEMM_F32    ? launch_gemm_spec_f32
                   : out_dtype == GEMM_BF16 ? launch_gemm_spec_bf16
                                            : launch_gemm_spec_f16);
-    e = launch(p.bn, pair, p.split_k, layout, sk, readc, mp, ka, p.grid, stream, dev);
+    e = launch(p.bn, pair, p.split_k, layout, sk, readc, epi, mp, ka, p.grid, stream, dev);
     if (e != cudaErrorNotSupported) return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
   switch (out_dtype) {

@@ -450,7 +450,8 @@ __device__ __forceinline__ unsigned int flag_acquire(const unsigned int* f) {
 
 
 // Specialised instances.  Most launches take the plain path: no C read (or,
-// with SPEC_READC, always a C read), no bias or activation, N * sizeof(out) a
+// with SPEC_READC, always a C read), no bias or activation (or, with SPEC_EPI,
+// the fused epilogue, its kinds chosen at run time), N * sizeof(out) a
 // multiple of 16 bytes, tiles in grouped order, no fault injection, and
 // data-parallel tiles only (or, with SPEC_STREAMK, a stream-K tail as well);
 // and each operand's major-ness is fixed by the call's layout.  Folding those parameters into constants drops
@@ -464,21 +465,26 @@ enum : int {
   SPEC_LAYOUT_SHIFT = 2,
   SPEC_STREAMK = 16,       // with SPEC_PLAIN: stream-K work stays a run-time choice
   SPEC_READC = 32,         // with SPEC_PLAIN: C is read (beta != 0)
+  SPEC_EPI = 64,           // with SPEC_PLAIN: a bias and/or an activation is applied
 };
 // the specialisation of a plain call with `layout` (stream-K work when sk, a C
-// read when readc)
-constexpr int spec_bits(int layout, bool sk, bool readc) {
+// read when readc, the fused epilogue when epi)
+constexpr int spec_bits(int layout, bool sk, bool readc, bool epi = false) {
   return SPEC_PLAIN | SPEC_LAYOUT | (layout << SPEC_LAYOUT_SHIFT) | (sk ? SPEC_STREAMK : 0) |
-         (readc ? SPEC_READC : 0);
+         (readc ? SPEC_READC : 0) | (epi ? SPEC_EPI : 0);
 }
 template <int SPEC, bool F8>
 __device__ __forceinline__ KernelArgs specialise_args(const KernelArgs& in) {
   KernelArgs a = in;
   if (SPEC & SPEC_PLAIN) {
     a.read_c = (SPEC & SPEC_READC) ? 1 : 0;
-    a.epi = 0;
-    a.bias_kind = EPI_BIAS_NONE;
-    a.act = EPI_ACT_NONE;
+    if (SPEC & SPEC_EPI) {
+      a.epi = 1;   // bias_kind and act stay run-time values
+    } else {
+      a.epi = 0;
+      a.bias_kind = EPI_BIAS_NONE;
+      a.act = EPI_ACT_NONE;
+    }
     a.n_ragged = 0;
     if (!(SPEC & SPEC_STREAMK)) a.sk_iters = 0;
     a.inject_skip = 0;

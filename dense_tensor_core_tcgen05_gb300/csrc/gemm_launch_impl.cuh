@@ -75,12 +75,12 @@ cudaError_t launch_inst(const OperandMaps& m, const KernelArgs& args, int grid,
 namespace {
 // The specialised instances of one layout in this unit's set (see spec_set).
 template <int LAYOUT>
-cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc,
+cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc, bool epi,
                                const OperandMaps& m, const KernelArgs& args, int grid,
                                cudaStream_t stream, int dev) {
   constexpr int S = spec_bits(LAYOUT, false, false);
 #if GEMM_SPEC_SET != 2
-  if (pair) {
+  if (pair && !epi) {
     if (sk) return launch_inst<256, true, 1, spec_bits(LAYOUT, true, false)>(m, args, grid, stream, dev);
     if (readc) return launch_inst<256, true, 1, spec_bits(LAYOUT, false, true)>(m, args, grid, stream, dev);
     return launch_inst<256, true, 1, S>(m, args, grid, stream, dev);
@@ -90,6 +90,11 @@ cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc
   if (split == 1 && bn == 64) return launch_inst<64, false, 1, S>(m, args, grid, stream, dev);
 #endif
 #if GEMM_SPEC_SET != 1
+  if (pair) {
+    constexpr int E = spec_bits(LAYOUT, false, false, true);
+    if (sk) return launch_inst<256, true, 1, spec_bits(LAYOUT, true, false, true)>(m, args, grid, stream, dev);
+    return launch_inst<256, true, 1, E>(m, args, grid, stream, dev);
+  }
   if (split == 1 && bn == 128) return launch_inst<128, false, 1, S>(m, args, grid, stream, dev);
   if (split == 4 && bn == 128) return launch_inst<128, false, 4, S>(m, args, grid, stream, dev);
   if (split == 4 && bn == 64) return launch_inst<64, false, 4, S>(m, args, grid, stream, dev);
@@ -100,19 +105,19 @@ cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc
 }  // namespace
 
 cudaError_t GEMM_LAUNCH_SPEC_NAME(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                  const OperandMaps& m, const KernelArgs& args, int grid,
+                                  bool epi, const OperandMaps& m, const KernelArgs& args, int grid,
                                   cudaStream_t stream, int dev) {
-  if (!spec_supported(bn, pair, split, layout, GEMM_F8, sk, readc)) return cudaErrorNotSupported;
-  if (GEMM_SPEC_SET != 0 && spec_set(bn, pair, split, sk, readc) != GEMM_SPEC_SET)
+  if (!spec_supported(bn, pair, split, layout, GEMM_F8, sk, readc, epi)) return cudaErrorNotSupported;
+  if (GEMM_SPEC_SET != 0 && spec_set(bn, pair, split, sk, readc, epi) != GEMM_SPEC_SET)
     return cudaErrorNotSupported;
   if constexpr (GEMM_F8) {   // 8-bit operands are K-major only
-    return launch_spec_layout<2>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
+    return launch_spec_layout<2>(bn, pair, split, sk, readc, epi, m, args, grid, stream, dev);
   } else {
     switch (layout) {
-      case 0: return launch_spec_layout<0>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
-      case 1: return launch_spec_layout<1>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
-      case 2: return launch_spec_layout<2>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
-      case 3: return launch_spec_layout<3>(bn, pair, split, sk, readc, m, args, grid, stream, dev);
+      case 0: return launch_spec_layout<0>(bn, pair, split, sk, readc, epi, m, args, grid, stream, dev);
+      case 1: return launch_spec_layout<1>(bn, pair, split, sk, readc, epi, m, args, grid, stream, dev);
+      case 2: return launch_spec_layout<2>(bn, pair, split, sk, readc, epi, m, args, grid, stream, dev);
+      case 3: return launch_spec_layout<3>(bn, pair, split, sk, readc, epi, m, args, grid, stream, dev);
       default: return cudaErrorNotSupported;
     }
   }

@@ -53,14 +53,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 // True once the phase with the given parity has completed.  CLUSTER selects
-// acquire semantics at cluster scope, for barriers another CTA arrives on.
+// acquire semantics at cluster scope, for barriers another CTA arrives on.  A
+// waiting thread may be suspended for up to 1 us (it resumes as soon as the
+// phase completes): fewer re-polls leave more issue slots to the producer and
+// MMA lanes that share the waiting warps' SM sub-partitions (4096^3 and 8192^3
+// about 0.5% faster than with the default limit).
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   if (CLUSTER) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, 1000;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -68,7 +72,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   } else {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)

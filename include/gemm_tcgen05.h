@@ -131,12 +131,13 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *             on the device per grid shape by the library (gemm_ex_noalloc
  *             always uses the grouped order).
  *   general   1: always launch the general kernel.  0 (the default): a call on
- *             the plain path -- no bias or activation, N times the output
- *             element size a multiple of 16 bytes, the grouped tile order --
- *             runs a kernel instance specialised for its layout when the
- *             plan's configuration has one: the 256-wide CTA pair (beta == 0
- *             with or without stream-K work, beta != 0 without it), and with
- *             beta == 0 and no stream-K work the single CTA of width 64 or
+ *             the plain path -- N times the output element size a multiple of
+ *             16 bytes, the grouped tile order -- runs a kernel instance
+ *             specialised for its layout when the plan's configuration has
+ *             one: the 256-wide CTA pair (beta == 0 with or without stream-K
+ *             work, with or without a bias or activation; beta != 0 without
+ *             stream-K work, bias or activation), and with beta == 0, no bias
+ *             or activation and no stream-K work the single CTA of width 64 or
  *             128 and the split-K clusters of 2 CTAs (width 64, 128 or 256)
  *             and of 4 CTAs (width 64 or 128).  Both kernels compute the same
  *             result bit for bit.  Other values: GEMM_ERR_INVALID_ARG. */

@@ -124,6 +124,30 @@ def test_specialised_beta(_lib, a_col, b_col, out_dtype):
                              a_col=a_col, b_col=b_col, beta=beta, C=C, exact=True)
 
 
+@pytest.mark.parametrize("a_col,b_col", LAYOUTS)
+@pytest.mark.parametrize("mode", [{"cta_group": 2, "bn": 256},
+                                  {"cta_group": 2, "bn": 256, "stream_k": 2}], ids=["dp", "streamk"])
+def test_specialised_fused_epilogue(_lib, a_col, b_col, mode):
+    """The CTA pair's fused-epilogue instances (bias per column or row, with and
+    without ReLU): exact on integers and identical to the general kernel."""
+    M, N, K = (520, 776, 456) if "stream_k" not in mode else (1032, 1288, 1000)
+    A, B = operands(M, N, K, "bf16", a_col, b_col, dist="int", seed=M + 3, pad=True)
+    rng = np.random.default_rng(N)
+    for kind in ("col", "row"):
+        bias = rng.integers(-40, 41, size=N if kind == "col" else M).astype(np.float32)
+        for relu in (False, True):
+            spec, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
+                                  a_col=a_col, b_col=b_col, cfg=mode, ldc=pad8(N), bias=bias,
+                                  bias_kind=kind, relu=relu)
+            gen, _ = run_library(A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
+                                 a_col=a_col, b_col=b_col, cfg=dict(mode, general=1), ldc=pad8(N),
+                                 bias=bias, bias_kind=kind, relu=relu)
+            np.testing.assert_array_equal(spec, gen)
+            check_against_oracle(spec, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
+                                 a_col=a_col, b_col=b_col, exact=True, bias=bias,
+                                 bias_kind=kind, relu=relu)
+
+
 def test_workload_2048_specialised(_lib):
     """The 2048^3 fp16 -> fp32 workload runs a specialised instance; same bits as
     the general kernel."""
