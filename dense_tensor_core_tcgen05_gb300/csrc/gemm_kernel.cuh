@@ -619,8 +619,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   };
   uint32_t producer_iters = 0;  // ring iterations armed (producer thread only)
 
-  // Start-up.  The lanes of warp 0 initialise the barriers (one each) and
-  // prefetch the tensor maps while warp 1 allocates TMEM.  The start-up barrier
+  // Start-up.  The lanes of warp 0 initialise the barriers (one each) while
+  // warp 1 allocates TMEM and warp 2 prefetches the tensor maps (on warp 0's
+  // path the prefetches delayed the first copy by ~0.4 us).  The start-up barrier
   // is split: warp 0 arrives, works out the producer's first work item and L2
   // policies, and waits only where it must (pair mode: the odd CTA's copies
   // signal the leader's barrier), so the first copies go out as soon as it opens.
@@ -633,16 +634,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bars + i, count);
     }
     if (lane == 0) *abort_flag = 0;
-    if (lane == 1) prefetch_tensormap(&tmA);
-    if (lane == 2) prefetch_tensormap(&tmB);
-    if (lane == 3 && args.a_full3d) prefetch_tensormap(&tmA3);
-    if (lane == 4 && args.b_full3d) prefetch_tensormap(&tmB3);
-    if (lane == 5) prefetch_tensormap(&tmC);
     fence_barrier_init();
     __syncwarp();
     // early split-K exchange: the peer's block is expected from the start; the
     // cluster barrier below orders this before the peer's copy
     if (EARLY && lane == 0) mbar_arrive_expect_tx(rfull, SLICE_BYTES);
+  }
+  if (warp == 2) {
+    if (lane == 0) prefetch_tensormap(&tmA);
+    if (lane == 1) prefetch_tensormap(&tmB);
+    if (lane == 2 && args.a_full3d) prefetch_tensormap(&tmA3);
+    if (lane == 3 && args.b_full3d) prefetch_tensormap(&tmB3);
+    if (lane == 4) prefetch_tensormap(&tmC);
   }
   if (warp == 1) {
     if (PAIR) {
