@@ -406,7 +406,13 @@ def test_device_checks_on_gpu(_lib):
 
 # ------------------------------------------------------------ bounded waits
 
-@pytest.mark.parametrize("mode", ALL_MODES, ids=MODE_IDS)
+# plus the two-CTA split-K clusters whose slices are exchanged early (each warp
+# sends its rows as soon as they are staged, and after an abort all the same)
+TIMEOUT_MODES = ALL_MODES + [{"split_k": 2, "bn": 128}, {"split_k": 2, "bn": 64}]
+TIMEOUT_IDS = MODE_IDS + ["splitk2-bn128-early", "splitk2-bn64-early"]
+
+
+@pytest.mark.parametrize("mode", TIMEOUT_MODES, ids=TIMEOUT_IDS)
 def test_wait_timeout_is_reported_and_context_survives(_lib, mode):
     """The producer leaves one ring slot unarmed (host-set debug flag): the MMA
     issuer's wait must run out, the kernel must record the timeout and return,
