@@ -12,6 +12,22 @@
 //    (64 elements, 8 rows, KO blocks, row groups) fetches the KO blocks of each
 //    group of 8 rows back to back, landing as the same 128B-swizzled K-major tile
 //    with 8-row atoms KO * 1024 B apart.  The L2 promotion of the map is a knob.
+//    Variant bits: 1 waits through a shared helper, 2 keeps the slot, k-group and
+//    row-block indices incrementally (the default divides by run-time values, which
+//    costs the single issuing thread ~0.3 us per copy and bounds the copy rate), 4
+//    runs the problem through the intake kernel instead; variant >> 8 adds KB of
+//    unused dynamic shared memory.
+//  * store_rate: every CTA writes a 128 x 256 fp32 block of C (the share of one CTA
+//    of a 256 x 256 pair tile) from registers, by one of five routes: tensor stores
+//    of 32 x 32 chunks through two staging buffers per warp (the GEMM epilogue),
+//    the same with a buffer per chunk, plain 16-byte global stores by row,
+//    coalesced 16-byte global stores through the swizzled staging buffer, or one
+//    3-D tensor store of the warp's whole 32 x 256 block -> the time the output
+//    of a one-wave GEMM takes to leave the SMs.
+//  * intake: an SM taking in L2-resident data by TMA copies (one thread, a ring of
+//    128-row x 2-block copies) and, at the same time, by cp.async 16-byte copies
+//    from up to 4 other warps -> whether a second load path adds to what TMA
+//    alone brings into an SM.
 // Every wait is bounded (1-2 s, %globaltimer); a CTA that gives up writes ~0.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -81,9 +97,16 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int iters, unsigned lo
   }
 }
 
-__global__ void __launch_bounds__(64, 1)
+__device__ bool probe_wait_fn(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait<false>(bar, parity))
+    if (globaltimer_ns() - t0 > 1000000000ull) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(160, 1)
     tma_stream_kernel(const __grid_constant__ CUtensorMap tm, int rows_per_cta, int R, int KO, int S,
-                      int K, int grouped, int reps, unsigned long long* out) {
+                      int K, int grouped, int reps, int variant, unsigned long long* out) {
   extern __shared__ uint8_t raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   const int box_bytes = R * 128 * KO;
@@ -97,9 +120,32 @@ __global__ void __launch_bounds__(64, 1)
   const int row0 = blockIdx.x * rows_per_cta;
   const int kgroups = K / (64 * KO), rblocks = rows_per_cta / R, pass = kgroups * rblocks;
   const int total = pass * reps;
+  int ns = 0, nkg = 0, nrb = 0, ws = 0;   // next slot, k-group, row block; slot waited for next
+  uint32_t wph = 0;                        // its phase parity
   const uint64_t t0 = globaltimer_ns();
   for (int i = 0; i < total + S; ++i) {
-    if (i >= S) {   // the copy issued S iterations ago must have landed before its slot is reused
+    if (i >= S && (variant & 2)) {   // the wait with incremental slot and parity
+      if (!probe_wait_fn(&bars[ws], wph)) {
+        const uint64_t g1 = globaltimer_ns();
+        while (globaltimer_ns() - g1 < 1000000ull) {
+        }
+        out[blockIdx.x] = ~0ull;
+        return;
+      }
+      if (++ws == S) {
+        ws = 0;
+        wph ^= 1;
+      }
+    } else if (i >= S && (variant & 1)) {   // the same wait through the shared helper
+      const int j = i - S;
+      if (!probe_wait_fn(&bars[j % S], (j / S) & 1)) {
+        const uint64_t g1 = globaltimer_ns();
+        while (globaltimer_ns() - g1 < 1000000ull) {
+        }
+        out[blockIdx.x] = ~0ull;
+        return;
+      }
+    } else if (i >= S) {   // the copy issued S iterations ago must have landed before its slot is reused
       const int j = i - S, s = j % S;
       const uint64_t g0 = globaltimer_ns();
       while (!mbar_try_wait(&bars[s], (j / S) & 1)) {
@@ -114,7 +160,21 @@ __global__ void __launch_bounds__(64, 1)
       }
     }
     if (i < total) {
-      const int s = i % S, kg = i % kgroups, rb = (i % pass) / kgroups;
+      int s, kg, rb;
+      if (variant & 2) {   // indices kept incrementally (no division by run-time values)
+        s = ns;
+        kg = nkg;
+        rb = nrb;
+        if (++ns == S) ns = 0;
+        if (++nkg == kgroups) {
+          nkg = 0;
+          if (++nrb == rblocks) nrb = 0;
+        }
+      } else {
+        s = i % S;
+        kg = i % kgroups;
+        rb = (i % pass) / kgroups;
+      }
       mbar_arrive_expect_tx(&bars[s], box_bytes);
       if (grouped)
         tma_load_4d(smem + s * box_bytes, &tm, 0, 0, kg * KO, (row0 + rb * R) / 8, &bars[s]);
@@ -232,6 +292,90 @@ __global__ void __launch_bounds__(64, 1)
   cluster_sync();
 }
 
+
+// ------------------------------------------------------------------- intake
+constexpr int CP_BUFS = 6;   // 4 KB cp.async buffers per warp (CP_BUFS - 1 rounds in flight)
+
+// Warp 0, lane 0: `tma_copies` copies of 128 rows x 2 blocks from rows
+// [128 g, 128 g + 128) of A ([rows, cols] bf16, L2-resident), g = b / share
+// (`share` consecutive CTAs read the same rows), walking the row's columns
+// cyclically, through S = 3 slots.  Warps 1..W: each re-reads its own 24 KB
+// slice of P `cp_iters` times 4 KB with cp.async.cg (16 B per lane and copy),
+// or with cp_iters < 0 reads its 24 KB of shared memory -cp_iters times 4 KB.
+// out[8 b] = TMA ns, out[8 b + w] = warp w's ns (~0 if the TMA thread gave up).
+__global__ void __launch_bounds__(160, 1)
+    intake_kernel(const __grid_constant__ CUtensorMap tm, int cols, int share, const uint8_t* P, int W,
+                  int tma_copies, int cp_iters, int bars_after_ring, unsigned long long* out) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  constexpr int S = 3, BOX = 128 * 128 * 2;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * BOX + (bars_after_ring ? 0 : 4 * CP_BUFS * 4096));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    if (lane != 0 || tma_copies == 0) return;
+    const int groups = cols / 128;   // copies per pass over the row's columns
+    const int y = (static_cast<int>(blockIdx.x) / share) * 128;
+    const uint64_t t0 = globaltimer_ns();
+    for (int i = 0; i < tma_copies + S; ++i) {
+      if (i >= S) {
+        const int j = i - S;
+        if (!probe_wait<false>(&bars[j % S], (j / S) & 1)) {
+          const uint64_t g1 = globaltimer_ns();
+          while (globaltimer_ns() - g1 < 1000000ull) {
+          }
+          out[8 * blockIdx.x] = ~0ull;
+          return;
+        }
+      }
+      if (i < tma_copies) {
+        const int s = i % S;
+        mbar_arrive_expect_tx(&bars[s], BOX);
+        tma_load_3d(smem + s * BOX, &tm, 0, y, (i % groups) * 2, &bars[s]);
+      }
+    }
+    out[8 * blockIdx.x] = globaltimer_ns() - t0;
+    return;
+  }
+  if (warp > W) return;
+  const uint8_t* src = P + (static_cast<size_t>(blockIdx.x) * 4 + (warp - 1)) * (CP_BUFS * 4096);
+  const uint32_t dst = smem_u32(smem + S * BOX + (warp - 1) * CP_BUFS * 4096);
+  const uint64_t t0 = globaltimer_ns();
+  if (cp_iters < 0) {
+    // shared-memory reads only: 16 bytes per lane and load over the warp's
+    // 24 KB, -cp_iters passes of 4 KB; the sum keeps the loads alive
+    uint32_t acc = 0;
+    for (int it = 0; it < -cp_iters; ++it) {
+      const int b = it % CP_BUFS;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 q = ld_shared_v4(dst + b * 4096 + (j * 32 + lane) * 16);
+        acc += q.x ^ q.y ^ q.z ^ q.w;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) out[8 * blockIdx.x + warp] = (globaltimer_ns() - t0) | (acc == 0x9e3779b9u ? 1ull : 0ull);
+    return;
+  }
+  for (int it = 0; it < cp_iters; ++it) {
+    const int b = it % CP_BUFS;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int off = b * 4096 + (j * 32 + lane) * 16;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + off), "l"(src + off) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group %0;" ::"n"(CP_BUFS - 1) : "memory");
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncwarp();
+  if (lane == 0) out[8 * blockIdx.x + warp] = globaltimer_ns() - t0;
+}
+
 template <int N, bool PAIR>
 int launch_mma(int grid, int iters, unsigned long long* dout) {
   auto k = mma_rate_kernel<N, PAIR>;
@@ -252,6 +396,101 @@ int launch_mma(int grid, int iters, unsigned long long* dout) {
   }
   if (cudaLaunchKernelEx(&cfg, k, iters, dout) != cudaSuccess) return -2;
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -3;
+}
+
+
+// ---------------------------------------------------------------- store_rate
+__device__ __forceinline__ void tma_store_3d_probe(const CUtensorMap* m, const void* src, int32_t x,
+                                                   int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4_probe(float* p, float a, float b, float c, float d) {
+  asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// 4 warps; warp w writes rows [32 w, 32 w + 32) of the CTA's 128 x 256 block,
+// as 8 chunks of 32 columns.  Element (r, c) of C holds 0.5 r + c.  out[5 b] =
+// start, out[5 b + 1 + w] = the time warp w's writes were complete.
+__global__ void __launch_bounds__(128, 1)
+    store_rate_kernel(const __grid_constant__ CUtensorMap tm2, const __grid_constant__ CUtensorMap tm3,
+                      float* C, int ldc, int grid_n, int mode, unsigned long long* out) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int row0 = (blockIdx.x / grid_n) * 128 + warp * 32;
+  const int col0 = (blockIdx.x % grid_n) * 256;
+  uint8_t* wbuf = smem + warp * 32768;
+  __syncthreads();
+  const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.5f * static_cast<float>(row0 + lane) + static_cast<float>(col0 + c * 32 + i);
+    if (mode == 2) {
+      float* dst = C + static_cast<size_t>(row0 + lane) * ldc + col0 + c * 32;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) st_global_v4_probe(dst + 4 * j, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      continue;
+    }
+    uint8_t* buf = wbuf + (mode == 0 ? (c & 1) : c) * 4096;
+    if (mode == 0) {
+      if (lane == 0) bulk_wait_group_read<1>();
+      __syncwarp();
+    }
+    const uint32_t rowp = smem_u32(buf) + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t a = rowp + ((j ^ (lane & 7)) << 4);
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v[4 * j]), "f"(v[4 * j + 1]),
+                   "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
+                   : "memory");
+    }
+    if (mode == 3) {
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = i * 4 + (lane >> 3), piece = lane & 7;
+        const uint4 q = ld_shared_v4(smem_u32(buf) + r * 128 + ((piece ^ (r & 7)) << 4));
+        st_global_v4_probe(C + static_cast<size_t>(row0 + r) * ldc + col0 + c * 32 + piece * 4,
+                           __uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z),
+                           __uint_as_float(q.w));
+      }
+      __syncwarp();
+      continue;
+    }
+    if (mode == 4) continue;   // stored at once after the loop
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&tm2, buf, col0 + c * 32, row0);
+      bulk_commit_group();
+    }
+  }
+  if (mode == 4) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d_probe(&tm3, wbuf, 0, row0, col0 / 32);
+      bulk_commit_group();
+    }
+  }
+  if (mode == 2 || mode == 3) {
+    __threadfence();
+  } else if (lane == 0) {
+    bulk_wait_group<0>();
+  }
+  __syncwarp();
+  const uint64_t t1 = globaltimer_ns();
+  if (lane == 0) {
+    if (warp == 0) out[5 * blockIdx.x] = t0;
+    out[5 * blockIdx.x + 1 + warp] = t1;
+  }
 }
 
 }  // namespace
@@ -277,7 +516,9 @@ extern "C" int probe_mma_rate(int n, int pair, int grid, int iters, unsigned lon
 // K % (64 * KO) == 0, (N / grid) % R == 0, R % 8 == 0, R <= 256, the ring within
 // 227 KB.  Returns 0 or a negative error.
 extern "C" int probe_tma_stream(const void* B, int N, int K, int grid, int R, int KO, int S,
-                                int grouped, int promo, int reps, unsigned long long* dout) {
+                                int grouped, int promo, int reps, int variant, int threads,
+                                unsigned long long* dout) {
+  if (threads != 64 && threads != 160) return -10;
   if (grid <= 0 || N % grid || (N / grid) % R || R > 256 || R % 8 || KO < 1 || K % (64 * KO) ||
       S < 1 || promo < 0 || promo > 3 || N % 8 || reps < 1)
     return -10;
@@ -305,12 +546,23 @@ extern "C" int probe_tma_stream(const void* B, int N, int K, int grid, int R, in
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, pr[promo],
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return -2;
-  const int smem = S * R * 128 * KO + 1024 + 8 * S + 64;
+  // variant >> 8: extra KB of dynamic shared memory (unused; sizes the carveout)
+  const int smem = S * R * 128 * KO + 1024 + 8 * S + 64 + (variant >> 8) * 1024;
   if (smem > 232448) return -12;
   if (cudaFuncSetAttribute(tma_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return -3;
-  tma_stream_kernel<<<grid, 64, smem>>>(tm, N / grid, R, KO, S, K, grouped, reps, dout);
+  if (variant & 4) {
+    // this map and problem through the intake kernel (R = 128, KO = 2, S = 3 only)
+    if (R != 128 || KO != 2 || S != 3 || grouped || N / grid != 128) return -13;
+    const int ismem = 3 * 32768 + 4 * CP_BUFS * 4096 + 1024 + 64;
+    if (cudaFuncSetAttribute(intake_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ismem) !=
+        cudaSuccess)
+      return -3;
+    intake_kernel<<<grid, 160, ismem>>>(tm, K, 1, nullptr, 0, reps * (K / 128), 0, 0, dout);
+  } else {
+    tma_stream_kernel<<<grid, threads, smem>>>(tm, N / grid, R, KO, S, K, grouped, reps, variant, dout);
+  }
   if (cudaGetLastError() != cudaSuccess) return -4;
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -5;
 }
@@ -364,5 +616,97 @@ extern "C" int probe_tma_mcast(const void* B, int N, int K, int grid, int R, int
                          dout) !=
       cudaSuccess)
     return -4;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -5;
+}
+
+// Start and per-warp completion times (globaltimer ns, 5 per CTA) of store_rate:
+// grid_m x grid_n CTAs each writing a 128 x 256 fp32 block of C ([M, N] row
+// major, ldc elements, base 16-byte aligned) by route `mode` (0..4, see top).
+// Requires grid_m * 128 <= M, grid_n * 256 <= N, ldc % 4 == 0.  Returns 0 or a
+// negative error.
+extern "C" int probe_store_rate(float* C, int M, int N, int ldc, int grid_m, int grid_n, int mode,
+                                unsigned long long* dout) {
+  if (mode < 0 || mode > 4 || grid_m < 1 || grid_n < 1 || grid_m * 128 > M || grid_n * 256 > N ||
+      ldc < N || ldc % 4 || (reinterpret_cast<uintptr_t>(C) & 15))
+    return -10;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return -1;
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  CUtensorMap tm2, tm3;
+  cuuint64_t dims2[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides2[1] = {static_cast<cuuint64_t>(ldc) * 4};
+  cuuint32_t box2[2] = {32, 32};
+  cuuint64_t dims3[3] = {32, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(N / 32)};
+  cuuint64_t strides3[2] = {static_cast<cuuint64_t>(ldc) * 4, 128};
+  cuuint32_t box3[3] = {32, 32, 8};
+  cuuint32_t es[3] = {1, 1, 1};
+  if (enc(&tm2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims2, strides2, box2, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return -2;
+  if (enc(&tm3, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, C, dims3, strides3, box3, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return -2;
+  const int smem = 4 * 32768 + 1024;
+  if (cudaFuncSetAttribute(store_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return -3;
+  store_rate_kernel<<<grid_m * grid_n, 128, smem>>>(tm2, tm3, C, ldc, grid_n, mode, dout);
+  if (cudaGetLastError() != cudaSuccess) return -4;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -5;
+}
+
+// Per-CTA nanoseconds of intake_kernel (8 per CTA: TMA, then cp.async warps
+// 1..W): grid CTAs; A [rows, cols] bf16 with cols % 128 == 0 and
+// rows >= 128 * ceil(grid / share); P at least grid * 4 * 24 KB, 16-byte
+// aligned.  tma_copies = 0 turns the TMA stream off, W = 0 the cp.async warps.
+// Returns 0 or a negative error.
+extern "C" int probe_intake(const void* A, int rows, int cols, int share, const void* P,
+                            long long p_bytes, int grid, int W, int tma_copies, int cp_iters,
+                            int bars_after_ring, unsigned long long* dout) {
+  // barriers right after the TMA ring overlap the cp.async buffers
+  if (W > 0 && bars_after_ring) return -10;
+  if (grid < 1 || share < 1 || cols < 128 || cols % 128 || rows < 128 * ((grid + share - 1) / share) ||
+      W < 0 || W > 4 || tma_copies < 0 ||
+      p_bytes < static_cast<long long>(grid) * 4 * CP_BUFS * 4096 || (reinterpret_cast<uintptr_t>(P) & 15))
+    return -10;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return -1;
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  CUtensorMap tm;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
+  cuuint32_t box[3] = {64, 128, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(A), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return -2;
+  const int smem = 3 * 32768 + 4 * CP_BUFS * 4096 + 1024 + 64;
+  if (cudaFuncSetAttribute(intake_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -3;
+  if (bars_after_ring == 2) {
+    // this map and problem through the streaming kernel (S = 3, one row block)
+    if (share != 1 || W != 0 || tma_copies % (cols / 128)) return -13;
+    const int ssmem = 3 * 32768 + 1024 + 24 + 64;
+    if (cudaFuncSetAttribute(tma_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ssmem) !=
+        cudaSuccess)
+      return -3;
+    tma_stream_kernel<<<grid, 64, ssmem>>>(tm, 128, 128, 2, 3, cols, 0, tma_copies / (cols / 128), 1,
+                                           dout);
+  } else {
+    intake_kernel<<<grid, 160, smem>>>(tm, cols, share, static_cast<const uint8_t*>(P), W, tma_copies,
+                                       cp_iters, bars_after_ring, dout);
+  }
+  if (cudaGetLastError() != cudaSuccess) return -4;
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -5;
 }
