@@ -565,7 +565,7 @@ def run_reference(args):
     import oracle
     cfg = WORKLOAD_BY_NAME[args.workload]
     w = si.workload_operands(cfg)
-    rows_per_step = 32 if w["M"] >= 32 else w["M"]
+    rows_per_step = 256 if w["M"] >= 256 else w["M"]
     run = lambda r0: oracle.gemm(w["A"], w["B"], M=w["M"], N=w["N"], K=w["K"],  # noqa: E731
                                  in_dtype=w["in_dtype"], out_dtype=w["out_dtype"],
                                  a_col=w["a_col"], b_col=w["b_col"], alpha=w["alpha"],
