@@ -280,11 +280,14 @@ __device__ __forceinline__ void finish_piece(float* x, uint4* p, const KernelArg
 // row, CHUNK columns from col0: v0 = columns 0..31, v1 = 32..63), before any of
 // it is stored: x = alpha*acc, + beta*c (c from the staged C chunk at rowp when
 // read_c), + bias, then ReLU (negative -> 0, NaN kept); written back into v0/v1.
-// With no store in between, the chunk's bias loads (the same addresses in every
-// lane) issue together, and the branches are taken once per chunk.
+// The bias was loaded before the accumulator was ready: with a column bias,
+// lane l holds columns l (cb0) and 32 + l (cb1) of the chunk (0 past N) and the
+// values go round by shuffle; with a row bias, rb is this thread's row's value.
+// The branches are taken once per chunk.
 template <int OUT, int CHUNK>
 __device__ __forceinline__ void fused_chunk(uint32_t* v0, uint32_t* v1, const uint8_t* rowp,
-                                            const KernelArgs& args, int col0, int grow, int r) {
+                                            const KernelArgs& args, float cb0, float cb1,
+                                            float rb, int r) {
   constexpr int E = OUT == OUT_F32 ? 4 : 8;
   float x[CHUNK];
 #pragma unroll
@@ -307,25 +310,11 @@ __device__ __forceinline__ void fused_chunk(uint32_t* v0, uint32_t* v1, const ui
     }
   }
   if (args.bias_kind == EPI_BIAS_COL) {
-    if (col0 + CHUNK <= args.N) {
-      const float4* b4 = reinterpret_cast<const float4*>(args.bias + col0);
 #pragma unroll
-      for (int q = 0; q < CHUNK / 4; ++q) {
-        const float4 b = __ldg(b4 + q);
-        x[4 * q + 0] += b.x;
-        x[4 * q + 1] += b.y;
-        x[4 * q + 2] += b.z;
-        x[4 * q + 3] += b.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < CHUNK; ++i)
-        if (col0 + i < args.N) x[i] += __ldg(args.bias + col0 + i);
-    }
+    for (int i = 0; i < CHUNK; ++i) x[i] += __shfl_sync(0xffffffffu, i < 32 ? cb0 : cb1, i & 31);
   } else if (args.bias_kind == EPI_BIAS_ROW) {
-    const float b = grow < args.M ? __ldg(args.bias + grow) : 0.0f;
 #pragma unroll
-    for (int i = 0; i < CHUNK; ++i) x[i] += b;
+    for (int i = 0; i < CHUNK; ++i) x[i] += rb;
   }
   if (args.act == EPI_ACT_RELU) {
 #pragma unroll
@@ -506,26 +495,25 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 }
 
 // Stage one output chunk row (this thread's row r, registers v0 = columns 0..31,
-// v1 = 32..63) as alpha * acc cast to the output format, into the swizzled
+// v1 = 32..63) as alpha * acc (SCALE) or as the finished values themselves
+// (!SCALE: bits kept as they are), cast to the output format, into the swizzled
 // staging row at shared address `row`: 16-byte piece j at (j ^ (r & 7)) * 16.
-template <int OUT>
+template <int OUT, bool SCALE = true>
 __device__ __forceinline__ void stage_chunk_scaled(const uint32_t* v0, const uint32_t* v1,
                                                    uint32_t row, float alpha, int r) {
+  auto f = [&](uint32_t w) { return SCALE ? __uint_as_float(w) * alpha : __uint_as_float(w); };
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     uint4 o;
     if (OUT == OUT_F32) {
       const uint32_t* s = v0 + 4 * j;
-      o = make_uint4(__float_as_uint(__uint_as_float(s[0]) * alpha),
-                     __float_as_uint(__uint_as_float(s[1]) * alpha),
-                     __float_as_uint(__uint_as_float(s[2]) * alpha),
-                     __float_as_uint(__uint_as_float(s[3]) * alpha));
+      o = SCALE ? make_uint4(__float_as_uint(f(s[0])), __float_as_uint(f(s[1])),
+                             __float_as_uint(f(s[2])), __float_as_uint(f(s[3])))
+                : make_uint4(s[0], s[1], s[2], s[3]);
     } else {
       const uint32_t* s = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
-      o = make_uint4(pack2(__uint_as_float(s[0]) * alpha, __uint_as_float(s[1]) * alpha, OUT),
-                     pack2(__uint_as_float(s[2]) * alpha, __uint_as_float(s[3]) * alpha, OUT),
-                     pack2(__uint_as_float(s[4]) * alpha, __uint_as_float(s[5]) * alpha, OUT),
-                     pack2(__uint_as_float(s[6]) * alpha, __uint_as_float(s[7]) * alpha, OUT));
+      o = make_uint4(pack2(f(s[0]), f(s[1]), OUT), pack2(f(s[2]), f(s[3]), OUT),
+                     pack2(f(s[4]), f(s[5]), OUT), pack2(f(s[6]), f(s[7]), OUT));
     }
     st_shared_v4(row + ((j ^ (r & 7)) << 4), o);
   }
@@ -885,6 +873,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* const pbar = pfull + ew * PSLOTS_MAX;
     uint32_t p_issued = 0, p_done = 0;
 
+    float tb[BN / 32] = {};   // the current tile's column bias (see the tile loop)
+    float trb = 0.0f;         // ... or this thread's row bias
     // Write one finished tile: TMEM -> registers (+ the later units' partial
     // sums, in unit order, when ADD) -> alpha * acc + beta * C -> output.
     // Returns false if a wait gave up.
@@ -969,8 +959,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         uint8_t* rowp = stg + r * SW;
-        if (FUSED) fused_chunk<OUT, CHUNK>(v0, v1, rowp, args, col0, row0 + r, r);
-        if (!FUSED && !ADD && !ragged && !args.read_c) {
+        if (FUSED) {
+          // this chunk's column-bias registers (static selects: no local memory)
+          float cb0 = 0.0f, cb1 = 0.0f;
+#pragma unroll
+          for (int q = 0; q < BN / 32; ++q) {
+            if (q == c * (CHUNK / 32)) cb0 = tb[q];
+            if (CHUNK == 64 && q == c * (CHUNK / 32) + 1) cb1 = tb[q];
+          }
+          fused_chunk<OUT, CHUNK>(v0, v1, rowp, args, cb0, cb1, trb, r);
+        }
+        if (FUSED && !ragged) {
+          // finished values (alpha, beta * C, bias and activation applied in
+          // registers): cast and staged by the same branch-free shared stores
+          stage_chunk_scaled<OUT, false>(v0, v1, smem_u32(rowp), 1.0f, r);
+        } else if (!FUSED && !ADD && !ragged && !args.read_c) {
           // the common case, branch-free: alpha * acc, cast, one 16-byte
           // shared store per piece (per-piece branches slowed the stores ~1.6x)
           stage_chunk_scaled<OUT>(v0, v1, smem_u32(rowp), args.alpha, r);
@@ -1003,13 +1006,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int buf = tl & 1;
       const uint32_t aph = (tl >> 1) & 1;
       if (args.epi) {
-        // the tile's bias into L1 while its mainloop runs (in bounds only)
+        // the tile's bias into registers while its mainloop runs: lane l holds
+        // column nb * BN + 32 q + l in tb[q] (0 past N), or its row's value
         if (args.bias_kind == EPI_BIAS_COL) {
-          const int c = nb * BN + lane * 32;   // one 128-byte line per lane
-          if (lane < BN / 32 && c < args.N) prefetch_l1(args.bias + c);
-        } else if (args.bias_kind == EPI_BIAS_ROW && lane == 0) {
-          const int rr = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32;
-          if (rr < args.M) prefetch_l1(args.bias + rr);
+#pragma unroll
+          for (int q = 0; q < BN / 32; ++q) {
+            const int c = nb * BN + q * 32 + lane;
+            tb[q] = c < args.N ? __ldg(args.bias + c) : 0.0f;
+          }
+        } else if (args.bias_kind == EPI_BIAS_ROW) {
+          const int rr = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32 + lane;
+          trb = rr < args.M ? __ldg(args.bias + rr) : 0.0f;
         }
       }
       if (!wait_warp<PAIR>(&tfull[buf], aph, abort_flag, args, SITE_EPI_TMEM_FULL)) {
