@@ -410,10 +410,26 @@ def time_cublas(w, a, b, steps, warmup, flush):
     return statistics.median([x.elapsed_time(y) for x, y in evs])
 
 
+def time_hot(launch, reps=20, warmup=3):
+    """Mean ms per launch of `reps` back-to-back launches inside one CUDA-event
+    pair, with no flush between them (operands warm in L2)."""
+    import torch
+    for _ in range(warmup):
+        launch()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        launch()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def run_suite(g, args, device, peaks, skip_cfg):
     """Every workload timed the same way (20 steps, 5 warm-ups), with the cuBLAS
     reference point beside ours; the headline workload is included again so its
-    cuBLAS time sits next to it."""
+    cuBLAS time sits next to it.  Tensor-bound workloads are also timed hot
+    (back-to-back launches), ours and cuBLAS's."""
     import torch
     res = {}
     flush = L2Flush(device)
@@ -437,6 +453,19 @@ def run_suite(g, args, device, peaks, skip_cfg):
                           "cublas_ms": cub_ms, "cublas_tflops": flops / (cub_ms * 1e-3) / 1e12,
                           "bias_relu_median_ms": statistics.median(ftimes),
                           "bias_relu_mean_over_plain_mean": statistics.mean(ftimes) / statistics.mean(times)}
+        if bound == "tensor":
+            # back-to-back launches ("hot": no flush in between), ours and cuBLAS's
+            try:
+                st = torch.cuda.current_stream(device)
+                bb = b.t() if w["b_col"] else b
+                hot = time_hot(lambda: g.matmul(a, b, c, alpha=w["alpha"], beta=w["beta"],
+                                                a_col=w["a_col"], b_col=w["b_col"],
+                                                stream=st.cuda_stream))
+                cub_hot = time_hot(lambda: torch.matmul(a, bb))
+                res[w["name"]].update({"hot_ms": hot, "hot_tflops": flops / (hot * 1e-3) / 1e12,
+                                       "cublas_hot_ms": cub_hot})
+            except Exception as e:  # reported, never fatal to the bench line
+                res[w["name"]]["hot_error"] = str(e)[:200]
         del a, b, c, c0
         torch.cuda.empty_cache()
     return res
