@@ -228,7 +228,7 @@ def time_gemm(g, w, a, b, c, c0, steps, warmup, stream, flush, **epilogue):
     import torch
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
-    st = torch.cuda.Stream(stream) if False else stream
+    st = stream
     with torch.cuda.stream(st):
         for i in range(warmup + steps):
             if c0 is not None:
