@@ -2,10 +2,11 @@
 """Benchmark of the tcgen05 GEMM library (one JSON line on stdout, rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-suite]
+                    [--workload NAME] [--no-suite] [--no-cpu] [--detail]
 
 A step is one GEMM C <- alpha*A*B + beta*C of the chosen workload (default: the
-2048^3 fp16 -> fp32 workload) with operands already resident in HBM.  Between
+largest one, 8192^3 bf16 -> fp32 with A row-major, B column-major and beta = 0.5
+reading an fp32 C) with operands already resident in HBM.  Between
 timed steps L2 is flushed by writing a buffer larger than L2 and then reading it
 back (so L2 holds clean lines of the flush buffer, not dirty ones whose write-back
 would be charged to the next step), and only the GEMM launch is inside each
@@ -16,8 +17,11 @@ Besides value and ms_per_step the line carries: the roofline of the GEMM kernel
 (achieved TFLOP/s or GB/s against the measured peak), the end-to-end rate through
 the host-buffer entry point gemm_host (pinned host operands, copies included),
 the CPU oracle timed on the host cores on a bounded sample, SM clocks sampled
-during the timed region, and a "suite" with the other workloads (4096^3 bf16,
-8192^3 bf16 beta, 128x8192x8192 skinny, 512^3).
+during the timed region, and compact summaries of every workload (512^3,
+2048^3, 4096^3, 8192^3 and the 128x8192x8192 skinny shape, each beside cuBLAS),
+of the odd and tail shapes and of the FP8 shapes, placed at the end of the line
+so that a reader keeping only its tail still has them (--detail adds the full
+per-workload records).
 
 --impl reference times the CPU oracle (the plain FP64 triple loop) on the same
 workload, one bounded row sample per step, on the host cores.
@@ -46,7 +50,7 @@ import numpy as np  # noqa: E402
 import seeded_inputs as si  # noqa: E402
 
 WORKLOAD_BY_NAME = {w["name"]: k for k, w in si.WORKLOADS.items()}
-DEFAULT_WORKLOAD = si.WORKLOADS[2]["name"]
+DEFAULT_WORKLOAD = si.WORKLOADS[4]["name"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20    # > 129 MB L2
 CSRC = os.path.join(ROOT, "dense_tensor_core_tcgen05_gb300", "csrc")
@@ -381,14 +385,44 @@ def run_ours(args, rank, world, device):
         out["e2e"] = {"value": flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                       "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "entry_point": "gemm_host (pinned host operands)"}
-        if not args.no_suite:
-            out["suite"] = run_suite(g, args, device, peaks, cfg)
-            out["odd_tail"] = run_odd_tail(g, device, peaks)
-            out["fp8"] = run_fp8(g, device, peaks)
         if not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline(w)
         out["kernel_hash"] = kernel_source_hash()
+        if not args.no_suite:
+            suite = run_suite(g, args, device, peaks, cfg)
+            odd = run_odd_tail(g, device, peaks)
+            fp8 = run_fp8(g, device, peaks)
+            if args.detail:
+                out.update(suite=suite, odd_tail=odd, fp8=fp8)
+            # compact summaries last: a reader that keeps only the line's tail has them
+            out.update(summarise(suite, odd, fp8))
     return out
+
+
+def _r(x, nd=4):
+    return None if x is None else float(f"{x:.{nd}g}")
+
+
+def summarise(suite, odd, fp8):
+    """Short per-workload records (microseconds, fractions of the measured peaks)."""
+    cols = {"suite_cols": "ours_us, frac (tensor or HBM, of measured), bound, cuBLAS_us, "
+                          "ours_hot_us, cuBLAS_hot_us, bias_relu_us",
+            "suite_summary": {}, "odd_tail_cols": "ours_us, frac_hbm, cuBLAS_us",
+            "odd_tail_summary": {}, "fp8_cols": "ours_us, frac (of 2x measured bf16), cuBLASLt_us",
+            "fp8_summary": {}}
+    for name, r in suite.items():
+        cols["suite_summary"][name] = [
+            _r(r["median_ms"] * 1e3), _r(r["frac"], 3), r["bound"], _r(r["cublas_ms"] * 1e3),
+            _r(r.get("hot_ms", 0) * 1e3) if "hot_ms" in r else None,
+            _r(r.get("cublas_hot_ms", 0) * 1e3) if "cublas_hot_ms" in r else None,
+            _r(r["bias_relu_median_ms"] * 1e3)]
+    for name, r in odd.items():
+        cols["odd_tail_summary"][name] = [_r(r["median_ms"] * 1e3), _r(r["frac_hbm"], 3),
+                                          _r(r["cublas_ms"] * 1e3)]
+    for name, r in fp8.items():
+        cols["fp8_summary"][name] = [_r(r["median_ms"] * 1e3), _r(r["frac"], 3),
+                                     _r(r["cublaslt_ms"] * 1e3) if r.get("cublaslt_ms") else None]
+    return cols
 
 
 def time_cublas(w, a, b, steps, warmup, flush):
@@ -633,6 +667,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_BY_NAME))
     ap.add_argument("--no-suite", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--detail", action="store_true",
+                    help="add the full per-workload suite, odd-tail and FP8 records")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

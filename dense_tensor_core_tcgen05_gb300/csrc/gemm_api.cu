@@ -133,8 +133,11 @@ std::mutex g_noalloc_mu;
 // Set-up, once per device with that device current: the array's device
 // address.  The flags are cleared on the stream of the first launch that uses
 // them (and again when the epoch wraps), then every launch takes the next epoch.
-gemm_status_t noalloc_scratch(int dev, cudaStream_t st, size_t need, float** ws,
+gemm_status_t noalloc_scratch(int dev, cudaStream_t st, size_t slot_bytes, int ctas, float** ws,
                               unsigned int** flags, unsigned int* epoch) {
+  // the flag region holds kMaxSkCtas flags: a wider grid would index past it
+  if (ctas > kMaxSkCtas) return GEMM_ERR_INVALID_ARG;
+  const size_t need = kFlagBytes + slot_bytes * static_cast<size_t>(ctas);
   if (need > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH;
   NoAllocScratch& n = g_noalloc[dev];
   std::call_once(n.once, [&n]() {
@@ -631,7 +634,7 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
     if (s != GEMM_OK) return s;
   }
   if (p.sk_iters) {
-    s = fixed_scratch ? noalloc_scratch(dev, stream, static_cast<size_t>(p.scratch_bytes), &ka.ws,
+    s = fixed_scratch ? noalloc_scratch(dev, stream, size_t(BM) * p.bn * 4, p.grid, &ka.ws,
                                         &ka.ws_flags, &ka.epoch)
                       : scratch_for(dev, stream, size_t(BM) * p.bn * 4, p.grid, &ka.ws,
                                     &ka.ws_flags, &ka.epoch);

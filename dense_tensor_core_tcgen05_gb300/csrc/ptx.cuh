@@ -129,20 +129,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, int
       : "memory");
 }
 
-// 3-D tiled load multicast to the CTAs of the cluster named in `cta_mask`: the
-// box lands at the same shared-memory offset in each of them and its bytes are
-// counted on the mbarrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_3d_mcast(void* dst, const CUtensorMap* m, int32_t x,
-                                                  int32_t y, int32_t z, uint64_t* bar,
-                                                  uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
-      "h"(cta_mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m, int32_t x,
                                                  int32_t y, int32_t z, uint64_t* bar,
                                                  uint64_t policy) {

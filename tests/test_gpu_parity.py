@@ -131,6 +131,30 @@ def test_workload5_skinny_integer_each_mode(mode):
     _check_w(w, out, exact=True)
 
 
+def _check_w_blocks(w, out, exact=False, block=1024):
+    """Every element, in blocks of rows (bounded host memory for the oracle's
+    binary64 results at 8192^3)."""
+    for r0 in range(0, w["M"], block):
+        _check_w(w, out, rows=list(range(r0, min(w["M"], r0 + block))), exact=exact)
+
+
+def test_workload4_integer_bit_exact_full():
+    """8192^3 bf16 -> fp32 with beta = 0.5 on integer inputs (C_in integer too, so
+    beta * c is exact): every element equals the oracle's bits."""
+    w = _workload(4, integer=True)
+    out, _ = _run_w(w)
+    _check_w_blocks(w, out, exact=True)
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+def test_workload_normal_tolerance_full(cfg):
+    """4096^3 bf16 -> bf16 and 8192^3 bf16 -> fp32 (beta 0.5) on their normal
+    draws: every element within the error bound of its output format."""
+    w = _workload(cfg, integer=False)
+    out, _ = _run_w(w)
+    _check_w_blocks(w, out)
+
+
 def test_workload4_integer_bit_exact_sampled():
     w = _workload(4, integer=True)
     out, _ = _run_w(w)
