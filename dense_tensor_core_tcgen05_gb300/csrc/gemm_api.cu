@@ -629,6 +629,9 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.act = act;
   ka.epi = (bias_kind != GEMM_BIAS_NONE || act != GEMM_ACT_NONE) ? 1 : 0;
   ka.tile_map = nullptr;
+  // beta * C goes into the accumulator ahead of the MMAs (persistent launches
+  // with alpha == 1; a split-K cluster's CTAs each hold only part of the sum)
+  ka.pre_c = (alpha == 1.0f && beta != 0.0f && p.split_k == 1) ? 1 : 0;
   if (p.order == GEMM_ORDER_HILBERT && !fixed_scratch) {   // the fixed-scratch path allocates nothing
     s = hilbert_map_for(dev, p.m_tiles, p.n_tiles, &ka.tile_map);
     if (s != GEMM_OK) return s;

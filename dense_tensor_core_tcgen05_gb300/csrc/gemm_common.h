@@ -201,7 +201,18 @@ struct KernelArgs {
   // Tile order: NULL = grouped (tile_coord), else (m block, n block) of tile t
   // in Hilbert-curve order, num_tiles entries.
   const int2* tile_map;
+  // 1: beta * C is written into a tile's TMEM accumulator before its first MMA
+  // (alpha == 1 only, so the accumulator then holds alpha*AB + beta*C), for every
+  // work item after a unit's first two that holds its tile's first k-groups.
+  int pre_c;
 };
+
+// Whether work item number `tl` of a unit (item `w`) starts from an accumulator
+// holding beta * C rather than zero (see KernelArgs::pre_c).  The MMA issuer and
+// the epilogue warps evaluate it on the same item sequence.
+GEMM_HD bool item_preloads_c(const KernelArgs& a, uint32_t tl, const WorkItem& w) {
+  return a.pre_c && a.read_c && tl >= 2 && w.g0 == 0;
+}
 
 #if defined(__CUDACC__)
 // Output block (m_blk, n_blk) of tile index t in the launch's tile order.

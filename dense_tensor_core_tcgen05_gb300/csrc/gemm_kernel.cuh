@@ -85,9 +85,9 @@ struct SmemLayout {
   static constexpr int RING_BYTES = off_epi;
   static constexpr int PWARP_BYTES = RING_BYTES / EPI_WARPS;
   // full[STAGES], empty[STAGES], tfull[2], tempty[2], cload[EPI_WARPS*EPI_BUFS], drain, esync,
-  // pfull[EPI_WARPS*PSLOTS_MAX], rfull
+  // pfull[EPI_WARPS*PSLOTS_MAX], rfull, pfb[EPI_WARPS]
   static constexpr int NUM_BARS =
-      2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 2 + EPI_WARPS * PSLOTS_MAX + 1;
+      2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 2 + EPI_WARPS * PSLOTS_MAX + 1 + EPI_WARPS;
   static constexpr int off_tmem = off_bar + NUM_BARS * 8;
   static constexpr int off_flag = off_tmem + 8;
   static constexpr int BYTES = off_flag + 8;
@@ -239,7 +239,7 @@ __device__ __forceinline__ void bias_act(float* x, const EpiBias& b, int pc) {
 
 // One 16-byte piece of an output row: x holds its accumulator values (4 for
 // fp32 output, 8 for 16-bit output, alpha not yet applied).  Applies
-// alpha*acc + beta*c (c read from the staged C chunk at p when read_c), then
+// alpha*acc + beta*c (c read from the staged C chunk at p when rc), then
 // (FUSED) the bias and activation, casts, and either writes the piece to the
 // swizzled staging buffer (p) or, for a chunk crossing the ragged right edge of
 // C, stores its in-range elements straight to global memory.
@@ -248,14 +248,14 @@ __device__ __forceinline__ void store_piece(const float* x, uint4* p, const Kern
                                             bool ragged, bool store_row, int grow, int gcol);
 
 template <int OUT, bool FUSED = false>
-__device__ __forceinline__ void finish_piece(float* x, uint4* p, const KernelArgs& args,
+__device__ __forceinline__ void finish_piece(float* x, uint4* p, const KernelArgs& args, bool rc,
                                              bool ragged, bool store_row, int grow, int gcol,
                                              const EpiBias& eb = EpiBias{0.0f, 0.0f, 0.0f, 0.0f},
                                              int pc = 0) {
   constexpr int E = OUT == OUT_F32 ? 4 : 8;
 #pragma unroll
   for (int e = 0; e < E; ++e) x[e] *= args.alpha;
-  if (args.read_c) {
+  if (rc) {
     const uint4 ci = *p;
     if (OUT == OUT_F32) {
       x[0] = fmaf(args.beta, __uint_as_float(ci.x), x[0]);
@@ -279,20 +279,20 @@ __device__ __forceinline__ void finish_piece(float* x, uint4* p, const KernelArg
 // The fused epilogue on a whole output chunk held in registers (this thread's
 // row, CHUNK columns from col0: v0 = columns 0..31, v1 = 32..63), before any of
 // it is stored: x = alpha*acc, + beta*c (c from the staged C chunk at rowp when
-// read_c), + bias, then ReLU (negative -> 0, NaN kept); written back into v0/v1.
+// rc), + bias, then ReLU (negative -> 0, NaN kept); written back into v0/v1.
 // The bias was loaded before the accumulator was ready: with a column bias,
 // lane l holds columns l (cb0) and 32 + l (cb1) of the chunk (0 past N) and the
 // values go round by shuffle; with a row bias, rb is this thread's row's value.
 // The branches are taken once per chunk.
 template <int OUT, int CHUNK>
 __device__ __forceinline__ void fused_chunk(uint32_t* v0, uint32_t* v1, const uint8_t* rowp,
-                                            const KernelArgs& args, float cb0, float cb1,
+                                            const KernelArgs& args, bool rc, float cb0, float cb1,
                                             float rb, int r) {
   constexpr int E = OUT == OUT_F32 ? 4 : 8;
   float x[CHUNK];
 #pragma unroll
   for (int i = 0; i < CHUNK; ++i) x[i] = __uint_as_float(i < 32 ? v0[i] : v1[i - 32]) * args.alpha;
-  if (args.read_c) {
+  if (rc) {
 #pragma unroll
     for (int j = 0; j < CHUNK / E; ++j) {
       const uint4 ci = *reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4));
@@ -372,18 +372,19 @@ struct EpiState {
 };
 
 // Prepare the next staging buffer for an output chunk at (row0, col0): wait
-// until the store that last read it has finished, and when beta != 0 fetch the
-// C chunk into it.  Returns false if a wait gave up.
+// until the store that last read it has finished, and when rc (beta != 0 and C
+// not already in the accumulator) fetch the C chunk into it.  Returns false if
+// a wait gave up.
 template <bool CLUSTER, int EPI_BUF_BYTES>
 __device__ __forceinline__ bool begin_chunk(EpiState& st, uint8_t*& stg, const CUtensorMap* tmC,
                                             int row0, int col0, volatile int* abort_flag,
-                                            const KernelArgs& args) {
+                                            const KernelArgs& args, bool rc) {
   const int lane = threadIdx.x & 31;
   const int sbuf = st.chunk_ctr & 1;
   stg = st.stage0 + sbuf * EPI_BUF_BYTES;
   if (lane == 0) bulk_wait_group_read<1>();
   __syncwarp();
-  if (args.read_c) {
+  if (rc) {
     uint64_t* cb = &st.cload[sbuf];
     const uint32_t cph = (st.chunk_ctr >> 1) & 1;
     if (lane == 0) {
@@ -519,6 +520,58 @@ __device__ __forceinline__ void stage_chunk_scaled(const uint32_t* v0, const uin
   }
 }
 
+// beta * C[grow][col0 .. col0 + 32) as fp32 bits (0 outside C), read with plain
+// loads: the initial accumulator value of a tile whose C term is added by the
+// MMAs.  Rows are 16-byte aligned (ldc times the element size is a multiple of
+// 16) and col0 is a multiple of 32.
+template <int OUT>
+__device__ __forceinline__ void load_c32(const KernelArgs& a, int grow, int col0, uint32_t (&v)[32]) {
+  if (grow >= a.M || col0 >= a.N) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = 0u;
+    return;
+  }
+  const bool full = col0 + 32 <= a.N;
+  if (OUT == OUT_F32) {
+    const float* src = static_cast<const float*>(a.c_ptr) + static_cast<long long>(grow) * a.ldc + col0;
+    if (full) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 f = reinterpret_cast<const float4*>(src)[j];
+        v[4 * j] = __float_as_uint(a.beta * f.x);
+        v[4 * j + 1] = __float_as_uint(a.beta * f.y);
+        v[4 * j + 2] = __float_as_uint(a.beta * f.z);
+        v[4 * j + 3] = __float_as_uint(a.beta * f.w);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = col0 + e < a.N ? __float_as_uint(a.beta * src[e]) : 0u;
+    }
+  } else {
+    const uint16_t* src =
+        static_cast<const uint16_t*>(a.c_ptr) + static_cast<long long>(grow) * a.ldc + col0;
+    if (full) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 w = reinterpret_cast<const uint4*>(src)[j];
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack2(ws[e], OUT);
+          v[8 * j + 2 * e] = __float_as_uint(a.beta * f.x);
+          v[8 * j + 2 * e + 1] = __float_as_uint(a.beta * f.y);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float f = col0 + e < a.N ? unpack2(src[e], OUT).x : 0.0f;
+        v[e] = __float_as_uint(a.beta * f);
+      }
+    }
+  }
+}
+
 // PAIR: two CTAs per 256-row tile (cta_group::2).  SPLIT > 1: a cluster of
 // SPLIT CTAs shares one 128-row tile, each accumulating 1/SPLIT of the K range;
 // the partial sums meet in distributed shared memory (split-K without a global
@@ -575,6 +628,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* esync = drain + 1;   // rendezvous of the four epilogue warps (stream-K hand-off)
   uint64_t* pfull = esync + 1;   // stream-K partial staging slots, PSLOTS_MAX per epilogue warp
   uint64_t* rfull = pfull + EPI_WARPS * PSLOTS_MAX;   // split-K: the peers' slices have landed
+  // stream-K owner: the single later unit's partial of epilogue warp q's rows,
+  // prefetched into the draining ring by the producer lane, has landed (pfb[q])
+  uint64_t* pfb = rfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_tmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_flag);
 
@@ -605,7 +661,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto work_begin = [&](WorkIter& wi) {
     wi.init(unit0, unit_stride, args.dp_tiles, args.sk_iters, args.groups);
   };
+  // Stream-K owner segment with a single later unit: where epilogue warp q's
+  // share of that unit's partial (32 rows x BN fp32) lands in the draining ring,
+  // given the producer's ring iteration count at the end: the A and B parts of
+  // the first slot to drain after its last copy (warps 0 and 1), then of the
+  // second (warps 2 and 3).
+  static_assert(EPI_ROWS * BN * 4 <= L::A_BYTES && EPI_ROWS * BN * 4 <= L::B_BYTES,
+                "a warp's partial must fit a ring slot's operand part");
+  auto sk_prefetch_dst = [&](uint32_t it_end, int q) -> uint8_t* {
+    const int s = static_cast<int>((it_end + static_cast<uint32_t>(q >> 1)) % STAGES);
+    return (q & 1) ? smem + L::off_b + s * L::B_BYTES : smem + L::off_a + s * L::A_BYTES;
+  };
   uint32_t producer_iters = 0;  // ring iterations armed (producer thread only)
+  int pf_issued = 0;            // partial prefetch copies issued (producer thread only)
 
   // Start-up.  The lanes of warp 0 initialise the barriers (one each) while
   // warp 1 allocates TMEM and warp 2 prefetches the tensor maps (on warp 0's
@@ -685,6 +753,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------ TMA producer
       uint32_t it = 0;
       bool ok = true;
+      const bool any_item = have;
       while (ok && have) {
         int kb_begin, kb_end;
         kb_range(w, &kb_begin, &kb_end);
@@ -755,6 +824,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (have) tile_of(args, w.tile, &mb, &nb);
       }
       producer_iters = it;
+      // Stream-K owner segment with a single later unit (always the unit's last
+      // item): wait for that unit's flag, then fetch its partial into the first
+      // two ring slots to drain (sk_prefetch_dst), so the epilogue finds it in
+      // shared memory when the accumulator is complete.
+      if (ok && any_item && args.sk_iters != 0 && w.g0 == 0 && w.g1 < args.groups) {
+        const long long base = static_cast<long long>(w.tile - args.dp_tiles) * args.groups;
+        const int c0 = unit0 + 1;
+        const int c1 = sk_unit_of(base + args.groups - 1, unit_stride, args.sk_iters) + 1;
+        if (c1 - c0 == 1) {
+          const unsigned int* f = args.ws_flags + c0 * UNIT_CTAS + rank;
+          const uint64_t t0 = globaltimer_ns();
+          bool ready = true;
+          while (flag_acquire(f) != args.epoch) {
+            __nanosleep(64);
+            if (*abort_flag) {
+              ready = false;
+              break;
+            }
+            if (globaltimer_ns() - t0 > args.timeout_ns) {
+              record_error(args.status, SITE_STREAMK_FLAG);
+              *abort_flag = 1;
+              ready = false;
+              break;
+            }
+          }
+          if (ready) {
+            fence_proxy_async_global();   // the partial was published by another CTA
+            const uint64_t pol = policy_evict_first();
+            constexpr uint32_t PBYTES = EPI_ROWS * BN * 4;
+            const float* src0 = args.ws + static_cast<size_t>(c0 * UNIT_CTAS + rank) * BM * BN;
+            for (int q = 0; q < EPI_WARPS; ++q) {
+              // the slot of ring iteration it + q/2, once its last MMAs have completed
+              const uint32_t j = it + static_cast<uint32_t>(q >> 1);
+              if ((q & 1) == 0 && !wait_one<PAIR>(&empty[j % STAGES], ((j / STAGES) & 1) ^ 1,
+                                                  abort_flag, args, SITE_PRODUCER_EMPTY))
+                break;
+              const int quarter_q = (q + EPI_WARP0) & 3;   // the TMEM lane quarter of warp q
+              mbar_arrive_expect_tx(&pfb[q], PBYTES);
+              bulk_load_g2s(sk_prefetch_dst(it, q), src0 + static_cast<size_t>(quarter_q) * BN * EPI_ROWS,
+                            PBYTES, &pfb[q], pol);
+              pf_issued = q + 1;
+            }
+          }
+        }
+      }
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -778,6 +892,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         kb_range(w, &kb_begin, &kb_end);
         const int buf = tl & 1;
         const uint32_t aph = (tl >> 1) & 1;
+        // the epilogue warps may have written beta * C into the accumulator
+        const bool pre = item_preloads_c(args, tl, w);
         if (!wait_one<PAIR>(&tempty[buf], aph ^ 1, abort_flag, args, SITE_MMA_TMEM_EMPTY)) {
           ok = false;
           break;
@@ -804,7 +920,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               for (int kk = 0; kk < BK / UMMA_K; ++kk) {   // 4 x 32 bytes of each row
                 const uint64_t da = da0 + static_cast<uint64_t>(kk) * a_step;
                 const uint64_t db = db0 + static_cast<uint64_t>(kk) * b_step;
-                const uint32_t acc = (kb0 != kb_begin || j != 0 || kk != 0) ? 1u : 0u;
+                const uint32_t acc = (pre || kb0 != kb_begin || j != 0 || kk != 0) ? 1u : 0u;
                 if (F8) {
                   if (PAIR)
                     umma_f8_pair(d_tmem, da, db, args.idesc, acc);
@@ -876,14 +992,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     float tb[BN / 32] = {};   // the current tile's column bias (see the tile loop)
     float trb = 0.0f;         // ... or this thread's row bias
     // Write one finished tile: TMEM -> registers (+ the later units' partial
-    // sums, in unit order, when ADD) -> alpha * acc + beta * C -> output.
-    // Returns false if a wait gave up.
-    auto store_tile = [&](auto add_tag, auto fused_tag, uint32_t t_row, int nb,
-                          int row0, int buf, int contrib0, int ncontrib) -> bool {
+    // sums, in unit order, when ADD) -> alpha * acc + beta * C (C read here when
+    // rc) -> output.  hold: the accumulator is not handed back here (the caller
+    // first writes the next item's initial value into it).  pf_addr (nonzero):
+    // the single later unit's partial of this warp's rows was prefetched by the
+    // producer lane to this shared address, [BN/4 pieces][32 rows][16 B], its
+    // arrival signalled on pfb[ew].  Returns false if a wait gave up.
+    auto store_tile = [&](auto add_tag, auto fused_tag, uint32_t t_row, int nb, int row0, int buf,
+                          int contrib0, int ncontrib, bool rc, bool hold,
+                          uint32_t pf_addr) -> bool {
       constexpr bool ADD = decltype(add_tag)::value;
       constexpr bool FUSED = decltype(fused_tag)::value;   // bias / activation
       const uint32_t first = p_issued;
-      const uint32_t total = ADD ? static_cast<uint32_t>(CHUNKS * ncontrib) : 0u;
+      const uint32_t total = (ADD && !pf_addr) ? static_cast<uint32_t>(CHUNKS * ncontrib) : 0u;
       uint64_t pol = 0;
       // issue copies until number `upto`; copy n = first + c * ncontrib + k
       // holds chunk c of contributing unit contrib0 + k
@@ -901,7 +1022,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           bulk_load_g2s(pstage + (p_issued % PSLOTS) * PART_BYTES, src, PART_BYTES, b, pol);
         }
       };
-      if (ADD) {
+      if (ADD && !pf_addr) {
         if (lane == 0) {
           pol = policy_evict_first();
           fence_proxy_async_global();   // the partials were published by other CTAs
@@ -912,7 +1033,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int c = 0; c < CHUNKS; ++c) {
         const int col0 = nb * BN + c * CHUNK;
         uint8_t* stg;
-        if (!begin_chunk<PAIR, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args))
+        if (!begin_chunk<PAIR, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args, rc))
           return false;
         // A chunk that crosses the right edge of C when N * sizeof(out) is not a
         // multiple of 16 bytes is written with predicated plain stores: the
@@ -924,7 +1045,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_ld_32x32b_x32(t_row, v0, c * CHUNK);
         if (CHUNK == 64) tmem_ld_32x32b_x32(t_row, v1, c * CHUNK + 32);
         tmem_ld_wait();
-        if (c == CHUNKS - 1) {
+        if (c == CHUNKS - 1 && !hold) {
           // accumulator fully read: hand it back to the MMA issuer
           tc_fence_before();
           __syncwarp();
@@ -935,7 +1056,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               mbar_arrive_cluster(map_to_rank(&tempty[buf], 0));
           }
         }
-        if (ADD) {
+        if (ADD && pf_addr) {
+          if (c == 0 && !wait_warp(&pfb[ew], 0, abort_flag, args, SITE_STREAMK_FLAG)) return false;
+          // piece P = c * CHUNK / 4 + q of row r at (P * 32 + r) * 16
+          const uint32_t pb = pf_addr + static_cast<uint32_t>((c * (CHUNK / 4) * EPI_ROWS + r) * 16);
+#pragma unroll
+          for (int q = 0; q < CHUNK / 4; ++q) {
+            const uint4 pv = ld_shared_v4(pb + q * EPI_ROWS * 16);
+            uint32_t* a = q < 8 ? v0 + 4 * q : v1 + 4 * (q - 8);
+            a[0] = __float_as_uint(__uint_as_float(a[0]) + __uint_as_float(pv.x));
+            a[1] = __float_as_uint(__uint_as_float(a[1]) + __uint_as_float(pv.y));
+            a[2] = __float_as_uint(__uint_as_float(a[2]) + __uint_as_float(pv.z));
+            a[3] = __float_as_uint(__uint_as_float(a[3]) + __uint_as_float(pv.w));
+          }
+        } else if (ADD) {
           for (int k = 0; k < ncontrib; ++k) {
             const uint32_t n = first + static_cast<uint32_t>(c * ncontrib + k);
             if (!wait_warp(&pbar[n % PSLOTS], (n / PSLOTS) & 1, abort_flag, args,
@@ -967,13 +1101,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (q == c * (CHUNK / 32)) cb0 = tb[q];
             if (CHUNK == 64 && q == c * (CHUNK / 32) + 1) cb1 = tb[q];
           }
-          fused_chunk<OUT, CHUNK>(v0, v1, rowp, args, cb0, cb1, trb, r);
+          fused_chunk<OUT, CHUNK>(v0, v1, rowp, args, rc, cb0, cb1, trb, r);
         }
         if (FUSED && !ragged) {
           // finished values (alpha, beta * C, bias and activation applied in
           // registers): cast and staged by the same branch-free shared stores
           stage_chunk_scaled<OUT, false>(v0, v1, smem_u32(rowp), 1.0f, r);
-        } else if (!FUSED && !ADD && !ragged && !args.read_c) {
+        } else if (!FUSED && !ADD && !ragged && !rc) {
           // the common case, branch-free: alpha * acc, cast, one 16-byte
           // shared store per piece (per-piece branches slowed the stores ~1.6x)
           stage_chunk_scaled<OUT>(v0, v1, smem_u32(rowp), args.alpha, r);
@@ -990,17 +1124,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             store_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
                              col0 + E * j);
           else
-            finish_piece<OUT>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
+            finish_piece<OUT>(x, p, args, rc, ragged, !skip_store && row0 + r < args.M, row0 + r,
                               col0 + E * j);
         }
         end_chunk(st, stg, &tmC, row0, col0, ragged, skip_store);
       }
       return true;
     };
-    WorkIter wi;
-    WorkItem w;
-    work_begin(wi);
-    for (; ok && wi.next(&w); ++tl) {
+    // Hand accumulator buffer b back to the MMA issuer (after this warp's last
+    // TMEM access to it).
+    auto release_acc = [&](int b) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(&tempty[b]);
+        else
+          mbar_arrive_cluster(map_to_rank(&tempty[b], 0));
+      }
+    };
+    // beta * C of item wp's tile (this warp's 32 rows) into accumulator buffer b,
+    // the value its MMAs then accumulate onto.  Two column groups in flight.
+    auto preload_c = [&](const WorkItem& wp, int b) {
+      int mbp, nbp;
+      tile_of(args, wp.tile, &mbp, &nbp);
+      const int grow = mbp * TILE_M + static_cast<int>(rank) * BM + quarter * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(b * BN);
+      constexpr int NQ = BN / 32;
+      uint32_t va[32], vb[32];
+      load_c32<OUT>(args, grow, nbp * BN, va);
+#pragma unroll 1
+      for (int q = 0; q < NQ; q += 2) {
+        if (q + 1 < NQ) load_c32<OUT>(args, grow, nbp * BN + (q + 1) * 32, vb);
+        tmem_st_32x32b_x32(taddr, va, q * 32);
+        if (q + 2 < NQ) load_c32<OUT>(args, grow, nbp * BN + (q + 2) * 32, va);
+        if (q + 1 < NQ) tmem_st_32x32b_x32(taddr, vb, (q + 1) * 32);
+      }
+      tmem_st_wait();
+    };
+    // The unit's items in order, looked at two ahead: item tl + 2 uses the same
+    // accumulator buffer as item tl, and when it starts from beta * C this warp
+    // writes that into the buffer after finishing item tl.
+    WorkIter wq;
+    work_begin(wq);
+    WorkItem w, w1, w2;
+    bool h0 = wq.next(&w);
+    bool h1 = h0 && wq.next(&w1);
+    bool h2 = false;
+    uint32_t it_total = 0;   // ring iterations up to and including item tl
+    for (; ok && h0; ++tl, w = w1, h0 = h1, w1 = w2, h1 = h2) {
+      h2 = h1 && wq.next(&w2);
+      {
+        int kb_b, kb_e;
+        kb_range(w, &kb_b, &kb_e);
+        it_total += static_cast<uint32_t>((kb_e - kb_b + KO - 1) / KO);
+      }
+      const bool hold = h2 && item_preloads_c(args, tl + 2, w2);
+      const bool rc = args.read_c && !item_preloads_c(args, tl, w);
       int mb, nb;
       tile_of(args, w.tile, &mb, &nb);
       const int buf = tl & 1;
@@ -1063,66 +1244,85 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // the fp32 partial sum in this CTA's scratch slot, hand the accumulator
         // back, then release the CTA's flag with the launch epoch.  Such a
         // segment is the first (or only) one of its unit, so it is published
-        // early.  Slot layout [quarter][BN/4 pieces][32 rows][4 floats]: a warp's
-        // store covers 512 contiguous bytes and each epilogue warp's rows form
-        // one contiguous span, which the owner fetches with bulk copies.
-        float4* slot = reinterpret_cast<float4*>(args.ws + static_cast<size_t>(blockIdx.x) * BM * BN) +
-                       quarter * (BN / 4) * EPI_ROWS;
+        // early.  Slot layout [quarter][BN/4 pieces][32 rows][4 floats]: each
+        // group of 32 columns of a warp's rows is one contiguous 4 KB block,
+        // staged in the warp's epilogue buffers (conflict-free rows) and written
+        // with a bulk copy; each epilogue warp's rows form one contiguous span,
+        // which the owner fetches with bulk copies.
+        float* slot = args.ws + static_cast<size_t>(blockIdx.x) * BM * BN +
+                      static_cast<size_t>(quarter) * BN * EPI_ROWS;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(t_row, v, c * 32);
           tmem_ld_wait();
+          uint8_t* stg = st.stage0 + (st.chunk_ctr & 1) * L::EPI_BUF_BYTES;
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+          const uint32_t sb = smem_u32(stg) + static_cast<uint32_t>(r * 16);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            slot[(c * 8 + j) * EPI_ROWS + r] =
-                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            st_shared_v4(sb + j * EPI_ROWS * 16, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            bulk_store_s2g(slot + c * 32 * EPI_ROWS, smem_u32(stg), 32 * EPI_ROWS * 4);
+            bulk_commit_group();
+          }
+          __syncwarp();
+          ++st.chunk_ctr;
         }
-        tc_fence_before();
-        __syncwarp();
+        if (!hold) release_acc(buf);
         if (lane == 0) {
-          if (leader)
-            mbar_arrive(&tempty[buf]);
-          else
-            mbar_arrive_cluster(map_to_rank(&tempty[buf], 0));
+          bulk_wait_group<0>();          // the partial is written
+          fence_proxy_async_global();    // the owner reads it with bulk copies
         }
-        fence_proxy_async_global();   // the owner reads the slot with bulk copies
         __threadfence();
         if (!epilogue_sync()) {
           ok = false;
           break;
         }
         if (ew == 0 && lane == 0) flag_release(args.ws_flags + blockIdx.x, args.epoch);
+        if (hold) {
+          preload_c(w2, buf);
+          release_acc(buf);
+        }
         continue;
       }
       // A stream-K segment holding its tile's first k-groups but not the last
       // ones owns the tile: the units after it in the iteration space hold the
       // later k-groups as partial sums.  It is always the last segment of its
-      // unit, so the ring is idle once its accumulator is complete.
+      // unit, so the ring is idle once its accumulator is complete.  With a
+      // single such unit the producer lane has already waited for its flag and
+      // fetched the partial into the draining ring (pf_addr).
       int contrib0 = unit0, contrib1 = unit0;
+      uint32_t pf_addr = 0;
       if (w.g1 < args.groups) {
         const long long base = static_cast<long long>(w.tile - args.dp_tiles) * args.groups;
         contrib0 = unit0 + 1;
         contrib1 = sk_unit_of(base + args.groups - 1, unit_stride, args.sk_iters) + 1;
-        if (ew == 0 && lane == 0) {
-          for (int u = contrib0; u < contrib1 && !*abort_flag; ++u) {
-            const unsigned int* f = args.ws_flags + u * UNIT_CTAS + rank;
-            const uint64_t t0 = globaltimer_ns();
-            while (flag_acquire(f) != args.epoch) {
-              __nanosleep(64);
-              if (*abort_flag) break;
-              if (globaltimer_ns() - t0 > args.timeout_ns) {
-                record_error(args.status, SITE_STREAMK_FLAG);
-                *abort_flag = 1;
-                break;
+        if (contrib1 - contrib0 == 1 && !h1) {
+          pf_addr = smem_u32(sk_prefetch_dst(it_total, ew));
+        } else {
+          if (ew == 0 && lane == 0) {
+            for (int u = contrib0; u < contrib1 && !*abort_flag; ++u) {
+              const unsigned int* f = args.ws_flags + u * UNIT_CTAS + rank;
+              const uint64_t t0 = globaltimer_ns();
+              while (flag_acquire(f) != args.epoch) {
+                __nanosleep(64);
+                if (*abort_flag) break;
+                if (globaltimer_ns() - t0 > args.timeout_ns) {
+                  record_error(args.status, SITE_STREAMK_FLAG);
+                  *abort_flag = 1;
+                  break;
+                }
               }
             }
           }
-        }
-        if (!epilogue_sync() || *abort_flag) {
-          ok = false;
-          break;
+          if (!epilogue_sync() || *abort_flag) {
+            ok = false;
+            break;
+          }
         }
       }
       const int ncontrib = contrib1 - contrib0;
@@ -1130,11 +1330,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const BoolC<false> no;
       const BoolC<true> yes;
       if (ncontrib == 0)
-        ok = args.epi ? store_tile(no, yes, t_row, nb, row0, buf, 0, 0)
-                      : store_tile(no, no, t_row, nb, row0, buf, 0, 0);
+        ok = args.epi ? store_tile(no, yes, t_row, nb, row0, buf, 0, 0, rc, hold, 0u)
+                      : store_tile(no, no, t_row, nb, row0, buf, 0, 0, rc, hold, 0u);
       else
-        ok = args.epi ? store_tile(yes, yes, t_row, nb, row0, buf, contrib0, ncontrib)
-                      : store_tile(yes, no, t_row, nb, row0, buf, contrib0, ncontrib);
+        ok = args.epi ? store_tile(yes, yes, t_row, nb, row0, buf, contrib0, ncontrib, rc, hold, pf_addr)
+                      : store_tile(yes, no, t_row, nb, row0, buf, contrib0, ncontrib, rc, hold, pf_addr);
+      if (ok && hold) {
+        preload_c(w2, buf);
+        release_acc(buf);
+      }
     }
     // after an abort the rows are sent all the same, so the peer never waits
     // for a block that will not come
@@ -1208,7 +1412,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         EpiBias eb{0.0f, 0.0f, 0.0f, 0.0f};
         if (args.epi) eb = load_epi_bias<CHUNK>(args, col0, row0 + r);
         uint8_t* stg;
-        if (!begin_chunk<true, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args)) {
+        if (!begin_chunk<true, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args,
+                                                 args.read_c)) {
           ok = false;
           break;
         }
@@ -1245,11 +1450,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           uint4* p = reinterpret_cast<uint4*>(rowp + ((j ^ (r & 7)) << 4));
           if (args.epi)
-            finish_piece<OUT, true>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
-                                    col0 + E * j, eb, E * j);
+            finish_piece<OUT, true>(x, p, args, args.read_c, ragged, !skip_store && row0 + r < args.M,
+                                    row0 + r, col0 + E * j, eb, E * j);
           else
-            finish_piece<OUT, false>(x, p, args, ragged, !skip_store && row0 + r < args.M, row0 + r,
-                                     col0 + E * j);
+            finish_piece<OUT, false>(x, p, args, args.read_c, ragged,
+                                     !skip_store && row0 + r < args.M, row0 + r, col0 + E * j);
         }
         end_chunk(st, stg, &tmC, row0, col0, ragged, skip_store);
       }
@@ -1286,6 +1491,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         while (globaltimer_ns() - t0 < 200000ull) {
         }
       }
+      // partial copies into this CTA's ring (stream-K owner prefetch)
+      for (int q = 0; q < pf_issued; ++q) wait_drain(&pfb[q], 0, args);
     }
     if (warp == 1 && lane == 0 && leader) {
       // every MMA already issued (a commit with nothing pending arrives at once)
