@@ -405,9 +405,10 @@ def _r(x, nd=4):
 
 def summarise(suite, odd, fp8):
     """Short per-workload records (microseconds, fractions of the measured peaks)."""
-    cols = {"suite_cols": "ours_us, frac (tensor or HBM, of measured), bound, cuBLAS_us, "
-                          "ours_hot_us, cuBLAS_hot_us, bias_relu_us",
-            "suite_summary": {}, "odd_tail_cols": "ours_us, frac_hbm, cuBLAS_us",
+    cols = {"suite_cols": "ours_us, frac (tensor or HBM, of measured), bound, cuBLAS_us (same "
+                          "output dtype and beta), ours_hot_us, cuBLAS_hot_us, bias_relu_us, "
+                          "cuBLAS_us with input-dtype output and no beta",
+            "suite_summary": {}, "odd_tail_cols": "ours_us, frac_hbm, cuBLAS_us (same output dtype)",
             "odd_tail_summary": {}, "fp8_cols": "ours_us, frac (of 2x measured bf16), cuBLASLt_us",
             "fp8_summary": {}}
     for name, r in suite.items():
@@ -415,7 +416,7 @@ def summarise(suite, odd, fp8):
             _r(r["median_ms"] * 1e3), _r(r["frac"], 3), r["bound"], _r(r["cublas_ms"] * 1e3),
             _r(r.get("hot_ms", 0) * 1e3) if "hot_ms" in r else None,
             _r(r.get("cublas_hot_ms", 0) * 1e3) if "cublas_hot_ms" in r else None,
-            _r(r["bias_relu_median_ms"] * 1e3)]
+            _r(r["bias_relu_median_ms"] * 1e3), _r(r["cublas_inout_ms"] * 1e3)]
     for name, r in odd.items():
         cols["odd_tail_summary"][name] = [_r(r["median_ms"] * 1e3), _r(r["frac_hbm"], 3),
                                           _r(r["cublas_ms"] * 1e3)]
@@ -425,23 +426,52 @@ def summarise(suite, odd, fp8):
     return cols
 
 
-def time_cublas(w, a, b, steps, warmup, flush):
-    """cuBLAS reference point (torch.matmul, bench only, never the product path):
-    same shapes, input dtype and storage orders, output in the input dtype and
-    no beta term (torch has no fp16-in/fp32-out matmul); timed like ours."""
+def cublas_call(w, a, b, matched=True):
+    """A torch (cuBLAS) call for the workload's GEMM (bench only, never the
+    product path).  matched: the same problem as ours, i.e. the workload's output
+    dtype (fp16/bf16 inputs with fp32 output through torch's out_dtype) and its
+    alpha/beta (addmm reading a copy of C); when torch cannot express that, or
+    matched is False, the output is in the input dtype with no beta term.
+    Returns (callable, kind)."""
     import torch
+    aa = a.t() if w["a_col"] else a      # [M, K] view of A
     bb = b.t() if w["b_col"] else b      # [K, N] view of B (column-major when b_col)
+    if matched:
+        odt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w["out_dtype"]]
+        out = torch.empty(w["M"], w["N"], dtype=odt, device=a.device)
+        kw = {} if odt == a.dtype else {"out_dtype": odt}
+        if w["beta"] != 0.0:
+            c_in = torch.randn(w["M"], w["N"], device=a.device).to(odt)
+            fn = lambda: torch.addmm(c_in, aa, bb, beta=w["beta"], alpha=w["alpha"], out=out, **kw)
+        elif w["alpha"] != 1.0:
+            fn = lambda: torch.addmm(out, aa, bb, beta=0.0, alpha=w["alpha"], out=out, **kw)
+        else:
+            fn = lambda: torch.mm(aa, bb, out=out, **kw)
+        try:
+            fn()
+            torch.cuda.synchronize()
+            return fn, "matched (output dtype, alpha, beta)"
+        except (TypeError, RuntimeError):
+            pass
+    return (lambda: torch.matmul(aa, bb)), "input-dtype output, no beta"
+
+
+def time_cublas(w, a, b, steps, warmup, flush, matched=True):
+    """cuBLAS reference point, timed like ours (L2 flushed before each step,
+    outside the events).  Returns (median ms, kind) with kind from cublas_call."""
+    import torch
+    fn, kind = cublas_call(w, a, b, matched)
     evs = []
     for i in range(warmup + steps):
         flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        torch.matmul(a, bb)
+        fn()
         e1.record()
         if i >= warmup:
             evs.append((e0, e1))
     torch.cuda.synchronize()
-    return statistics.median([x.elapsed_time(y) for x, y in evs])
+    return statistics.median([x.elapsed_time(y) for x, y in evs]), kind
 
 
 def time_hot(launch, reps=20, warmup=3):
@@ -477,7 +507,10 @@ def run_suite(g, args, device, peaks, skip_cfg):
         bound = roofline_bound(w, peak_t, hbm)
         tf = flops / (ms * 1e-3) / 1e12
         gbs = algorithmic_bytes(w) / (ms * 1e-3) / 1e9
-        cub_ms = time_cublas(w, a, b, 20, 5, flush)
+        cub_ms, cub_kind = time_cublas(w, a, b, 20, 5, flush)
+        # cuBLAS writing the input dtype with no beta term (a smaller problem
+        # whenever the workload's output is fp32 or beta != 0)
+        cub_inout_ms, _ = time_cublas(w, a, b, 20, 5, flush, matched=False)
         # the same GEMM with the fused epilogue (per-column fp32 bias, then ReLU)
         bias = torch.from_numpy(si.normal(4000 + cfg, w["N"], 1.0)).to(device)
         ftimes = time_gemm(g, w, a, b, c, c0, 20, 5, torch.cuda.current_stream(device), flush,
@@ -485,17 +518,17 @@ def run_suite(g, args, device, peaks, skip_cfg):
         res[w["name"]] = {"median_ms": ms, "tflops": tf, "gbs_algorithmic": gbs, "bound": bound,
                           "frac": tf / peak_t if bound == "tensor" else gbs / hbm,
                           "cublas_ms": cub_ms, "cublas_tflops": flops / (cub_ms * 1e-3) / 1e12,
+                          "cublas_kind": cub_kind, "cublas_inout_ms": cub_inout_ms,
                           "bias_relu_median_ms": statistics.median(ftimes),
                           "bias_relu_mean_over_plain_mean": statistics.mean(ftimes) / statistics.mean(times)}
         if bound == "tensor":
             # back-to-back launches ("hot": no flush in between), ours and cuBLAS's
             try:
                 st = torch.cuda.current_stream(device)
-                bb = b.t() if w["b_col"] else b
                 hot = time_hot(lambda: g.matmul(a, b, c, alpha=w["alpha"], beta=w["beta"],
                                                 a_col=w["a_col"], b_col=w["b_col"],
                                                 stream=st.cuda_stream))
-                cub_hot = time_hot(lambda: torch.matmul(a, bb))
+                cub_hot = time_hot(cublas_call(w, a, b)[0])
                 res[w["name"]].update({"hot_ms": hot, "hot_tflops": flops / (hot * 1e-3) / 1e12,
                                        "cublas_hot_ms": cub_hot})
             except Exception as e:  # reported, never fatal to the bench line
@@ -546,13 +579,13 @@ def run_odd_tail(g, device, peaks):
         w = {"alpha": 1.0, "beta": 0.0, "a_col": False, "b_col": b_col}
         times = time_gemm(g, w, a, b, c, None, 20, 5, torch.cuda.current_stream(device), flush)
         ms = statistics.median(times)
-        bt = b.t() if b_col else b
+        cub_fn, _ = cublas_call(dict(w, M=M, N=N, out_dtype=dout), a, b)
         ctimes = []
         for _ in range(25):
             flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            torch.matmul(a, bt)
+            cub_fn()
             e1.record()
             torch.cuda.synchronize()
             ctimes.append(e0.elapsed_time(e1))
