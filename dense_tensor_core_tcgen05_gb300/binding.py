@@ -26,6 +26,7 @@ GEMM_ORDER_AUTO, GEMM_ORDER_GROUPED, GEMM_ORDER_HILBERT = 0, 1, 2
 EXPORTS = ("gemm", "gemm_bias_act", "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_status_string",
            "gemm_sync_status",
            "gemm_debug_set", "gemm_plan", "gemm_tile_coord", "gemm_tile_order", "gemm_work_items",
+           "gemm_split_tile_item",
            "gemm_encode_idesc", "gemm_encode_sdesc", "gemm_version")
 
 
@@ -42,7 +43,8 @@ class gemm_plan_t(ctypes.Structure):
         "grid", "group_m", "threads", "smem_bytes", "tmem_cols", "a_mn", "b_mn",
         "epi_chunk_cols", "cta_group", "split_k", "groups", "dp_tiles", "order",
         "specialised")] + [
-        ("sk_iters", ctypes.c_int64), ("scratch_bytes", ctypes.c_int64)]
+        ("sk_iters", ctypes.c_int64), ("scratch_bytes", ctypes.c_int64),
+        ("tile_split", ctypes.c_int32), ("owner_groups", ctypes.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -87,6 +89,8 @@ def _load():
     lib.gemm_tile_order.restype = i32
     lib.gemm_work_items.argtypes = [i32, i32, i32, i64, i32, ctypes.POINTER(i32), i32]
     lib.gemm_work_items.restype = i32
+    lib.gemm_split_tile_item.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32)]
+    lib.gemm_split_tile_item.restype = i32
     lib.gemm_encode_idesc.argtypes = [ci, ci, ci, ci, ci]
     lib.gemm_encode_idesc.restype = ctypes.c_uint32
     lib.gemm_encode_sdesc.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
@@ -192,6 +196,13 @@ def gemm_work_items(unit, units, dp_tiles, sk_iters, groups, max_items=4096):
     buf = (ctypes.c_int32 * (3 * max_items))()
     n = _lib.gemm_work_items(unit, units, dp_tiles, sk_iters, groups, buf, max_items)
     return [tuple(buf[3 * i:3 * i + 3]) for i in range(min(n, max_items))]
+
+
+def gemm_split_tile_item(unit, tile_split, owner_groups, groups):
+    """(tile, first k-group, end k-group) of a unit under a split-tile plan, or None."""
+    buf = (ctypes.c_int32 * 3)()
+    n = _lib.gemm_split_tile_item(unit, tile_split, owner_groups, groups, buf)
+    return tuple(buf) if n == 1 else None
 
 
 def gemm_encode_idesc(in_dtype, a_mn, b_mn, m, n):

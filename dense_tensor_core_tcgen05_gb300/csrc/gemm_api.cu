@@ -340,6 +340,18 @@ int choose_split(int64_t M, int64_t N, int64_t K, int kbe, int num_sms, int* bn_
   return cands[best].s;
 }
 
+// k-groups of a split tile's first part, the one that finishes the tile: a
+// larger share than each of the others' (by about a tenth of the tile's
+// k-groups), so they finish first and their partial sums are in its spare
+// accumulator before its own MMAs end.  Every other part keeps at least one
+// k-group.
+int split_owner_groups(int groups, int parts) {
+  const int extra = std::max(1, groups / 10);
+  int owner = (groups + (parts - 1) * extra) / parts;
+  owner = std::min(owner, groups - (parts - 1));
+  return std::max(owner, 1);
+}
+
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int layout,
                         int num_sms, const gemm_config_t* cfg, gemm_plan_t* p) {
   const int kbe = kblock_elems(in_dtype);
@@ -361,7 +373,18 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
     pair = cfg->cta_group == 2;
     if (!cfg->bn) bn = 256;
   }
-  if (cfg && cfg->split_k) {
+  const int sk_mode = cfg ? cfg->stream_k : 0;
+  if (sk_mode < 0 || sk_mode > 3) return GEMM_ERR_INVALID_ARG;
+  // split-tile (stream_k 3): split_k parts per tile through the scratch buffer,
+  // single-CTA tiles, no cluster
+  int tile_split = 0;
+  if (sk_mode == 3) {
+    tile_split = cfg->split_k ? cfg->split_k : 2;
+    if (tile_split < 2 || tile_split > 16 || cfg->cta_group == 2) return GEMM_ERR_INVALID_ARG;
+    pair = false;
+    split = 1;
+    if (!cfg->bn) bn = 128;
+  } else if (cfg && cfg->split_k) {
     if (cfg->split_k < 1) return GEMM_ERR_INVALID_ARG;
     split = cfg->split_k;
     if (!cfg->bn) bn = 256;
@@ -413,11 +436,17 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   p->groups = static_cast<int32_t>(ceil_div(kb, ko));
   p->dp_tiles = p->num_tiles;
   p->sk_iters = 0;
-  const int sk_mode = cfg ? cfg->stream_k : 0;
-  if (sk_mode < 0 || sk_mode > 2) return GEMM_ERR_INVALID_ARG;
-  // Owners wait for partials of higher-numbered units, so stream-K needs every
-  // unit resident at once: at most one CTA per SM.
-  if (split == 1 && sk_mode != 1 && grid <= kMaxSkCtas && grid <= num_sms) {
+  // Owners wait for partials of higher-numbered units, so stream-K and
+  // split-tile work need every unit resident at once: at most one CTA per SM.
+  if (tile_split) {
+    if (p->groups < tile_split) return GEMM_ERR_INVALID_ARG;   // a k-group per part at least
+    if (int64_t(p->num_tiles) * tile_split > std::min(num_sms, kMaxSkCtas))
+      return GEMM_ERR_UNSUPPORTED;
+    p->dp_tiles = 0;
+    p->tile_split = tile_split;
+    p->owner_groups = split_owner_groups(p->groups, tile_split);
+    grid = p->num_tiles * tile_split;
+  } else if (split == 1 && sk_mode != 1 && grid <= kMaxSkCtas && grid <= num_sms) {
     const int64_t units = grid / per_unit;
     const int64_t waves = p->num_tiles / units, rem = p->num_tiles % units;
     const bool worth = rem != 0 && 2 * rem <= units && waves >= 2 && waves <= 5 && p->groups >= 4;
@@ -431,14 +460,15 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
     }
   }
   // a data-parallel launch needs no more units than tiles
-  if (!p->sk_iters && grid > p->num_tiles * per_unit) grid = p->num_tiles * per_unit;
+  if (!p->sk_iters && !tile_split && grid > p->num_tiles * per_unit) grid = p->num_tiles * per_unit;
   if (split > 1) {
     if (int64_t(p->num_tiles) * split >= (int64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
     grid = p->num_tiles * split;   // exactly one tile per split-K cluster
   }
   p->grid = grid;
   p->split_k = split;
-  p->scratch_bytes = p->sk_iters ? int64_t(kFlagBytes) + int64_t(grid) * BM * int64_t(bn) * 4 : 0;
+  p->scratch_bytes = (p->sk_iters || tile_split) ? int64_t(kFlagBytes) + int64_t(grid) * BM * int64_t(bn) * 4
+                                                 : 0;
   p->threads = NUM_THREADS;
   p->smem_bytes = smem_alloc_bytes(bn, pair);
   p->tmem_cols = 2 * bn;
@@ -449,7 +479,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   // the conditions of run_gemm's plain path that the plan itself fixes
   p->specialised = (p->order == GEMM_ORDER_GROUPED && !(cfg && cfg->general) &&
                     (N * out_size(out_dtype)) % 16 == 0 &&
-                    spec_supported(bn, pair, split, layout, is_fp8(in_dtype), p->sk_iters != 0,
+                    spec_supported(bn, pair, split, layout, is_fp8(in_dtype),
+                                   p->sk_iters != 0 || tile_split != 0,
                                    false, false))
                        ? 1
                        : 0;
@@ -624,6 +655,8 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.groups = p.groups;
   ka.dp_tiles = p.dp_tiles;
   ka.sk_iters = p.sk_iters;
+  ka.tile_split = p.tile_split;
+  ka.owner_groups = p.owner_groups;
   ka.bias = bias;
   ka.bias_kind = bias_kind;
   ka.act = act;
@@ -636,7 +669,7 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
     s = hilbert_map_for(dev, p.m_tiles, p.n_tiles, &ka.tile_map);
     if (s != GEMM_OK) return s;
   }
-  if (p.sk_iters) {
+  if (p.sk_iters || p.tile_split) {
     s = fixed_scratch ? noalloc_scratch(dev, stream, size_t(BM) * p.bn * 4, p.grid, &ka.ws,
                                         &ka.ws_flags, &ka.epoch)
                       : scratch_for(dev, stream, size_t(BM) * p.bn * 4, p.grid, &ka.ws,
@@ -648,7 +681,7 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   // configuration and layout when there is one (cfg->general = 1 forbids it).
   const bool plain = !(cfg && cfg->general) && !ka.n_ragged && ka.inject_skip == 0 &&
                      ka.tile_map == nullptr;
-  const bool sk = ka.sk_iters != 0, readc = ka.read_c != 0, epi = ka.epi != 0;
+  const bool sk = ka.sk_iters != 0 || ka.tile_split != 0, readc = ka.read_c != 0, epi = ka.epi != 0;
   cudaError_t e = cudaErrorNotSupported;
   if (plain) {
     using SpecLaunch = cudaError_t (*)(int, bool, int, int, bool, bool, bool, const OperandMaps&,
@@ -866,6 +899,23 @@ int32_t gemm_work_items(int32_t unit, int32_t units, int32_t dp_tiles, int64_t s
     }
     ++n;
   }
+  return n;
+}
+
+int32_t gemm_split_tile_item(int32_t unit, int32_t tile_split, int32_t owner_groups,
+                             int32_t groups, int32_t* item) {
+  if (unit < 0 || tile_split < 2 || groups < tile_split || owner_groups < 1 ||
+      groups - owner_groups < tile_split - 1 || item == nullptr)
+    return 0;
+  WorkIter wi;
+  wi.init(unit, 0, 0, 0, groups, tile_split, owner_groups);
+  WorkItem w;
+  if (!wi.next(&w)) return 0;
+  item[0] = w.tile;
+  item[1] = w.g0;
+  item[2] = w.g1;
+  int32_t n = 1;
+  while (wi.next(&w)) ++n;
   return n;
 }
 

@@ -109,22 +109,50 @@ struct WorkItem {
   int tile, g0, g1;   // tile index and k-group range [g0, g1)
 };
 
+// Split-tile schedule (tile_split = s >= 2, instead of the two phases above):
+// unit u works on tile u / s alone.  Part u % s = 0 takes k-groups
+// [0, owner_groups) and owns the tile; parts 1 .. s-1 split the remaining
+// k-groups evenly and leave partial sums.  The owner's share is the larger one,
+// so the other parts finish (and publish) while it is still accumulating.
 struct WorkIter {
   int units, dp_tiles, groups, next_dp;
   long long i, hi, sk_iters;
-  GEMM_HD void init(int unit, int units_, int dp_tiles_, long long sk_iters_, int groups_) {
+  int st_tile, st_g0, st_g1;   // split-tile: the unit's one item (st_tile < 0: taken)
+  GEMM_HD void init(int unit, int units_, int dp_tiles_, long long sk_iters_, int groups_,
+                    int tile_split = 0, int owner_groups = 0) {
     units = units_;
     dp_tiles = dp_tiles_;
     groups = groups_;
     next_dp = unit;
     sk_iters = sk_iters_;
     i = hi = 0;
-    if (sk_iters != 0) {   // 64-bit divisions only for stream-K plans (slow on the device)
+    st_tile = -1;
+    st_g0 = st_g1 = 0;
+    if (tile_split > 1) {
+      const int part = unit % tile_split;
+      st_tile = unit / tile_split;
+      if (part == 0) {
+        st_g1 = owner_groups;
+      } else {
+        const int rest = groups_ - owner_groups, np = tile_split - 1;
+        st_g0 = owner_groups + ((part - 1) * rest) / np;
+        st_g1 = owner_groups + (part * rest) / np;
+      }
+      dp_tiles = 0;
+      sk_iters = 0;
+    } else if (sk_iters != 0) {   // 64-bit divisions only for stream-K plans (slow on the device)
       i = (static_cast<long long>(unit) * sk_iters) / units;
       hi = (static_cast<long long>(unit + 1) * sk_iters) / units;
     }
   }
   GEMM_HD bool next(WorkItem* w) {
+    if (st_tile >= 0) {
+      w->tile = st_tile;
+      w->g0 = st_g0;
+      w->g1 = st_g1;
+      st_tile = -1;
+      return true;
+    }
     if (next_dp < dp_tiles) {
       w->tile = next_dp;
       w->g0 = 0;
@@ -205,6 +233,9 @@ struct KernelArgs {
   // (alpha == 1 only, so the accumulator then holds alpha*AB + beta*C), for every
   // work item after a unit's first two that holds its tile's first k-groups.
   int pre_c;
+  // Split-tile schedule (see WorkIter): parts per tile (0: not used) and the
+  // k-groups of the owning part.
+  int tile_split, owner_groups;
 };
 
 // Whether work item number `tl` of a unit (item `w`) starts from an accumulator
@@ -212,6 +243,19 @@ struct KernelArgs {
 // the epilogue warps evaluate it on the same item sequence.
 GEMM_HD bool item_preloads_c(const KernelArgs& a, uint32_t tl, const WorkItem& w) {
   return a.pre_c && a.read_c && tl >= 2 && w.g0 == 0;
+}
+
+// Units whose partial sums the owner of work item w (unit `unit` of `units`;
+// w holds its tile's first k-groups but not all of them) adds: [*c0, *c1).
+GEMM_HD void owner_contributors(const KernelArgs& a, int unit, int units, const WorkItem& w,
+                                int* c0, int* c1) {
+  *c0 = unit + 1;
+  if (a.tile_split > 1) {
+    *c1 = unit + a.tile_split;
+  } else {
+    const long long base = static_cast<long long>(w.tile - a.dp_tiles) * a.groups;
+    *c1 = sk_unit_of(base + a.groups - 1, units, a.sk_iters) + 1;
+  }
 }
 
 #if defined(__CUDACC__)

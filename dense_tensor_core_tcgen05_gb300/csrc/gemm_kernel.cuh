@@ -39,7 +39,6 @@ constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_ROWS = 32;     // rows per epilogue warp = its TMEM lane quarter
 constexpr int EPI_BUFS = 2;      // staging buffers per epilogue warp
-constexpr int PSLOTS_MAX = 8;    // stream-K partial staging slots per epilogue warp
 
 enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_F16 = 2 };
 
@@ -80,14 +79,10 @@ struct SmemLayout {
   static constexpr int off_b = STAGES * A_BYTES;
   static constexpr int off_epi = off_b + STAGES * B_BYTES;
   static constexpr int off_bar = off_epi + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-  // Stream-K owner: each epilogue warp stages the partial sums it adds in its
-  // quarter of the ring (idle by then), in up to PSLOTS_MAX slots.
   static constexpr int RING_BYTES = off_epi;
-  static constexpr int PWARP_BYTES = RING_BYTES / EPI_WARPS;
   // full[STAGES], empty[STAGES], tfull[2], tempty[2], cload[EPI_WARPS*EPI_BUFS], drain, esync,
-  // pfull[EPI_WARPS*PSLOTS_MAX], rfull, pfb[EPI_WARPS]
-  static constexpr int NUM_BARS =
-      2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 2 + EPI_WARPS * PSLOTS_MAX + 1 + EPI_WARPS;
+  // rfull
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_WARPS * EPI_BUFS + 2 + 1;
   static constexpr int off_tmem = off_bar + NUM_BARS * 8;
   static constexpr int off_flag = off_tmem + 8;
   static constexpr int BYTES = off_flag + 8;
@@ -453,7 +448,7 @@ enum : int {
   SPEC_PLAIN = 1,          // plain epilogue and scheduling (see above)
   SPEC_LAYOUT = 2,         // operand layout fixed: bits 2..3 hold GEMM_A_* | GEMM_B_*
   SPEC_LAYOUT_SHIFT = 2,
-  SPEC_STREAMK = 16,       // with SPEC_PLAIN: stream-K work stays a run-time choice
+  SPEC_STREAMK = 16,       // with SPEC_PLAIN: stream-K or split-tile work stays a run-time choice
   SPEC_READC = 32,         // with SPEC_PLAIN: C is read (beta != 0)
   SPEC_EPI = 64,           // with SPEC_PLAIN: a bias and/or an activation is applied
 };
@@ -476,7 +471,10 @@ __device__ __forceinline__ KernelArgs specialise_args(const KernelArgs& in) {
       a.act = EPI_ACT_NONE;
     }
     a.n_ragged = 0;
-    if (!(SPEC & SPEC_STREAMK)) a.sk_iters = 0;
+    if (!(SPEC & SPEC_STREAMK)) {
+      a.sk_iters = 0;
+      a.tile_split = 0;
+    }
     a.inject_skip = 0;
     a.tile_map = nullptr;
   }
@@ -626,11 +624,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* cload = tempty + 2;
   uint64_t* drain = cload + EPI_WARPS * EPI_BUFS;
   uint64_t* esync = drain + 1;   // rendezvous of the four epilogue warps (stream-K hand-off)
-  uint64_t* pfull = esync + 1;   // stream-K partial staging slots, PSLOTS_MAX per epilogue warp
-  uint64_t* rfull = pfull + EPI_WARPS * PSLOTS_MAX;   // split-K: the peers' slices have landed
-  // stream-K owner: the single later unit's partial of epilogue warp q's rows,
-  // prefetched into the draining ring by the producer lane, has landed (pfb[q])
-  uint64_t* pfb = rfull + 1;
+  uint64_t* rfull = esync + 1;   // split-K: the peers' slices have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_tmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_flag);
 
@@ -659,22 +653,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   };
   auto work_begin = [&](WorkIter& wi) {
-    wi.init(unit0, unit_stride, args.dp_tiles, args.sk_iters, args.groups);
-  };
-  // Stream-K owner segment with a single later unit: where epilogue warp q's
-  // share of that unit's partial (32 rows x BN fp32) lands in the draining ring,
-  // given the producer's ring iteration count at the end: the A and B parts of
-  // the first slot to drain after its last copy (warps 0 and 1), then of the
-  // second (warps 2 and 3).
-  static_assert(EPI_ROWS * BN * 4 <= L::A_BYTES && EPI_ROWS * BN * 4 <= L::B_BYTES,
-                "a warp's partial must fit a ring slot's operand part");
-  auto sk_prefetch_dst = [&](uint32_t it_end, int q) -> uint8_t* {
-    const int s = static_cast<int>((it_end + static_cast<uint32_t>(q >> 1)) % STAGES);
-    return (q & 1) ? smem + L::off_b + s * L::B_BYTES : smem + L::off_a + s * L::A_BYTES;
+    wi.init(unit0, unit_stride, args.dp_tiles, args.sk_iters, args.groups, args.tile_split,
+            args.owner_groups);
   };
   uint32_t producer_iters = 0;  // ring iterations armed (producer thread only)
-  int pf_issued = 0;            // partial prefetch copies issued (producer thread only)
-
   // Start-up.  The lanes of warp 0 initialise the barriers (one each) while
   // warp 1 allocates TMEM and warp 2 prefetches the tensor maps (on warp 0's
   // path the prefetches delayed the first copy by ~0.4 us).  The start-up barrier
@@ -753,7 +735,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------ TMA producer
       uint32_t it = 0;
       bool ok = true;
-      const bool any_item = have;
       while (ok && have) {
         int kb_begin, kb_end;
         kb_range(w, &kb_begin, &kb_end);
@@ -824,51 +805,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (have) tile_of(args, w.tile, &mb, &nb);
       }
       producer_iters = it;
-      // Stream-K owner segment with a single later unit (always the unit's last
-      // item): wait for that unit's flag, then fetch its partial into the first
-      // two ring slots to drain (sk_prefetch_dst), so the epilogue finds it in
-      // shared memory when the accumulator is complete.
-      if (ok && any_item && args.sk_iters != 0 && w.g0 == 0 && w.g1 < args.groups) {
-        const long long base = static_cast<long long>(w.tile - args.dp_tiles) * args.groups;
-        const int c0 = unit0 + 1;
-        const int c1 = sk_unit_of(base + args.groups - 1, unit_stride, args.sk_iters) + 1;
-        if (c1 - c0 == 1) {
-          const unsigned int* f = args.ws_flags + c0 * UNIT_CTAS + rank;
-          const uint64_t t0 = globaltimer_ns();
-          bool ready = true;
-          while (flag_acquire(f) != args.epoch) {
-            __nanosleep(64);
-            if (*abort_flag) {
-              ready = false;
-              break;
-            }
-            if (globaltimer_ns() - t0 > args.timeout_ns) {
-              record_error(args.status, SITE_STREAMK_FLAG);
-              *abort_flag = 1;
-              ready = false;
-              break;
-            }
-          }
-          if (ready) {
-            fence_proxy_async_global();   // the partial was published by another CTA
-            const uint64_t pol = policy_evict_first();
-            constexpr uint32_t PBYTES = EPI_ROWS * BN * 4;
-            const float* src0 = args.ws + static_cast<size_t>(c0 * UNIT_CTAS + rank) * BM * BN;
-            for (int q = 0; q < EPI_WARPS; ++q) {
-              // the slot of ring iteration it + q/2, once its last MMAs have completed
-              const uint32_t j = it + static_cast<uint32_t>(q >> 1);
-              if ((q & 1) == 0 && !wait_one<PAIR>(&empty[j % STAGES], ((j / STAGES) & 1) ^ 1,
-                                                  abort_flag, args, SITE_PRODUCER_EMPTY))
-                break;
-              const int quarter_q = (q + EPI_WARP0) & 3;   // the TMEM lane quarter of warp q
-              mbar_arrive_expect_tx(&pfb[q], PBYTES);
-              bulk_load_g2s(sk_prefetch_dst(it, q), src0 + static_cast<size_t>(quarter_q) * BN * EPI_ROWS,
-                            PBYTES, &pfb[q], pol);
-              pf_issued = q + 1;
-            }
-          }
-        }
-      }
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -884,6 +820,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t b_kb = args.b_mn ? BK * SW : L::B_COLS * SW;
       const uint32_t a_step = (args.a_mn ? UMMA_K * SW : UMMA_K * 2) >> 4;
       const uint32_t b_step = (args.b_mn ? UMMA_K * SW : UMMA_K * 2) >> 4;
+      auto mma = [&](uint32_t d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
+        if (F8) {
+          if (PAIR)
+            umma_f8_pair(d, da, db, idesc, acc);
+          else
+            umma_f8(d, da, db, idesc, acc);
+        } else {
+          if (PAIR)
+            umma_f16_pair(d, da, db, idesc, acc);
+          else
+            umma_f16(d, da, db, idesc, acc);
+        }
+      };
+      // The MMAs of one ring stage (slot s, nkb k-blocks, the item's stage si).
+      auto issue_stage = [&](int s, int nkb, int si, uint32_t d_tmem, bool pre) {
+        const uint32_t sa = smem_u32(smem + L::off_a + s * L::A_BYTES);
+        const uint32_t sb = smem_u32(smem + L::off_b + s * L::B_BYTES);
+#pragma unroll
+        for (int j = 0; j < KO; ++j) {
+          if (j < nkb) {
+            const uint64_t da0 = make_sdesc_sw128(sa + j * a_kb, a_lbo, 8 * SW);
+            const uint64_t db0 = make_sdesc_sw128(sb + j * b_kb, b_lbo, 8 * SW);
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {   // 4 x 32 bytes of each row
+              const uint64_t da = da0 + static_cast<uint64_t>(kk) * a_step;
+              const uint64_t db = db0 + static_cast<uint64_t>(kk) * b_step;
+              const uint32_t acc = (pre || si != 0 || j != 0 || kk != 0) ? 1u : 0u;
+              mma(d_tmem, da, db, args.idesc, acc);
+            }
+          }
+        }
+      };
+      auto commit_to = [&](uint64_t* bar) {
+        if (PAIR)
+          umma_commit_pair_multicast(bar, 0x3);   // in both CTAs
+        else
+          umma_commit(bar);
+      };
       WorkIter wi;
       WorkItem w;
       work_begin(wi);
@@ -900,7 +874,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int kb0 = kb_begin; kb0 < kb_end; kb0 += KO, ++it) {
+        int si = 0;
+        for (int kb0 = kb_begin; kb0 < kb_end; kb0 += KO, ++it, ++si) {
           const int nkb = kb_end - kb0 < KO ? kb_end - kb0 : KO;
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -909,42 +884,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + L::off_a + s * L::A_BYTES);
-          const uint32_t sb = smem_u32(smem + L::off_b + s * L::B_BYTES);
-#pragma unroll
-          for (int j = 0; j < KO; ++j) {
-            if (j < nkb) {
-              const uint64_t da0 = make_sdesc_sw128(sa + j * a_kb, a_lbo, 8 * SW);
-              const uint64_t db0 = make_sdesc_sw128(sb + j * b_kb, b_lbo, 8 * SW);
-#pragma unroll
-              for (int kk = 0; kk < BK / UMMA_K; ++kk) {   // 4 x 32 bytes of each row
-                const uint64_t da = da0 + static_cast<uint64_t>(kk) * a_step;
-                const uint64_t db = db0 + static_cast<uint64_t>(kk) * b_step;
-                const uint32_t acc = (pre || kb0 != kb_begin || j != 0 || kk != 0) ? 1u : 0u;
-                if (F8) {
-                  if (PAIR)
-                    umma_f8_pair(d_tmem, da, db, args.idesc, acc);
-                  else
-                    umma_f8(d_tmem, da, db, args.idesc, acc);
-                } else {
-                  if (PAIR)
-                    umma_f16_pair(d_tmem, da, db, args.idesc, acc);
-                  else
-                    umma_f16(d_tmem, da, db, args.idesc, acc);
-                }
-              }
-            }
-          }
-          if (PAIR)
-            umma_commit_pair_multicast(&empty[s], 0x3);   // free slot s in both CTAs
-          else
-            umma_commit(&empty[s]);
+          issue_stage(s, nkb, si, d_tmem, pre);
+          commit_to(&empty[s]);   // free slot s once these MMAs have completed
         }
         if (!ok) break;
-        if (PAIR)
-          umma_commit_pair_multicast(&tfull[buf], 0x3);   // accumulator ready in both CTAs
-        else
-          umma_commit(&tfull[buf]);
+        commit_to(&tfull[buf]);   // accumulator ready
       }
     }
   } else {
@@ -977,61 +921,92 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(esync);
       return wait_warp<PAIR>(esync, (esync_uses++) & 1, abort_flag, args, SITE_STREAMK_FLAG);
     };
-    // Stream-K owner tiles: this warp fetches each later unit's partial sum of
-    // its 32 rows chunk by chunk (one bulk copy per chunk and contributing
-    // unit) into PSLOTS slots of its quarter of the idle ring.  Copies are
-    // numbered in issue order; p_issued and p_done (waited for) are warp-uniform.
-    constexpr int PART_BYTES = CHUNK * EPI_ROWS * 4;
-    constexpr int PSLOTS =
-        L::PWARP_BYTES / PART_BYTES < PSLOTS_MAX ? L::PWARP_BYTES / PART_BYTES : PSLOTS_MAX;
-    static_assert(PSLOTS >= 2 && L::PWARP_BYTES % 128 == 0, "partial staging does not fit the ring");
-    uint8_t* const pstage = smem + ew * L::PWARP_BYTES;
-    uint64_t* const pbar = pfull + ew * PSLOTS_MAX;
-    uint32_t p_issued = 0, p_done = 0;
+    // Bounded wait by the whole warp for a contributing unit's ready flag (its
+    // partial sum published with this launch's epoch).  Every lane acquires the
+    // flag itself, so every lane's later loads of the partial see it.
+    auto wait_flag_warp = [&](const unsigned int* f) -> bool {
+      uint64_t t0 = 0;
+      for (uint32_t i = 0;; ++i) {
+        const bool done = flag_acquire(f) == args.epoch;
+        if (__all_sync(0xffffffffu, done)) return true;
+        __nanosleep(64);
+        if ((i & 7) == 7) {
+          int give_up = 0;
+          if (lane == 0) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            if (*abort_flag) {
+              give_up = 1;
+            } else if (now - t0 > args.timeout_ns) {
+              record_error(args.status, SITE_STREAMK_FLAG);
+              *abort_flag = 1;
+              give_up = 1;
+            }
+          }
+          if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+        }
+      }
+    };
+    // Owner of a tile whose later k-groups other units hold: once their flags
+    // are up, sum their partials of this warp's 32 rows (unit order c0, c0+1,
+    // ...) into the TMEM accumulator buffer at t_part, which the unit no longer
+    // uses (the owner item is the unit's last), while the item's own MMAs are
+    // still running.  A contributor's slot holds each 32-column group of a
+    // warp's rows as [8 pieces][32 rows][16 B], so one 16-byte load per lane and
+    // piece reads 512 contiguous bytes.  Returns false if a wait gave up.
+    auto preload_partials = [&](int c0, int n, uint32_t t_part) -> bool {
+      for (int k = 0; k < n; ++k)
+        if (!wait_flag_warp(args.ws_flags + (c0 + k) * UNIT_CTAS + rank)) return false;
+      static_assert((BN / 32) % 2 == 0, "partials are preloaded 64 columns at a time");
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; c += 2) {
+        uint32_t s0[32], s1[32];
+#pragma unroll 1
+        for (int k = 0; k < n; ++k) {
+          const float4* src = reinterpret_cast<const float4*>(
+              args.ws + static_cast<size_t>((c0 + k) * UNIT_CTAS + rank) * BM * BN +
+              static_cast<size_t>(quarter) * BN * EPI_ROWS) + static_cast<size_t>(c) * 8 * EPI_ROWS + lane;
+          float4 v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __ldcg(src + j * EPI_ROWS);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            uint32_t* d = j < 8 ? s0 + 4 * j : s1 + 4 * (j - 8);
+            if (k == 0) {
+              d[0] = __float_as_uint(v[j].x);
+              d[1] = __float_as_uint(v[j].y);
+              d[2] = __float_as_uint(v[j].z);
+              d[3] = __float_as_uint(v[j].w);
+            } else {
+              d[0] = __float_as_uint(__uint_as_float(d[0]) + v[j].x);
+              d[1] = __float_as_uint(__uint_as_float(d[1]) + v[j].y);
+              d[2] = __float_as_uint(__uint_as_float(d[2]) + v[j].z);
+              d[3] = __float_as_uint(__uint_as_float(d[3]) + v[j].w);
+            }
+          }
+        }
+        tmem_st_32x32b_x32(t_part, s0, c * 32);
+        tmem_st_32x32b_x32(t_part, s1, c * 32 + 32);
+      }
+      tmem_st_wait();
+      return true;
+    };
 
     float tb[BN / 32] = {};   // the current tile's column bias (see the tile loop)
     float trb = 0.0f;         // ... or this thread's row bias
     // Write one finished tile: TMEM -> registers (+ the later units' partial
-    // sums, in unit order, when ADD) -> alpha * acc + beta * C (C read here when
-    // rc) -> output.  hold: the accumulator is not handed back here (the caller
-    // first writes the next item's initial value into it).  pf_addr (nonzero):
-    // the single later unit's partial of this warp's rows was prefetched by the
-    // producer lane to this shared address, [BN/4 pieces][32 rows][16 B], its
-    // arrival signalled on pfb[ew].  Returns false if a wait gave up.
-    auto store_tile = [&](auto add_tag, auto fused_tag, uint32_t t_row, int nb, int row0, int buf,
-                          int contrib0, int ncontrib, bool rc, bool hold,
-                          uint32_t pf_addr) -> bool {
+    // sums, already summed in unit order in the TMEM buffer at t_part, when ADD)
+    // -> alpha * acc + beta * C (C read here when rc) -> output.  hold: the
+    // accumulator is not handed back here (the caller first writes the next
+    // item's initial value into it).  Returns false if a wait gave up.
+    auto store_tile = [&](auto add_tag, auto fused_tag, uint32_t t_row, uint32_t t_part, int nb,
+                          int row0, int buf, bool rc, bool hold) -> bool {
       constexpr bool ADD = decltype(add_tag)::value;
       constexpr bool FUSED = decltype(fused_tag)::value;   // bias / activation
-      const uint32_t first = p_issued;
-      const uint32_t total = (ADD && !pf_addr) ? static_cast<uint32_t>(CHUNKS * ncontrib) : 0u;
-      uint64_t pol = 0;
-      // issue copies until number `upto`; copy n = first + c * ncontrib + k
-      // holds chunk c of contributing unit contrib0 + k
-      auto refill = [&](uint32_t upto) {
-        for (; p_issued < upto; ++p_issued) {
-          if (lane != 0) continue;
-          const uint32_t i = p_issued - first;
-          const int c = static_cast<int>(i) / ncontrib, k = static_cast<int>(i) % ncontrib;
-          const float* src = args.ws +
-                             static_cast<size_t>((contrib0 + k) * UNIT_CTAS + rank) * BM * BN +
-                             static_cast<size_t>(quarter) * BN * EPI_ROWS +
-                             static_cast<size_t>(c) * CHUNK * EPI_ROWS;
-          uint64_t* b = &pbar[p_issued % PSLOTS];
-          mbar_arrive_expect_tx(b, PART_BYTES);
-          bulk_load_g2s(pstage + (p_issued % PSLOTS) * PART_BYTES, src, PART_BYTES, b, pol);
-        }
-      };
-      if (ADD && !pf_addr) {
-        if (lane == 0) {
-          pol = policy_evict_first();
-          fence_proxy_async_global();   // the partials were published by other CTAs
-        }
-        refill(first + (total < static_cast<uint32_t>(PSLOTS) ? total : PSLOTS));
-      }
 #pragma unroll 1
       for (int c = 0; c < CHUNKS; ++c) {
-        const int col0 = nb * BN + c * CHUNK;
+        const int pc = c * CHUNK;   // column inside the tile (and in TMEM)
+        const int col0 = nb * BN + pc;
         uint8_t* stg;
         if (!begin_chunk<PAIR, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args, rc))
           return false;
@@ -1042,9 +1017,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool ragged = args.n_ragged && (col0 + CHUNK > args.N);
         const bool skip_store = col0 >= args.N || row0 >= args.M;
         uint32_t v0[32], v1[32];
-        tmem_ld_32x32b_x32(t_row, v0, c * CHUNK);
-        if (CHUNK == 64) tmem_ld_32x32b_x32(t_row, v1, c * CHUNK + 32);
-        tmem_ld_wait();
+        tmem_ld_32x32b_x32(t_row, v0, pc);
+        if (CHUNK == 64) tmem_ld_32x32b_x32(t_row, v1, pc + 32);
+        if (ADD) {
+          uint32_t p0[32], p1[32];
+          tmem_ld_32x32b_x32(t_part, p0, pc);
+          if (CHUNK == 64) tmem_ld_32x32b_x32(t_part, p1, pc + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v0[i] = __float_as_uint(__uint_as_float(v0[i]) + __uint_as_float(p0[i]));
+            if (CHUNK == 64) v1[i] = __float_as_uint(__uint_as_float(v1[i]) + __uint_as_float(p1[i]));
+          }
+        } else {
+          tmem_ld_wait();
+        }
         if (c == CHUNKS - 1 && !hold) {
           // accumulator fully read: hand it back to the MMA issuer
           tc_fence_before();
@@ -1056,50 +1043,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               mbar_arrive_cluster(map_to_rank(&tempty[buf], 0));
           }
         }
-        if (ADD && pf_addr) {
-          if (c == 0 && !wait_warp(&pfb[ew], 0, abort_flag, args, SITE_STREAMK_FLAG)) return false;
-          // piece P = c * CHUNK / 4 + q of row r at (P * 32 + r) * 16
-          const uint32_t pb = pf_addr + static_cast<uint32_t>((c * (CHUNK / 4) * EPI_ROWS + r) * 16);
-#pragma unroll
-          for (int q = 0; q < CHUNK / 4; ++q) {
-            const uint4 pv = ld_shared_v4(pb + q * EPI_ROWS * 16);
-            uint32_t* a = q < 8 ? v0 + 4 * q : v1 + 4 * (q - 8);
-            a[0] = __float_as_uint(__uint_as_float(a[0]) + __uint_as_float(pv.x));
-            a[1] = __float_as_uint(__uint_as_float(a[1]) + __uint_as_float(pv.y));
-            a[2] = __float_as_uint(__uint_as_float(a[2]) + __uint_as_float(pv.z));
-            a[3] = __float_as_uint(__uint_as_float(a[3]) + __uint_as_float(pv.w));
-          }
-        } else if (ADD) {
-          for (int k = 0; k < ncontrib; ++k) {
-            const uint32_t n = first + static_cast<uint32_t>(c * ncontrib + k);
-            if (!wait_warp(&pbar[n % PSLOTS], (n / PSLOTS) & 1, abort_flag, args,
-                           SITE_STREAMK_FLAG))
-              return false;
-            // staged as [CHUNK/4 pieces][32 rows][16 B]: conflict-free rows
-            const uint32_t pb = smem_u32(pstage + (n % PSLOTS) * PART_BYTES) + r * 16;
-#pragma unroll
-            for (int q = 0; q < CHUNK / 4; ++q) {
-              const uint4 pv = ld_shared_v4(pb + q * EPI_ROWS * 16);
-              uint32_t* a = q < 8 ? v0 + 4 * q : v1 + 4 * (q - 8);
-              a[0] = __float_as_uint(__uint_as_float(a[0]) + __uint_as_float(pv.x));
-              a[1] = __float_as_uint(__uint_as_float(a[1]) + __uint_as_float(pv.y));
-              a[2] = __float_as_uint(__uint_as_float(a[2]) + __uint_as_float(pv.z));
-              a[3] = __float_as_uint(__uint_as_float(a[3]) + __uint_as_float(pv.w));
-            }
-            __syncwarp();
-            if (lane == 0) fence_proxy_async_smem();   // slot reads before its next copy
-            p_done = n + 1;
-            refill(p_done + PSLOTS < first + total ? p_done + PSLOTS : first + total);
-          }
-        }
         uint8_t* rowp = stg + r * SW;
         if (FUSED) {
           // this chunk's column-bias registers (static selects: no local memory)
           float cb0 = 0.0f, cb1 = 0.0f;
 #pragma unroll
           for (int q = 0; q < BN / 32; ++q) {
-            if (q == c * (CHUNK / 32)) cb0 = tb[q];
-            if (CHUNK == 64 && q == c * (CHUNK / 32) + 1) cb1 = tb[q];
+            if (q == pc / 32) cb0 = tb[q];
+            if (CHUNK == 64 && q == pc / 32 + 1) cb1 = tb[q];
           }
           fused_chunk<OUT, CHUNK>(v0, v1, rowp, args, rc, cb0, cb1, trb, r);
         }
@@ -1172,14 +1123,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool h0 = wq.next(&w);
     bool h1 = h0 && wq.next(&w1);
     bool h2 = false;
-    uint32_t it_total = 0;   // ring iterations up to and including item tl
     for (; ok && h0; ++tl, w = w1, h0 = h1, w1 = w2, h1 = h2) {
       h2 = h1 && wq.next(&w2);
-      {
-        int kb_b, kb_e;
-        kb_range(w, &kb_b, &kb_e);
-        it_total += static_cast<uint32_t>((kb_e - kb_b + KO - 1) / KO);
-      }
       const bool hold = h2 && item_preloads_c(args, tl + 2, w2);
       const bool rc = args.read_c && !item_preloads_c(args, tl, w);
       int mb, nb;
@@ -1198,6 +1143,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else if (args.bias_kind == EPI_BIAS_ROW) {
           const int rr = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32 + lane;
           trb = rr < args.M ? __ldg(args.bias + rr) : 0.0f;
+        }
+      }
+      // A work item holding its tile's first k-groups but not all of them owns
+      // the tile: the units after it hold the later k-groups and leave partial
+      // sums.  It is always its unit's last item (the last segment of a
+      // stream-K unit, or the only item of a split-tile unit), so the other
+      // accumulator buffer is free: the partials are summed into it while this
+      // item's MMAs run, and the chunk loop adds them from there.
+      const uint32_t t_part = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                              static_cast<uint32_t>((buf ^ 1) * BN);
+      int ncontrib = 0;
+      if (!SPLITK && w.g0 == 0 && w.g1 < args.groups) {
+        int c0, c1;
+        owner_contributors(args, unit0, unit_stride, w, &c0, &c1);
+        ncontrib = c1 - c0;
+        if (h1) {   // not the unit's last item: the work split is broken
+          if (lane == 0) {
+            record_error(args.status, SITE_STREAMK_FLAG);
+            *abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+        if (ncontrib > 0 && !preload_partials(c0, ncontrib, t_part)) {
+          ok = false;
+          break;
         }
       }
       if (!wait_warp<PAIR>(&tfull[buf], aph, abort_flag, args, SITE_EPI_TMEM_FULL)) {
@@ -1289,52 +1260,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         continue;
       }
-      // A stream-K segment holding its tile's first k-groups but not the last
-      // ones owns the tile: the units after it in the iteration space hold the
-      // later k-groups as partial sums.  It is always the last segment of its
-      // unit, so the ring is idle once its accumulator is complete.  With a
-      // single such unit the producer lane has already waited for its flag and
-      // fetched the partial into the draining ring (pf_addr).
-      int contrib0 = unit0, contrib1 = unit0;
-      uint32_t pf_addr = 0;
-      if (w.g1 < args.groups) {
-        const long long base = static_cast<long long>(w.tile - args.dp_tiles) * args.groups;
-        contrib0 = unit0 + 1;
-        contrib1 = sk_unit_of(base + args.groups - 1, unit_stride, args.sk_iters) + 1;
-        if (contrib1 - contrib0 == 1 && !h1) {
-          pf_addr = smem_u32(sk_prefetch_dst(it_total, ew));
-        } else {
-          if (ew == 0 && lane == 0) {
-            for (int u = contrib0; u < contrib1 && !*abort_flag; ++u) {
-              const unsigned int* f = args.ws_flags + u * UNIT_CTAS + rank;
-              const uint64_t t0 = globaltimer_ns();
-              while (flag_acquire(f) != args.epoch) {
-                __nanosleep(64);
-                if (*abort_flag) break;
-                if (globaltimer_ns() - t0 > args.timeout_ns) {
-                  record_error(args.status, SITE_STREAMK_FLAG);
-                  *abort_flag = 1;
-                  break;
-                }
-              }
-            }
-          }
-          if (!epilogue_sync() || *abort_flag) {
-            ok = false;
-            break;
-          }
-        }
-      }
-      const int ncontrib = contrib1 - contrib0;
       // one specialised chunk loop per case, chosen once per tile
       const BoolC<false> no;
       const BoolC<true> yes;
       if (ncontrib == 0)
-        ok = args.epi ? store_tile(no, yes, t_row, nb, row0, buf, 0, 0, rc, hold, 0u)
-                      : store_tile(no, no, t_row, nb, row0, buf, 0, 0, rc, hold, 0u);
+        ok = args.epi ? store_tile(no, yes, t_row, 0u, nb, row0, buf, rc, hold)
+                      : store_tile(no, no, t_row, 0u, nb, row0, buf, rc, hold);
       else
-        ok = args.epi ? store_tile(yes, yes, t_row, nb, row0, buf, contrib0, ncontrib, rc, hold, pf_addr)
-                      : store_tile(yes, no, t_row, nb, row0, buf, contrib0, ncontrib, rc, hold, pf_addr);
+        ok = args.epi ? store_tile(yes, yes, t_row, t_part, nb, row0, buf, rc, hold)
+                      : store_tile(yes, no, t_row, t_part, nb, row0, buf, rc, hold);
       if (ok && hold) {
         preload_c(w2, buf);
         release_acc(buf);
@@ -1346,8 +1280,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (!SPLITK) {
       if (!ok && st.pending_cload >= 0 && lane == 0)
         wait_drain<PAIR>(&st.cload[st.pending_cload], st.pending_phase, args);
-      if (!ok && lane == 0)   // partial copies still landing in the ring
-        for (uint32_t n = p_done; n < p_issued; ++n) wait_drain(&pbar[n % PSLOTS], (n / PSLOTS) & 1, args);
       // the staging buffers must be read out before the CTA exits; the grid's
       // completion makes the stores themselves visible
       if (lane == 0) bulk_wait_group_read<0>();
@@ -1491,8 +1423,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         while (globaltimer_ns() - t0 < 200000ull) {
         }
       }
-      // partial copies into this CTA's ring (stream-K owner prefetch)
-      for (int q = 0; q < pf_issued; ++q) wait_drain(&pfb[q], 0, args);
     }
     if (warp == 1 && lane == 0 && leader) {
       // every MMA already issued (a commit with nothing pending arrives at once)

@@ -118,6 +118,14 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *             over all CTAs (or CTA pairs); a tile's partial sums are added by the
  *             CTA that finishes it, in a fixed order, through a scratch buffer the
  *             library keeps per device and stream.  Ignored with split_k > 1.
+ *             3: split-tile.  Every tile's k-groups are split over split_k CTAs
+ *             (2 to 16; 0 means 2) of one-CTA tiles (bn 64, 128 or 256; 0 means
+ *             128) without a cluster: the first CTA takes the first and larger
+ *             share and finishes the tile, adding the other CTAs' partial sums
+ *             (in CTA order) from the same scratch buffer; each of the others
+ *             takes an even share of the rest.  Needs tiles x split_k <= the SM
+ *             count (GEMM_ERR_UNSUPPORTED otherwise), a k-group (two 64-element
+ *             k-blocks of 16-bit operands) per part, and cta_group 0 or 1.
  *   order     tile order of the persistent scheduler: 1 grouped (group_m
  *             tile-rows at a time, column-major inside the group; the default),
  *             2 Hilbert curve (the order the lecture "The Asynchronous Kernel:
@@ -283,7 +291,9 @@ typedef struct {
                           activation runs a specialised instance (see
                           gemm_config_t.general) */
   int64_t sk_iters;    /* stream-K iterations (tile k-groups) after it; 0 = none */
-  int64_t scratch_bytes; /* stream-K scratch the launch uses (0 = none) */
+  int64_t scratch_bytes; /* stream-K / split-tile scratch the launch uses (0 = none) */
+  int32_t tile_split;  /* split-tile parts per tile (gemm_config_t.stream_k 3); 0 = none */
+  int32_t owner_groups; /* k-groups of the part that finishes a split tile */
 } gemm_plan_t;
 
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int layout,
@@ -309,6 +319,15 @@ int32_t gemm_tile_order(int order, int32_t m_tiles, int32_t n_tiles, int32_t gro
  * items[3*i .. 3*i+2] and returns the number of items the unit has. */
 int32_t gemm_work_items(int32_t unit, int32_t units, int32_t dp_tiles, int64_t sk_iters,
                         int32_t groups, int32_t* items, int32_t max_items);
+
+/* The one work item of unit `unit` under a split-tile plan (gemm_plan_t
+ * tile_split and owner_groups, with the plan's groups), computed on the host
+ * exactly as the kernel walks it: tile unit / tile_split, k-groups [0,
+ * owner_groups) for the first part, an even share of the rest for the others.
+ * Writes (tile, first k-group, end k-group) to item[0..2] and returns the number
+ * of items the unit has (1), or 0 for invalid arguments. */
+int32_t gemm_split_tile_item(int32_t unit, int32_t tile_split, int32_t owner_groups,
+                             int32_t groups, int32_t* item);
 
 /* The tcgen05 descriptor encoders, exposed for host checks.  idesc: kind::f16
  * instruction descriptor; sdesc: 128B-swizzled shared-memory descriptor. */

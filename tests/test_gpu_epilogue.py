@@ -13,9 +13,10 @@ pytestmark = pytest.mark.gpu
 
 MODES = [{"cta_group": 1, "bn": 256}, {"cta_group": 1, "bn": 64}, {"cta_group": 2},
          {"split_k": 2}, {"split_k": 4}, {"split_k": 4, "bn": 64}, {"split_k": 8, "bn": 128},
-         {"cta_group": 1, "stream_k": 2}, {"cta_group": 2, "stream_k": 2}]
+         {"cta_group": 1, "stream_k": 2}, {"cta_group": 2, "stream_k": 2},
+         {"stream_k": 3}, {"stream_k": 3, "split_k": 4, "bn": 64}]
 MODE_IDS = ["cta1", "cta1-bn64", "pair", "splitk2", "splitk4", "splitk4-bn64", "splitk8-bn128",
-            "streamk1", "streamk2"]
+            "streamk1", "streamk2", "splittile2", "splittile4-bn64"]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -199,7 +199,7 @@ def test_stream_k_override(g):
     s, p = g.gemm_plan(1024, 1024, 1024, 1, 1, 0, 152, {"stream_k": 2, "cta_group": 1, "bn": 128})
     assert s == 0 and p.sk_iters == 64 * 8 and p.dp_tiles == 0 and p.grid == 152
     assert p.scratch_bytes == 4096 + 152 * 128 * 128 * 4
-    assert g.gemm_plan(1024, 1024, 1024, 1, 1, 0, 152, {"stream_k": 3})[0] == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_plan(1024, 1024, 1024, 1, 1, 0, 152, {"stream_k": 4})[0] == g.GEMM_ERR_INVALID_ARG
     # split-K plans never stream-K
     s, p = g.gemm_plan(128, 8192, 8192, 1, 1, 2, 152, {"stream_k": 2})
     assert s == 0 and p.split_k == 2 and p.sk_iters == 0
@@ -446,3 +446,42 @@ def test_plan_specialised_flag():
     assert plan(512, 512, 512, 0, 2, 0, 152) == 1   # the single 64-wide CTA
     # 8-bit operands: A row-major with B column-major only
     assert plan(2048, 2048, 2048, 3, 2, 2, 152) == 1
+
+
+def test_split_tile_plans(g):
+    # 128 x 8192 x 8192 bf16, B column-major: 64 tiles of 128 columns, 2 parts each
+    s, p = g.gemm_plan(128, 8192, 8192, 1, 1, 2, 152, {"stream_k": 3})
+    assert s == 0 and p.tile_split == 2 and p.split_k == 1 and p.cta_group == 1 and p.bn == 128
+    assert p.grid == 128 and p.dp_tiles == 0 and p.sk_iters == 0 and p.groups == 64
+    assert p.owner_groups == 35   # 32 + a tenth of the tile's k-groups over the 2 parts
+    assert p.scratch_bytes == 4096 + 128 * 128 * 128 * 4
+    s, p = g.gemm_plan(128, 8192, 8192, 1, 1, 2, 152, {"stream_k": 3, "split_k": 4, "bn": 256})
+    assert s == 0 and p.tile_split == 4 and p.grid == 128 and p.owner_groups == 20
+    # more units than SMs, a part without a k-group, a CTA pair: refused
+    assert g.gemm_plan(1024, 1024, 1024, 1, 1, 0, 152, {"stream_k": 3, "split_k": 4, "bn": 64})[0] == \
+        g.GEMM_ERR_UNSUPPORTED
+    assert g.gemm_plan(128, 1024, 128, 1, 1, 0, 152, {"stream_k": 3})[0] == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_plan(256, 1024, 4096, 1, 1, 0, 152, {"stream_k": 3, "cta_group": 2})[0] == \
+        g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_plan(128, 1024, 4096, 1, 1, 0, 152, {"stream_k": 3, "split_k": 17})[0] == \
+        g.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("parts,groups", [(2, 64), (2, 2), (3, 7), (4, 64), (8, 33), (16, 16)])
+def test_split_tile_items_cover_each_tile_once(g, parts, groups):
+    """Every k-group of a tile is held by exactly one of its parts; the first part
+    (the owner) starts at k-group 0 and holds the largest share."""
+    extra = max(1, groups // 10)
+    owner = min((groups + (parts - 1) * extra) // parts, groups - (parts - 1))
+    for tile in range(3):
+        items = [g.gemm_split_tile_item(tile * parts + q, parts, owner, groups) for q in range(parts)]
+        assert all(it is not None and it[0] == tile for it in items)
+        covered = []
+        for (_, g0, g1) in items:
+            assert g0 < g1
+            covered.extend(range(g0, g1))
+        assert sorted(covered) == list(range(groups))
+        assert items[0][1] == 0 and items[0][2] == owner
+        shares = [g1 - g0 for (_, g0, g1) in items]
+        assert shares[0] == max(shares)
+    assert g.gemm_split_tile_item(0, 1, 1, groups) is None

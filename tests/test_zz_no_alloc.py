@@ -1,5 +1,5 @@
-"""gemm_ex_noalloc: the stream-K launch with its scratch in the library's fixed
-per-device buffer instead of memory from cudaMalloc.
+"""gemm_ex_noalloc: the stream-K and split-tile launches with their scratch in
+the library's fixed per-device buffer instead of memory from cudaMalloc.
 
 It exists for callers that cannot allocate device memory on the call path: a
 framework whose caching allocator already holds the GPU's memory, or a serving
@@ -36,11 +36,13 @@ ORDER_HILBERT = 2
 
 # (M, N, K, cfg, in dtype, out dtype, alpha, beta): stream-K on CTA-pair tiles of
 # 256 x 256 over every SM (the largest scratch a 152-SM GPU can need), and on
-# single-CTA 128-wide tiles with a ragged shape and beta != 0.
+# single-CTA 128-wide tiles with a ragged shape and beta != 0; the split-tile
+# plan of a 128-row panel (every tile split over two CTAs through the scratch).
 CASES = [
     (2048, 2048, 2048, {"stream_k": 2, "cta_group": 2}, torch.float16, torch.float32, 1.0, 0.0),
     (1000, 1096, 1504, {"stream_k": 2, "cta_group": 1, "bn": 128}, torch.bfloat16,
      torch.bfloat16, 0.75, -0.5),
+    (128, 8192, 8192, {"stream_k": 3}, torch.bfloat16, torch.bfloat16, 1.0, 0.0),
 ]
 
 
@@ -65,7 +67,8 @@ def _call(fn, a, b, c, alpha, beta, cfg, stream):
 def _check_plan(g, M, N, K, idt, odt, cfg):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     s, p = g.gemm_plan(M, N, K, CODE[idt], CODE[odt], 0, sms, cfg)
-    assert s == g.GEMM_OK and p.sk_iters > 0, "case does not exercise stream-K"
+    assert s == g.GEMM_OK and (p.sk_iters > 0 or p.tile_split > 0), \
+        "case does not use the scratch"
     assert 0 < p.scratch_bytes <= g.GEMM_NOALLOC_SCRATCH_BYTES
 
 
@@ -93,7 +96,8 @@ def _noalloc_twice(g, a, b, c0, alpha, beta, cfg):
     return outs
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-cta{c[3]['cta_group']}")
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-" +
+                         "-".join(f"{k}{v}" for k, v in c[3].items()))
 def test_noalloc_matches_gemm_ex_twice(g, case):
     M, N, K, cfg, idt, odt, alpha, beta = case
     _check_plan(g, M, N, K, idt, odt, cfg)
