@@ -17,7 +17,7 @@ _BINDING_NAMES = frozenset((
     "GEMM_NOALLOC_SCRATCH_BYTES", "GEMM_OK", "GEMM_ORDER_AUTO", "GEMM_ORDER_GROUPED",
     "GEMM_ORDER_HILBERT", "LIB_PATH", "GemmError",
     "gemm", "gemm_config_t", "gemm_debug_set", "gemm_encode_idesc", "gemm_encode_sdesc",
-    "gemm_bias_act", "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_plan", "gemm_plan_t", "gemm_split_tile_item",
+    "gemm_bias_act", "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_plan", "gemm_plan_t", "gemm_split_tile_item", "gemm_fastdiv",
     "gemm_sync_status",
     "gemm_tile_coord", "gemm_tile_order", "gemm_version", "gemm_work_items", "library", "matmul", "status_string"))
 

@@ -26,7 +26,7 @@ GEMM_ORDER_AUTO, GEMM_ORDER_GROUPED, GEMM_ORDER_HILBERT = 0, 1, 2
 EXPORTS = ("gemm", "gemm_bias_act", "gemm_ex", "gemm_ex_noalloc", "gemm_host", "gemm_status_string",
            "gemm_sync_status",
            "gemm_debug_set", "gemm_plan", "gemm_tile_coord", "gemm_tile_order", "gemm_work_items",
-           "gemm_split_tile_item",
+           "gemm_split_tile_item", "gemm_fastdiv",
            "gemm_encode_idesc", "gemm_encode_sdesc", "gemm_version")
 
 
@@ -89,6 +89,8 @@ def _load():
     lib.gemm_tile_order.restype = i32
     lib.gemm_work_items.argtypes = [i32, i32, i32, i64, i32, ctypes.POINTER(i32), i32]
     lib.gemm_work_items.restype = i32
+    lib.gemm_fastdiv.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+    lib.gemm_fastdiv.restype = ctypes.c_uint32
     lib.gemm_split_tile_item.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32)]
     lib.gemm_split_tile_item.restype = i32
     lib.gemm_encode_idesc.argtypes = [ci, ci, ci, ci, ci]
@@ -203,6 +205,11 @@ def gemm_split_tile_item(unit, tile_split, owner_groups, groups):
     buf = (ctypes.c_int32 * 3)()
     n = _lib.gemm_split_tile_item(unit, tile_split, owner_groups, groups, buf)
     return tuple(buf) if n == 1 else None
+
+
+def gemm_fastdiv(n, d):
+    """n // d the kernel's way (multiply and shift); 0xFFFFFFFF out of range."""
+    return _lib.gemm_fastdiv(n, d)
 
 
 def gemm_encode_idesc(in_dtype, a_mn, b_mn, m, n):

@@ -662,6 +662,12 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.act = act;
   ka.epi = (bias_kind != GEMM_BIAS_NONE || act != GEMM_ACT_NONE) ? 1 : 0;
   ka.tile_map = nullptr;
+  {
+    const int64_t groups_m = ceil_div(p.m_tiles, p.group_m);
+    ka.fd_group = make_fastdiv(static_cast<uint32_t>(p.group_m) * static_cast<uint32_t>(p.n_tiles));
+    ka.fd_rows = make_fastdiv(static_cast<uint32_t>(p.group_m));
+    ka.fd_last_rows = make_fastdiv(static_cast<uint32_t>(p.m_tiles - (groups_m - 1) * p.group_m));
+  }
   // beta * C goes into the accumulator ahead of the MMAs (persistent launches
   // with alpha == 1; a split-K cluster's CTAs each hold only part of the sum)
   ka.pre_c = (alpha == 1.0f && beta != 0.0f && p.split_k == 1) ? 1 : 0;
@@ -862,10 +868,16 @@ int32_t gemm_tile_order(int order, int32_t m_tiles, int32_t n_tiles, int32_t gro
   if (m_tiles <= 0 || n_tiles <= 0 || !m_blk || !n_blk || max_tiles < 0) return -1;
   const int64_t tiles = int64_t(m_tiles) * n_tiles;
   if (order == GEMM_ORDER_GROUPED) {
-    if (group_m <= 0) return -1;
+    if (group_m <= 0 || tiles >= (int64_t(1) << 31)) return -1;
+    // the device's walk: the divisions by the group size and row counts done by
+    // fastdiv (a group_m above m_tiles orders the tiles as m_tiles does)
+    const int gmc = std::min(group_m, m_tiles);
+    const FastDiv gs = make_fastdiv(static_cast<uint32_t>(gmc) * static_cast<uint32_t>(n_tiles));
+    const FastDiv gm = make_fastdiv(static_cast<uint32_t>(gmc));
+    const FastDiv gl = make_fastdiv(static_cast<uint32_t>(m_tiles - (ceil_div(m_tiles, gmc) - 1) * gmc));
     for (int64_t t = 0; t < tiles && t < max_tiles; ++t) {
       int m = 0, n = 0;
-      tile_coord(static_cast<int>(t), m_tiles, n_tiles, group_m, &m, &n);
+      tile_coord_fast(static_cast<int>(t), m_tiles, gmc, gs, gm, gl, &m, &n);
       m_blk[t] = m;
       n_blk[t] = n;
     }
@@ -917,6 +929,12 @@ int32_t gemm_split_tile_item(int32_t unit, int32_t tile_split, int32_t owner_gro
   int32_t n = 1;
   while (wi.next(&w)) ++n;
   return n;
+}
+
+uint32_t gemm_fastdiv(uint32_t n, uint32_t d) {
+  if (d == 0 || d >= (1u << 31) || n >= (1u << 31)) return 0xFFFFFFFFu;
+  const FastDiv f = make_fastdiv(d);
+  return fastdiv(n, f.mul, f.shift);
 }
 
 uint32_t gemm_encode_idesc(int in_dtype, int a_mn, int b_mn, int m, int n) {

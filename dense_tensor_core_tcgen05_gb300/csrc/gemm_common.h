@@ -35,6 +35,52 @@ GEMM_HD void tile_coord(int t, int m_tiles, int n_tiles, int group_m, int* m_blk
   *n_blk = r / rows_in_group;
 }
 
+// Division by a run-time constant d (1 <= d < 2^31) of numerators n in
+// [0, 2^31) by a multiply and a shift, the constants worked out once on the host
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994: l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1,
+// q = (mulhi(m, n) + n) >> l; with n < 2^31 the sum cannot overflow 32 bits).
+// The device's own integer division is a long dependent instruction sequence,
+// and the tile order divides on the producer's path to its first copy.
+struct FastDiv {
+  uint32_t d, mul, shift;
+};
+
+GEMM_HD FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  f.shift = l;
+  f.mul = static_cast<uint32_t>((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+  return f;
+}
+
+GEMM_HD uint32_t fastdiv(uint32_t n, uint32_t mul, uint32_t shift) {
+#if defined(__CUDA_ARCH__)
+  const uint32_t t = __umulhi(n, mul);
+#else
+  const uint32_t t = static_cast<uint32_t>((static_cast<uint64_t>(n) * mul) >> 32);
+#endif
+  return (t + n) >> shift;
+}
+
+// The grouped order of tile_coord with its divisions by the group size (in
+// tiles) and by a group's row count (group_m, or the last group's rows) done by
+// fastdiv; gs, gm and gl are make_fastdiv of those three.
+GEMM_HD void tile_coord_fast(int t, int m_tiles, int group_m, const FastDiv& gs, const FastDiv& gm,
+                             const FastDiv& gl, int* m_blk, int* n_blk) {
+  const int g = static_cast<int>(fastdiv(static_cast<uint32_t>(t), gs.mul, gs.shift));
+  const int first_m = g * group_m;
+  const int r = t - g * static_cast<int>(gs.d);
+  const bool last = m_tiles - first_m < group_m;
+  const uint32_t rows = last ? gl.d : gm.d;
+  const int n = static_cast<int>(fastdiv(static_cast<uint32_t>(r), last ? gl.mul : gm.mul,
+                                         last ? gl.shift : gm.shift));
+  *m_blk = first_m + (r - n * static_cast<int>(rows));
+  *n_blk = n;
+}
+
 // Cell (x, y) at index d of the Hilbert curve over a 2^k x 2^k grid (the order the
 // lecture "The Asynchronous Kernel: Tensor Cores & TMA" compares in "Scheduling
 // is geometry": a space-filling curve whose every prefix stays compact).  Built
@@ -115,22 +161,25 @@ struct WorkItem {
 // k-groups evenly and leave partial sums.  The owner's share is the larger one,
 // so the other parts finish (and publish) while it is still accumulating.
 struct WorkIter {
-  int units, dp_tiles, groups, next_dp;
+  int units, dp_tiles, groups, next_dp, unit;
   long long i, hi, sk_iters;
   int st_tile, st_g0, st_g1;   // split-tile: the unit's one item (st_tile < 0: taken)
-  GEMM_HD void init(int unit, int units_, int dp_tiles_, long long sk_iters_, int groups_,
+  bool sk_ready;               // the stream-K range [i, hi) has been worked out
+  GEMM_HD void init(int unit_, int units_, int dp_tiles_, long long sk_iters_, int groups_,
                     int tile_split = 0, int owner_groups = 0) {
     units = units_;
     dp_tiles = dp_tiles_;
     groups = groups_;
-    next_dp = unit;
+    next_dp = unit_;
+    unit = unit_;
     sk_iters = sk_iters_;
     i = hi = 0;
+    sk_ready = false;
     st_tile = -1;
     st_g0 = st_g1 = 0;
     if (tile_split > 1) {
-      const int part = unit % tile_split;
-      st_tile = unit / tile_split;
+      const int part = unit_ % tile_split;
+      st_tile = unit_ / tile_split;
       if (part == 0) {
         st_g1 = owner_groups;
       } else {
@@ -140,9 +189,6 @@ struct WorkIter {
       }
       dp_tiles = 0;
       sk_iters = 0;
-    } else if (sk_iters != 0) {   // 64-bit divisions only for stream-K plans (slow on the device)
-      i = (static_cast<long long>(unit) * sk_iters) / units;
-      hi = (static_cast<long long>(unit + 1) * sk_iters) / units;
     }
   }
   GEMM_HD bool next(WorkItem* w) {
@@ -159,6 +205,14 @@ struct WorkIter {
       w->g1 = groups;
       next_dp += units;
       return true;
+    }
+    if (sk_iters != 0 && !sk_ready) {
+      // The unit's stream-K range, worked out only once its data-parallel tiles
+      // are handed out: 64-bit divisions are slow on the device, and the first
+      // item of a unit with data-parallel tiles must not wait for them.
+      i = (static_cast<long long>(unit) * sk_iters) / units;
+      hi = (static_cast<long long>(unit + 1) * sk_iters) / units;
+      sk_ready = true;
     }
     if (i < hi) {
       const long long t = i / groups;
@@ -189,36 +243,19 @@ enum { EPI_ACT_NONE = 0, EPI_ACT_RELU = 1 };
 
 // Kernel arguments (plain data, built on the host).
 struct KernelArgs {
-  int M, N, K;
-  int m_tiles, n_tiles, k_blocks, num_tiles, group_m;
-  float alpha, beta;
-  uint32_t idesc;        // tcgen05 instruction descriptor (formats, majors, M, N)
-  int a_mn, b_mn;        // 1: operand is MN-major in memory (A column-major / B row-major)
-  int read_c;            // beta != 0
-  int* status;           // device status word (0 = ok)
-  unsigned long long timeout_ns;
-  int inject_skip;       // debug: the producer leaves ring iteration (inject_skip - 1) unarmed
-  void* c_ptr;           // C base (for the ragged right edge, written with plain stores)
-  long long ldc;         // C leading dimension in elements
-  int n_ragged;          // 1 when N * sizeof(out) is not a multiple of 16 bytes
+  // The fields the producer and the MMA issuer read before their first copy and
+  // first MMA come first, so that those reads touch few constant-cache lines
+  // (each line a kernel's CTAs first read costs a round trip to memory).
+  int m_tiles, n_tiles, group_m, k_blocks;
+  // Work split (see WorkIter): k-groups per tile, whole tiles of the
+  // data-parallel phase, stream-K iterations after it; or the split-tile
+  // schedule's parts per tile (0: not used) and the k-groups of its owning part.
+  int groups, dp_tiles, tile_split, owner_groups;
   int a_hint, b_hint;    // L2 policy of the operand loads: 0 default, 1 evict first, 2 evict last
+  int a_mn, b_mn;        // 1: operand is MN-major in memory (A column-major / B row-major)
   // Extent of the 3-D operand maps in whole 64-element blocks (0: no 3-D map):
   // K-major operand -> full k-blocks (K / 64); MN-major -> full 64-wide atoms.
   int a_full3d, b_full3d;
-  // Work split (see WorkIter): k-groups per tile, whole tiles of the
-  // data-parallel phase, stream-K iterations after it.
-  int groups, dp_tiles;
-  long long sk_iters;
-  // Stream-K scratch: one fp32 partial tile slot and one ready flag per CTA;
-  // a flag holds the epoch of the launch whose partial is in the slot.
-  float* ws;
-  unsigned int* ws_flags;
-  unsigned int epoch;
-  // Fused epilogue: out = act(alpha*acc + beta*C + bias) before the rounding.
-  const float* bias;     // N floats (EPI_BIAS_COL) or M floats (EPI_BIAS_ROW), 16-byte aligned
-  int bias_kind;         // EPI_BIAS_*
-  int act;               // EPI_ACT_*
-  int epi;               // 1 when bias_kind or act is set (selects the fused epilogue)
   // K elements of one k-block (64 for 16-bit operands, 128 for 8-bit ones: one
   // 128-byte swizzled row either way).
   int kblock_elems;
@@ -226,16 +263,38 @@ struct KernelArgs {
   // with M < BM: the rows of smem beyond them only feed accumulator rows >= M,
   // which are never stored).
   int a_box_rows;
+  long long sk_iters;
+  unsigned long long timeout_ns;
+  int* status;           // device status word (0 = ok)
   // Tile order: NULL = grouped (tile_coord), else (m block, n block) of tile t
   // in Hilbert-curve order, num_tiles entries.
   const int2* tile_map;
+  // The grouped order's divisors (tile_coord_fast): group size in tiles
+  // (group_m * n_tiles), group_m, and the last group's row count.
+  FastDiv fd_group, fd_rows, fd_last_rows;
+  uint32_t idesc;        // tcgen05 instruction descriptor (formats, majors, M, N)
+  int read_c;            // beta != 0
   // 1: beta * C is written into a tile's TMEM accumulator before its first MMA
   // (alpha == 1 only, so the accumulator then holds alpha*AB + beta*C), for every
   // work item after a unit's first two that holds its tile's first k-groups.
   int pre_c;
-  // Split-tile schedule (see WorkIter): parts per tile (0: not used) and the
-  // k-groups of the owning part.
-  int tile_split, owner_groups;
+  int inject_skip;       // debug: the producer leaves ring iteration (inject_skip - 1) unarmed
+  int num_tiles;
+  int M, N, K;
+  float alpha, beta;
+  void* c_ptr;           // C base (for the ragged right edge, written with plain stores)
+  long long ldc;         // C leading dimension in elements
+  int n_ragged;          // 1 when N * sizeof(out) is not a multiple of 16 bytes
+  // Stream-K scratch: one fp32 partial tile slot and one ready flag per CTA;
+  // a flag holds the epoch of the launch whose partial is in the slot.
+  unsigned int epoch;
+  float* ws;
+  unsigned int* ws_flags;
+  // Fused epilogue: out = act(alpha*acc + beta*C + bias) before the rounding.
+  const float* bias;     // N floats (EPI_BIAS_COL) or M floats (EPI_BIAS_ROW), 16-byte aligned
+  int bias_kind;         // EPI_BIAS_*
+  int act;               // EPI_ACT_*
+  int epi;               // 1 when bias_kind or act is set (selects the fused epilogue)
 };
 
 // Whether work item number `tl` of a unit (item `w`) starts from an accumulator
@@ -266,7 +325,7 @@ __device__ __forceinline__ void tile_of(const KernelArgs& a, int t, int* m_blk, 
     *m_blk = v.x;
     *n_blk = v.y;
   } else {
-    tile_coord(t, a.m_tiles, a.n_tiles, a.group_m, m_blk, n_blk);
+    tile_coord_fast(t, a.m_tiles, a.group_m, a.fd_group, a.fd_rows, a.fd_last_rows, m_blk, n_blk);
   }
 }
 #endif

@@ -721,8 +721,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool have = false;
     int mb = 0, nb = 0;
     if (lane == 0) {
-      pol_a = args.a_hint == 1 ? policy_evict_first() : policy_evict_last();
-      pol_b = args.b_hint == 1 ? policy_evict_first() : policy_evict_last();
+      // (made only when used: a copy without a hint needs none)
+      if (args.a_hint) pol_a = args.a_hint == 1 ? policy_evict_first() : policy_evict_last();
+      if (args.b_hint) pol_b = args.b_hint == 1 ? policy_evict_first() : policy_evict_last();
       work_begin(wi);
       have = wi.next(&w);
       if (have) tile_of(args, w.tile, &mb, &nb);
@@ -957,38 +958,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto preload_partials = [&](int c0, int n, uint32_t t_part) -> bool {
       for (int k = 0; k < n; ++k)
         if (!wait_flag_warp(args.ws_flags + (c0 + k) * UNIT_CTAS + rank)) return false;
-      static_assert((BN / 32) % 2 == 0, "partials are preloaded 64 columns at a time");
+      // Each round loads GR 32-column groups (8 x 16 B per lane each) before
+      // writing any to TMEM, so 128 B per lane and group are in flight: the
+      // partials come from L2 while it serves the mainloop's operand traffic.
+      // Contributor 0 is stored, the later ones are added to what is stored.
+      constexpr int GR = BN / 32 < 4 ? BN / 32 : 4;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; c += 2) {
-        uint32_t s0[32], s1[32];
+      for (int k = 0; k < n; ++k) {
+        const float4* src = reinterpret_cast<const float4*>(
+            args.ws + static_cast<size_t>((c0 + k) * UNIT_CTAS + rank) * BM * BN +
+            static_cast<size_t>(quarter) * BN * EPI_ROWS) + lane;
 #pragma unroll 1
-        for (int k = 0; k < n; ++k) {
-          const float4* src = reinterpret_cast<const float4*>(
-              args.ws + static_cast<size_t>((c0 + k) * UNIT_CTAS + rank) * BM * BN +
-              static_cast<size_t>(quarter) * BN * EPI_ROWS) + static_cast<size_t>(c) * 8 * EPI_ROWS + lane;
-          float4 v[16];
+        for (int c = 0; c < BN / 32; c += GR) {
+          float4 v[8 * GR];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __ldcg(src + j * EPI_ROWS);
+          for (int j = 0; j < 8 * GR; ++j) v[j] = __ldcg(src + static_cast<size_t>(c * 8 + j) * EPI_ROWS);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            uint32_t* d = j < 8 ? s0 + 4 * j : s1 + 4 * (j - 8);
-            if (k == 0) {
-              d[0] = __float_as_uint(v[j].x);
-              d[1] = __float_as_uint(v[j].y);
-              d[2] = __float_as_uint(v[j].z);
-              d[3] = __float_as_uint(v[j].w);
-            } else {
-              d[0] = __float_as_uint(__uint_as_float(d[0]) + v[j].x);
-              d[1] = __float_as_uint(__uint_as_float(d[1]) + v[j].y);
-              d[2] = __float_as_uint(__uint_as_float(d[2]) + v[j].z);
-              d[3] = __float_as_uint(__uint_as_float(d[3]) + v[j].w);
+          for (int q = 0; q < GR; ++q) {
+            uint32_t r[32];
+            if (k > 0) {
+              tmem_ld_32x32b_x32(t_part, r, (c + q) * 32);
+              tmem_ld_wait();
             }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 f = v[8 * q + j];
+              if (k == 0) {
+                r[4 * j] = __float_as_uint(f.x);
+                r[4 * j + 1] = __float_as_uint(f.y);
+                r[4 * j + 2] = __float_as_uint(f.z);
+                r[4 * j + 3] = __float_as_uint(f.w);
+              } else {
+                r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + f.x);
+                r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + f.y);
+                r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + f.z);
+                r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + f.w);
+              }
+            }
+            tmem_st_32x32b_x32(t_part, r, (c + q) * 32);
           }
         }
-        tmem_st_32x32b_x32(t_part, s0, c * 32);
-        tmem_st_32x32b_x32(t_part, s1, c * 32 + 32);
+        tmem_st_wait();   // stored before the next contributor's sums read them back
       }
-      tmem_st_wait();
       return true;
     };
 

@@ -308,7 +308,9 @@ void gemm_tile_coord(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_
 /* A whole tile order on the host: order GEMM_ORDER_GROUPED (with group_m) or
  * GEMM_ORDER_HILBERT; writes the (m_blk, n_blk) of tiles 0 .. m_tiles*n_tiles-1
  * (at most max_tiles of them) and returns the tile count, or -1 when the order
- * is unknown or (Hilbert) not used for this grid shape. */
+ * is unknown or (Hilbert) not used for this grid shape.  The grouped order is
+ * computed the kernel's way (gemm_fastdiv divisions); gemm_tile_coord computes
+ * it with plain division, so the two agree tile for tile. */
 int32_t gemm_tile_order(int order, int32_t m_tiles, int32_t n_tiles, int32_t group_m,
                         int32_t* m_blk, int32_t* n_blk, int32_t max_tiles);
 
@@ -328,6 +330,11 @@ int32_t gemm_work_items(int32_t unit, int32_t units, int32_t dp_tiles, int64_t s
  * of items the unit has (1), or 0 for invalid arguments. */
 int32_t gemm_split_tile_item(int32_t unit, int32_t tile_split, int32_t owner_groups,
                              int32_t groups, int32_t* item);
+
+/* n / d as the kernel divides by a run-time constant (a multiply and a shift
+ * with host-computed constants), for host checks: 1 <= d < 2^31 and n < 2^31;
+ * returns 0xFFFFFFFF for arguments outside that range. */
+uint32_t gemm_fastdiv(uint32_t n, uint32_t d);
 
 /* The tcgen05 descriptor encoders, exposed for host checks.  idesc: kind::f16
  * instruction descriptor; sdesc: 128B-swizzled shared-memory descriptor. */

@@ -485,3 +485,37 @@ def test_split_tile_items_cover_each_tile_once(g, parts, groups):
         shares = [g1 - g0 for (_, g0, g1) in items]
         assert shares[0] == max(shares)
     assert g.gemm_split_tile_item(0, 1, 1, groups) is None
+
+
+def test_fastdiv_matches_integer_division(g):
+    """The kernel divides by run-time constants with a multiply and a shift
+    (Granlund-Montgomery); it must equal integer division for every divisor and
+    numerator below 2^31: small and power-of-two divisors, divisors next to powers
+    of two, and numerators at the top of the range and at multiples of d."""
+    rng = np.random.default_rng(5)
+    ds = [1, 2, 3, 5, 6, 7, 9, 76, 152, 255, 256, 257, 1000, 65535, 65536, 65537,
+          (1 << 30) - 1, 1 << 30, (1 << 30) + 1, (1 << 31) - 1]
+    ds += [int(x) for x in rng.integers(1, 1 << 31, size=60)]
+    for d in ds:
+        ns = [0, 1, d - 1, d, d + 1, 2 * d - 1, 2 * d, (1 << 31) - 1, (1 << 31) - 2]
+        ns += [int(x) for x in rng.integers(0, 1 << 31, size=40)]
+        ns += [(k * d) % (1 << 31) for k in range(1, 6)] + [((k * d) - 1) % (1 << 31) for k in range(1, 6)]
+        for n in ns:
+            if 0 <= n < (1 << 31):
+                assert g.gemm_fastdiv(n, d) == n // d, (n, d)
+    assert g.gemm_fastdiv(5, 0) == 0xFFFFFFFF
+    assert g.gemm_fastdiv(1 << 31, 3) == 0xFFFFFFFF
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_grouped_order_kernel_walk_matches_definition(g, seed):
+    """gemm_tile_order walks the grouped order the kernel's way (fastdiv);
+    gemm_tile_coord computes the definition with plain division."""
+    rng = np.random.default_rng(100 + seed)
+    for _ in range(8):
+        mt, nt = int(rng.integers(1, 70)), int(rng.integers(1, 70))
+        gm = int(rng.integers(1, 20))
+        order = g.gemm_tile_order(1, mt, nt, gm)
+        assert order is not None and len(order) == mt * nt
+        for t in range(mt * nt):
+            assert order[t] == g.gemm_tile_coord(t, mt, nt, gm), (mt, nt, gm, t)
