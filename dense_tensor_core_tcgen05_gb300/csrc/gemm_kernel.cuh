@@ -678,6 +678,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // cluster barrier below orders this before the peer's copy
     if (EARLY && lane == 0) mbar_arrive_expect_tx(rfull, SLICE_BYTES);
   }
+  // Pair mode, phase 1 of the cluster barrier: both CTAs' mbarriers exist (the
+  // odd CTA's copies and the MMA commits signal the leader's and the peer's).
+  // Warp 0 arrives after initialising them (relaxed: fence.mbarrier_init has
+  // published them), every other warp at once, before the TMEM allocation.
+  if (PAIR) cluster_arrive_relaxed();
   if (warp == 2) {
     if (lane == 0) prefetch_tensormap(&tmA);
     if (lane == 1) prefetch_tensormap(&tmB);
@@ -696,10 +701,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   __syncwarp();
   tc_fence_before();
-  // both CTAs' barriers exist before any cross-CTA signal (pair mode); the
-  // barriers and the TMEM address are visible to every role
+  // The barriers (and, for every role but the producer, the TMEM address) are
+  // visible before use.  Pair mode, phase 2: TMEM is allocated in both CTAs
+  // (the leader's MMAs write both); warp 1 arrives after allocating, with
+  // release for the address it wrote.  The producer waits for phase 1 only and
+  // for phase 2 at the end, so its first copies do not wait for the allocation.
   if (PAIR) {
-    cluster_arrive();
+    cluster_wait();
+    if (warp == 1)
+      cluster_arrive();
+    else
+      cluster_arrive_relaxed();
     if (warp != 0) cluster_wait();
   } else if (warp == 0) {
     named_bar_arrive(1, NUM_THREADS);
@@ -709,7 +721,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // early split-K exchange: every CTA's barriers exist before a peer copies into
   // it (waited for by the epilogue warps before their copies, by the others at
   // the end)
-  if (EARLY) cluster_arrive();
+  if (EARLY) {
+    if (warp == 0)
+      cluster_arrive_relaxed();
+    else
+      cluster_arrive();
+  }
   tc_fence_after();
   const uint32_t tmem_base = warp == 0 ? 0u : *tmem_slot;   // warp 0 never touches TMEM
 
@@ -721,16 +738,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool have = false;
     int mb = 0, nb = 0;
     if (lane == 0) {
-      // (made only when used: a copy without a hint needs none)
-      if (args.a_hint) pol_a = args.a_hint == 1 ? policy_evict_first() : policy_evict_last();
-      if (args.b_hint) pol_b = args.b_hint == 1 ? policy_evict_first() : policy_evict_last();
       work_begin(wi);
       have = wi.next(&w);
       if (have) tile_of(args, w.tile, &mb, &nb);
-    }
-    if (PAIR) {
-      __syncwarp();
-      cluster_wait();
     }
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer
@@ -745,6 +755,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int nkb = kb_end - kb0 < KO ? kb_end - kb0 : KO;
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
+          if (it == 1) {   // the L2 policies of every copy after the first stage's
+            if (args.a_hint) pol_a = args.a_hint == 1 ? policy_evict_first() : policy_evict_last();
+            if (args.b_hint) pol_b = args.b_hint == 1 ? policy_evict_first() : policy_evict_last();
+          }
           if (!wait_one<PAIR>(&empty[s], ph ^ 1, abort_flag, args, SITE_PRODUCER_EMPTY)) {
             ok = false;
             break;
@@ -798,9 +812,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
             }
           };
-          load_operand(sa, &tmA, &tmA3, args.a_mn, BM, a_row, args.a_full3d, args.a_hint, pol_a);
-          load_operand(sb, &tmB, &tmB3, args.b_mn, L::B_COLS, b_col, args.b_full3d, args.b_hint,
-                       pol_b);
+          // the first stage goes out without L2 hints: their policies are made
+          // after it is issued (createpolicy is slow enough to delay the first copy)
+          const bool hinted = it != 0;
+          load_operand(sa, &tmA, &tmA3, args.a_mn, BM, a_row, args.a_full3d, hinted ? args.a_hint : 0,
+                       pol_a);
+          load_operand(sb, &tmB, &tmB3, args.b_mn, L::B_COLS, b_col, args.b_full3d,
+                       hinted ? args.b_hint : 0, pol_b);
+
         }
         have = wi.next(&w);
         if (have) tile_of(args, w.tile, &mb, &nb);
@@ -1187,6 +1206,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
+      // the C map's descriptor back in the TMA unit's cache before this tile's
+      // stores (its prefetch at start-up may have been evicted long ago)
+      if (ew == 0 && lane == 0) prefetch_tensormap(&tmC);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
       const int row0 = mb * TILE_M + static_cast<int>(rank) * BM + quarter * 32;
@@ -1299,6 +1321,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   if (EARLY && warp < EPI_WARP0) {   // the start-up cluster barrier, for the other roles
+    __syncwarp();
+    cluster_wait();
+  }
+  if (PAIR && warp == 0) {   // phase 2 of the start-up barrier, for the producer
     __syncwarp();
     cluster_wait();
   }
