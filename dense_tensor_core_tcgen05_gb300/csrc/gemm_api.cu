@@ -478,10 +478,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   p->cta_group = pair ? 2 : 1;
   // the conditions of run_gemm's plain path that the plan itself fixes
   p->specialised = (p->order == GEMM_ORDER_GROUPED && !(cfg && cfg->general) &&
-                    (N * out_size(out_dtype)) % 16 == 0 &&
                     spec_supported(bn, pair, split, layout, is_fp8(in_dtype),
-                                   p->sk_iters != 0 || tile_split != 0,
-                                   false, false))
+                                   p->sk_iters != 0 || tile_split != 0, false, false,
+                                   (N * out_size(out_dtype)) % 16 != 0))
                        ? 1
                        : 0;
   return GEMM_OK;
@@ -685,26 +684,29 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
 
   // A call on the plain path takes the specialised instance of its
   // configuration and layout when there is one (cfg->general = 1 forbids it).
-  const bool plain = !(cfg && cfg->general) && !ka.n_ragged && ka.inject_skip == 0 &&
-                     ka.tile_map == nullptr;
+  const bool plain = !(cfg && cfg->general) && ka.inject_skip == 0 && ka.tile_map == nullptr;
   const bool sk = ka.sk_iters != 0 || ka.tile_split != 0, readc = ka.read_c != 0, epi = ka.epi != 0;
+  const bool ragged = ka.n_ragged != 0;
   cudaError_t e = cudaErrorNotSupported;
   if (plain) {
-    using SpecLaunch = cudaError_t (*)(int, bool, int, int, bool, bool, bool, const OperandMaps&,
-                                       const KernelArgs&, int, cudaStream_t, int);
+    using SpecLaunch = cudaError_t (*)(int, bool, int, int, bool, bool, bool, bool,
+                                       const OperandMaps&, const KernelArgs&, int, cudaStream_t, int);
     const bool f8 = is_fp8(in_dtype);
-    const bool set2 = spec_set(p.bn, pair, p.split_k, sk, readc, epi) == 2;
+    const int set = spec_set(p.bn, pair, p.split_k, sk, readc, epi, ragged);
     const SpecLaunch launch =
         f8 ? (out_dtype == GEMM_F32    ? launch_gemm_f8_spec_f32
               : out_dtype == GEMM_BF16 ? launch_gemm_f8_spec_bf16
                                        : launch_gemm_f8_spec_f16)
-        : set2 ? (out_dtype == GEMM_F32    ? launch_gemm_spec2_f32
-                  : out_dtype == GEMM_BF16 ? launch_gemm_spec2_bf16
-                                           : launch_gemm_spec2_f16)
-               : (out_dtype == GEMM_F32    ? launch_gemm_spec_f32
-                  : out_dtype == GEMM_BF16 ? launch_gemm_spec_bf16
-                                           : launch_gemm_spec_f16);
-    e = launch(p.bn, pair, p.split_k, layout, sk, readc, epi, mp, ka, p.grid, stream, dev);
+        : set == 3 ? (out_dtype == GEMM_F32    ? launch_gemm_spec3_f32
+                      : out_dtype == GEMM_BF16 ? launch_gemm_spec3_bf16
+                                               : launch_gemm_spec3_f16)
+        : set == 2 ? (out_dtype == GEMM_F32    ? launch_gemm_spec2_f32
+                      : out_dtype == GEMM_BF16 ? launch_gemm_spec2_bf16
+                                               : launch_gemm_spec2_f16)
+                   : (out_dtype == GEMM_F32    ? launch_gemm_spec_f32
+                      : out_dtype == GEMM_BF16 ? launch_gemm_spec_bf16
+                                               : launch_gemm_spec_f16);
+    e = launch(p.bn, pair, p.split_k, layout, sk, readc, epi, ragged, mp, ka, p.grid, stream, dev);
     if (e != cudaErrorNotSupported) return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
   }
   switch (out_dtype) {

@@ -451,12 +451,14 @@ enum : int {
   SPEC_STREAMK = 16,       // with SPEC_PLAIN: stream-K or split-tile work stays a run-time choice
   SPEC_READC = 32,         // with SPEC_PLAIN: C is read (beta != 0)
   SPEC_EPI = 64,           // with SPEC_PLAIN: a bias and/or an activation is applied
+  SPEC_RAGGED = 128,       // with SPEC_PLAIN: the ragged right edge stays a run-time choice
 };
 // the specialisation of a plain call with `layout` (stream-K work when sk, a C
-// read when readc, the fused epilogue when epi)
-constexpr int spec_bits(int layout, bool sk, bool readc, bool epi = false) {
+// read when readc, the fused epilogue when epi, a ragged right edge possible when
+// ragged)
+constexpr int spec_bits(int layout, bool sk, bool readc, bool epi = false, bool ragged = false) {
   return SPEC_PLAIN | SPEC_LAYOUT | (layout << SPEC_LAYOUT_SHIFT) | (sk ? SPEC_STREAMK : 0) |
-         (readc ? SPEC_READC : 0) | (epi ? SPEC_EPI : 0);
+         (readc ? SPEC_READC : 0) | (epi ? SPEC_EPI : 0) | (ragged ? SPEC_RAGGED : 0);
 }
 template <int SPEC, bool F8>
 __device__ __forceinline__ KernelArgs specialise_args(const KernelArgs& in) {
@@ -470,7 +472,7 @@ __device__ __forceinline__ KernelArgs specialise_args(const KernelArgs& in) {
       a.bias_kind = EPI_BIAS_NONE;
       a.act = EPI_ACT_NONE;
     }
-    a.n_ragged = 0;
+    if (!(SPEC & SPEC_RAGGED)) a.n_ragged = 0;
     if (!(SPEC & SPEC_STREAMK)) {
       a.sk_iters = 0;
       a.tile_split = 0;

@@ -56,9 +56,16 @@ cudaError_t launch_gemm_f8_f16(int bn, bool pair, int split, const OperandMaps& 
 // readc, or neither), the 2-way split-K clusters of width 128 and 64 and the
 // single 64-wide CTA; set 2, the CTA pair with the fused epilogue (epi; with or
 // without a stream-K tail) and the other single-panel choices (the single
-// 128-wide CTA, 4-way clusters of width 64 and 128, 2-way clusters of width
-// 256).  8-bit operands keep both sets in their own units.
-constexpr int spec_set(int bn, bool pair, int split, bool sk, bool readc, bool epi) {
+// 128-wide CTA, 4-way clusters of width 64 and 128, 8-way clusters of width 128,
+// 2-way clusters of width 256); set 3, the single CTA of width 64 or 128 when N times the output size is
+// not a multiple of 16 bytes (the ragged right edge, stored element by element,
+// stays a run-time choice): small and odd shapes, where the general kernel's
+// larger code costs microseconds of instruction fetches.  8-bit operands keep
+// every set in their own units.
+constexpr int spec_set(int bn, bool pair, int split, bool sk, bool readc, bool epi,
+                       bool ragged = false) {
+  if (ragged)
+    return (!pair && split == 1 && (bn == 64 || bn == 128) && !sk && !readc && !epi) ? 3 : 0;
   if (pair) {
     if (bn != 256 || split != 1) return 0;
     if (epi) return readc ? 0 : 2;
@@ -67,47 +74,56 @@ constexpr int spec_set(int bn, bool pair, int split, bool sk, bool readc, bool e
   if (sk || readc || epi) return 0;
   if ((split == 2 && (bn == 128 || bn == 64)) || (split == 1 && bn == 64)) return 1;
   if ((split == 1 && bn == 128) || (split == 4 && (bn == 128 || bn == 64)) ||
-      (split == 2 && bn == 256))
+      (split == 2 && bn == 256) || (split == 8 && bn == 128))
     return 2;
   return 0;
 }
 
 // Every layout has them (8-bit operands: A row-major with B column-major only).
 constexpr bool spec_supported(int bn, bool pair, int split, int layout, bool fp8, bool sk,
-                              bool readc, bool epi) {
+                              bool readc, bool epi, bool ragged = false) {
   if (layout < 0 || layout > 3 || (fp8 && layout != 2)) return false;
-  return spec_set(bn, pair, split, sk, readc, epi) != 0;
+  return spec_set(bn, pair, split, sk, readc, epi, ragged) != 0;
 }
 
-// Launch the specialised instance of (bn, pair, split, layout, sk, readc, epi), or return
+// Launch the specialised instance of (bn, pair, split, layout, sk, readc, epi, ragged), or return
 // cudaErrorNotSupported when spec_supported() says there is none.  Only for
 // calls on the plain path.
 cudaError_t launch_gemm_spec_f32(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                 bool epi, const OperandMaps& m, const KernelArgs& args,
+                                 bool epi, bool ragged, const OperandMaps& m, const KernelArgs& args,
                                  int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_spec_bf16(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                  bool epi, const OperandMaps& m, const KernelArgs& args,
+                                  bool epi, bool ragged, const OperandMaps& m, const KernelArgs& args,
                                   int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_spec_f16(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                 bool epi, const OperandMaps& m, const KernelArgs& args,
+                                 bool epi, bool ragged, const OperandMaps& m, const KernelArgs& args,
                                  int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_spec2_f32(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                  bool epi, const OperandMaps& m, const KernelArgs& args,
+                                  bool epi, bool ragged, const OperandMaps& m, const KernelArgs& args,
                                   int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_spec2_bf16(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                   bool epi, const OperandMaps& m, const KernelArgs& args,
+                                   bool epi, bool ragged, const OperandMaps& m, const KernelArgs& args,
                                    int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_spec2_f16(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                  bool epi, const OperandMaps& m, const KernelArgs& args,
+                                  bool epi, bool ragged, const OperandMaps& m, const KernelArgs& args,
                                   int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_spec3_f32(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                  bool epi, bool ragged, const OperandMaps& m,
+                                  const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_spec3_bf16(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                   bool epi, bool ragged, const OperandMaps& m,
+                                   const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_spec3_f16(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                  bool epi, bool ragged, const OperandMaps& m,
+                                  const KernelArgs& args, int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_f8_spec_f32(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                    bool epi, const OperandMaps& m, const KernelArgs& args,
+                                    bool epi, bool ragged, const OperandMaps& m, const KernelArgs& args,
                                     int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_f8_spec_bf16(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                     bool epi, const OperandMaps& m, const KernelArgs& args,
+                                     bool epi, bool ragged, const OperandMaps& m, const KernelArgs& args,
                                      int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_f8_spec_f16(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                    bool epi, const OperandMaps& m, const KernelArgs& args,
+                                    bool epi, bool ragged, const OperandMaps& m, const KernelArgs& args,
                                     int grid, cudaStream_t stream, int dev);
 
 // Split-K cluster shapes that have kernel instances: (bn, split).

@@ -76,10 +76,20 @@ namespace {
 // The specialised instances of one layout in this unit's set (see spec_set).
 template <int LAYOUT>
 cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc, bool epi,
-                               const OperandMaps& m, const KernelArgs& args, int grid,
+                               bool ragged, const OperandMaps& m, const KernelArgs& args, int grid,
                                cudaStream_t stream, int dev) {
   constexpr int S = spec_bits(LAYOUT, false, false);
-#if GEMM_SPEC_SET != 2
+#if GEMM_SPEC_SET == 0 || GEMM_SPEC_SET == 3
+  if (ragged) {
+    constexpr int R = spec_bits(LAYOUT, false, false, false, true);
+    if (!pair && split == 1 && bn == 64) return launch_inst<64, false, 1, R>(m, args, grid, stream, dev);
+    if (!pair && split == 1 && bn == 128) return launch_inst<128, false, 1, R>(m, args, grid, stream, dev);
+    return cudaErrorNotSupported;
+  }
+#else
+  if (ragged) return cudaErrorNotSupported;
+#endif
+#if GEMM_SPEC_SET == 0 || GEMM_SPEC_SET == 1
   if (pair && !epi) {
     if (sk) return launch_inst<256, true, 1, spec_bits(LAYOUT, true, false)>(m, args, grid, stream, dev);
     if (readc) return launch_inst<256, true, 1, spec_bits(LAYOUT, false, true)>(m, args, grid, stream, dev);
@@ -89,7 +99,7 @@ cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc
   if (split == 2 && bn == 64) return launch_inst<64, false, 2, S>(m, args, grid, stream, dev);
   if (split == 1 && bn == 64) return launch_inst<64, false, 1, S>(m, args, grid, stream, dev);
 #endif
-#if GEMM_SPEC_SET != 1
+#if GEMM_SPEC_SET == 0 || GEMM_SPEC_SET == 2
   if (pair) {
     constexpr int E = spec_bits(LAYOUT, false, false, true);
     if (sk) return launch_inst<256, true, 1, spec_bits(LAYOUT, true, false, true)>(m, args, grid, stream, dev);
@@ -99,25 +109,27 @@ cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc
   if (split == 4 && bn == 128) return launch_inst<128, false, 4, S>(m, args, grid, stream, dev);
   if (split == 4 && bn == 64) return launch_inst<64, false, 4, S>(m, args, grid, stream, dev);
   if (split == 2 && bn == 256) return launch_inst<256, false, 2, S>(m, args, grid, stream, dev);
+  if (split == 8 && bn == 128) return launch_inst<128, false, 8, S>(m, args, grid, stream, dev);
 #endif
   return cudaErrorNotSupported;
 }
 }  // namespace
 
 cudaError_t GEMM_LAUNCH_SPEC_NAME(int bn, bool pair, int split, int layout, bool sk, bool readc,
-                                  bool epi, const OperandMaps& m, const KernelArgs& args, int grid,
-                                  cudaStream_t stream, int dev) {
-  if (!spec_supported(bn, pair, split, layout, GEMM_F8, sk, readc, epi)) return cudaErrorNotSupported;
-  if (GEMM_SPEC_SET != 0 && spec_set(bn, pair, split, sk, readc, epi) != GEMM_SPEC_SET)
+                                  bool epi, bool ragged, const OperandMaps& m,
+                                  const KernelArgs& args, int grid, cudaStream_t stream, int dev) {
+  if (!spec_supported(bn, pair, split, layout, GEMM_F8, sk, readc, epi, ragged))
+    return cudaErrorNotSupported;
+  if (GEMM_SPEC_SET != 0 && spec_set(bn, pair, split, sk, readc, epi, ragged) != GEMM_SPEC_SET)
     return cudaErrorNotSupported;
   if constexpr (GEMM_F8) {   // 8-bit operands are K-major only
-    return launch_spec_layout<2>(bn, pair, split, sk, readc, epi, m, args, grid, stream, dev);
+    return launch_spec_layout<2>(bn, pair, split, sk, readc, epi, ragged, m, args, grid, stream, dev);
   } else {
     switch (layout) {
-      case 0: return launch_spec_layout<0>(bn, pair, split, sk, readc, epi, m, args, grid, stream, dev);
-      case 1: return launch_spec_layout<1>(bn, pair, split, sk, readc, epi, m, args, grid, stream, dev);
-      case 2: return launch_spec_layout<2>(bn, pair, split, sk, readc, epi, m, args, grid, stream, dev);
-      case 3: return launch_spec_layout<3>(bn, pair, split, sk, readc, epi, m, args, grid, stream, dev);
+      case 0: return launch_spec_layout<0>(bn, pair, split, sk, readc, epi, ragged, m, args, grid, stream, dev);
+      case 1: return launch_spec_layout<1>(bn, pair, split, sk, readc, epi, ragged, m, args, grid, stream, dev);
+      case 2: return launch_spec_layout<2>(bn, pair, split, sk, readc, epi, ragged, m, args, grid, stream, dev);
+      case 3: return launch_spec_layout<3>(bn, pair, split, sk, readc, epi, ragged, m, args, grid, stream, dev);
       default: return cudaErrorNotSupported;
     }
   }

@@ -1,7 +1,7 @@
 """Specialised kernel instances (the plain path -- beta == 0, no bias or activation,
-no ragged right edge, grouped tiles, data-parallel or with a stream-K tail on the
-CTA pair -- with the operand layout fixed at compile time) against the general
-kernel and the oracle.  The same call with
+grouped tiles, data-parallel or with a stream-K tail on the CTA pair, a ragged
+right edge only on single CTAs of width 64 or 128 -- with the operand layout fixed
+at compile time) against the general kernel and the oracle.  The same call with
 gemm_config_t.general = 0 and = 1 must give identical bits, and integer inputs
 must match the oracle exactly, in every layout and every configuration that has
 specialised instances."""
@@ -25,9 +25,16 @@ CASES = [({"cta_group": 2, "bn": 256}, 520, 776, 456),
          ({"cta_group": 1, "bn": 128}, 136, 520, 392),
          ({"cta_group": 1, "split_k": 4, "bn": 128}, 120, 392, 1096),
          ({"cta_group": 1, "split_k": 4, "bn": 64}, 72, 200, 1096),
-         ({"cta_group": 1, "split_k": 2, "bn": 256}, 130, 776, 648)]
+         ({"cta_group": 1, "split_k": 2, "bn": 256}, 130, 776, 648),
+         ({"cta_group": 1, "split_k": 8, "bn": 128}, 40, 264, 1096)]
 CASE_IDS = ["pair256", "pair256-streamk", "splitk2-bn128", "splitk2-bn64", "cta1-bn64", "cta1-bn128",
-            "splitk4-bn128", "splitk4-bn64", "splitk2-bn256"]
+            "splitk4-bn128", "splitk4-bn64", "splitk2-bn256", "splitk8-bn128"]
+# single CTAs whose right edge is ragged for every output format (N * 2 bytes not
+# a multiple of 16): their own specialised instances keep the predicated edge
+# stores and fold everything else
+RAGGED_CASES = [({"cta_group": 1, "bn": 64}, 73, 61, 67), ({"cta_group": 1, "bn": 64}, 257, 263, 251),
+                ({"cta_group": 1, "bn": 128}, 136, 517, 392), ({"cta_group": 1, "bn": 64}, 17, 65, 19)]
+RAGGED_IDS = ["bn64-73x61x67", "bn64-257x263x251", "bn128-136x517x392", "bn64-17x65x19"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -45,7 +52,7 @@ def _layout(a_col, b_col):
     return (1 if a_col else 0) | (2 if b_col else 0)
 
 
-@pytest.mark.parametrize("case", CASES, ids=CASE_IDS)
+@pytest.mark.parametrize("case", CASES + RAGGED_CASES, ids=CASE_IDS + RAGGED_IDS)
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
 @pytest.mark.parametrize("in_dtype,out_dtype", [("f16", "f32"), ("bf16", "bf16"), ("f16", "f16")])
 def test_specialised_matches_general_and_oracle(_lib, case, a_col, b_col, in_dtype, out_dtype):

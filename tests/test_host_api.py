@@ -438,10 +438,15 @@ def test_plan_specialised_flag():
     assert plan(2048, 2048, 2048, 1, 1, 0, 152, {"order": 2}) == 0
     # configurations without specialised instances
     assert plan(2048, 2048, 2048, 1, 1, 0, 152, {"cta_group": 1, "bn": 256}) == 0
-    assert plan(128, 8192, 8192, 1, 1, 2, 152, {"split_k": 8, "bn": 128}) == 0
     assert plan(128, 8192, 8192, 1, 1, 2, 152, {"split_k": 4, "bn": 256}) == 0
     # the second set: the other single-panel choices
     assert plan(128, 8192, 8192, 1, 1, 2, 152, {"split_k": 4, "bn": 128}) == 1
+    assert plan(32, 2048, 8192, 1, 1, 2, 152) == 1   # 8-way clusters of width 128
+    assert plan(128, 8192, 8192, 1, 1, 2, 152, {"split_k": 8, "bn": 128}) == 1
+    # the third set: single CTAs of width 64 or 128 with a ragged right edge
+    assert plan(73, 61, 67, 0, 2, 0, 152) == 1
+    assert plan(257, 263, 251, 0, 2, 0, 152) == 1
+    assert plan(257, 263, 251, 0, 2, 0, 152, {"bn": 256}) == 0
     assert plan(8, 14336, 4096, 1, 1, 2, 152) == 1   # the single 128-wide CTA
     assert plan(512, 512, 512, 0, 2, 0, 152) == 1   # the single 64-wide CTA
     # 8-bit operands: A row-major with B column-major only
