@@ -697,6 +697,9 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
         f8 ? (out_dtype == GEMM_F32    ? launch_gemm_f8_spec_f32
               : out_dtype == GEMM_BF16 ? launch_gemm_f8_spec_bf16
                                        : launch_gemm_f8_spec_f16)
+        : set == 4 ? (out_dtype == GEMM_F32    ? launch_gemm_spec4_f32
+                      : out_dtype == GEMM_BF16 ? launch_gemm_spec4_bf16
+                                               : launch_gemm_spec4_f16)
         : set == 3 ? (out_dtype == GEMM_F32    ? launch_gemm_spec3_f32
                       : out_dtype == GEMM_BF16 ? launch_gemm_spec3_bf16
                                                : launch_gemm_spec3_f16)

@@ -1369,6 +1369,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int prow = quarter * 32 + r;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
       const uint32_t rbase = smem_u32(smem) + RECV0;
+      // the first chunk's bias is loaded before the wait for the peers' slices
+      // (the loads' round trip overlaps it)
+      EpiBias eb0{0.0f, 0.0f, 0.0f, 0.0f};
+      if (args.epi) eb0 = load_epi_bias<CHUNK>(args, nb * BN + static_cast<int>(srank) * SLICE, row0 + r);
       bool ok = wait_warp<true>(rfull, 0, abort_flag, args, SITE_SPLITK_SLICES);
       received = ok;
       // chunks of PCH columns: whole epilogue chunks, or one slice narrower than a
@@ -1380,8 +1384,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int c = 0; ok && c < SLICE / PCH; ++c) {
         const int tcol = static_cast<int>(srank) * SLICE + c * PCH;   // column inside the tile
         const int col0 = nb * BN + tcol;
-        EpiBias eb{0.0f, 0.0f, 0.0f, 0.0f};
-        if (args.epi) eb = load_epi_bias<CHUNK>(args, col0, row0 + r);
+        EpiBias eb = eb0;
+        if (args.epi && c > 0) eb = load_epi_bias<CHUNK>(args, col0, row0 + r);
         uint8_t* stg;
         if (!begin_chunk<true, L::EPI_BUF_BYTES>(st, stg, &tmC, row0, col0, abort_flag, args,
                                                  args.read_c)) {

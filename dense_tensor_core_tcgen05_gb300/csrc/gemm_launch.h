@@ -60,12 +60,16 @@ cudaError_t launch_gemm_f8_f16(int bn, bool pair, int split, const OperandMaps& 
 // 2-way clusters of width 256); set 3, the single CTA of width 64 or 128 when N times the output size is
 // not a multiple of 16 bytes (the ragged right edge, stored element by element,
 // stays a run-time choice): small and odd shapes, where the general kernel's
-// larger code costs microseconds of instruction fetches.  8-bit operands keep
+// larger code costs microseconds of instruction fetches; set 4, the fused
+// epilogue (bias and/or activation, their kinds chosen at run time) on the single
+// CTA and the 2-way split-K cluster of width 64 or 128.  8-bit operands keep
 // every set in their own units.
 constexpr int spec_set(int bn, bool pair, int split, bool sk, bool readc, bool epi,
                        bool ragged = false) {
   if (ragged)
     return (!pair && split == 1 && (bn == 64 || bn == 128) && !sk && !readc && !epi) ? 3 : 0;
+  if (epi && !pair)
+    return (!sk && !readc && (split == 1 || split == 2) && (bn == 64 || bn == 128)) ? 4 : 0;
   if (pair) {
     if (bn != 256 || split != 1) return 0;
     if (epi) return readc ? 0 : 2;
@@ -114,6 +118,15 @@ cudaError_t launch_gemm_spec3_bf16(int bn, bool pair, int split, int layout, boo
                                    bool epi, bool ragged, const OperandMaps& m,
                                    const KernelArgs& args, int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_spec3_f16(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                  bool epi, bool ragged, const OperandMaps& m,
+                                  const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_spec4_f32(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                  bool epi, bool ragged, const OperandMaps& m,
+                                  const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_spec4_bf16(int bn, bool pair, int split, int layout, bool sk, bool readc,
+                                   bool epi, bool ragged, const OperandMaps& m,
+                                   const KernelArgs& args, int grid, cudaStream_t stream, int dev);
+cudaError_t launch_gemm_spec4_f16(int bn, bool pair, int split, int layout, bool sk, bool readc,
                                   bool epi, bool ragged, const OperandMaps& m,
                                   const KernelArgs& args, int grid, cudaStream_t stream, int dev);
 cudaError_t launch_gemm_f8_spec_f32(int bn, bool pair, int split, int layout, bool sk, bool readc,

@@ -89,6 +89,18 @@ cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc
 #else
   if (ragged) return cudaErrorNotSupported;
 #endif
+#if GEMM_SPEC_SET == 0 || GEMM_SPEC_SET == 4
+  if (epi && !pair) {
+    constexpr int E = spec_bits(LAYOUT, false, false, true);
+    if (split == 1 && bn == 64) return launch_inst<64, false, 1, E>(m, args, grid, stream, dev);
+    if (split == 1 && bn == 128) return launch_inst<128, false, 1, E>(m, args, grid, stream, dev);
+    if (split == 2 && bn == 64) return launch_inst<64, false, 2, E>(m, args, grid, stream, dev);
+    if (split == 2 && bn == 128) return launch_inst<128, false, 2, E>(m, args, grid, stream, dev);
+    return cudaErrorNotSupported;
+  }
+#else
+  if (epi && !pair) return cudaErrorNotSupported;
+#endif
 #if GEMM_SPEC_SET == 0 || GEMM_SPEC_SET == 1
   if (pair && !epi) {
     if (sk) return launch_inst<256, true, 1, spec_bits(LAYOUT, true, false)>(m, args, grid, stream, dev);

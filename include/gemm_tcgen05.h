@@ -141,16 +141,17 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *   general   1: always launch the general kernel.  0 (the default): a call on
  *             the plain path -- the grouped tile order -- runs a kernel instance
  *             specialised for its layout when the plan's configuration has
- *             one: with N times the output element size a multiple of 16
- *             bytes, the 256-wide CTA pair (beta == 0 with or without stream-K
+ *             one.  With N times the output element size a multiple of 16
+ *             bytes: the 256-wide CTA pair (beta == 0 with or without stream-K
  *             work, with or without a bias or activation; beta != 0 without
- *             stream-K work, bias or activation), and with beta == 0, no bias
- *             or activation and no stream-K work the single CTA of width 64 or
- *             128 and the split-K clusters of 2 CTAs (width 64, 128 or 256),
- *             of 4 CTAs (width 64 or 128) and of 8 CTAs (width 128); with any N, beta == 0, no bias
- *             or activation and no stream-K work, the single CTA of width 64 or
- *             128.  Both kernels compute the same result bit for bit.  Other
- *             values: GEMM_ERR_INVALID_ARG. */
+ *             stream-K work, bias or activation); with beta == 0 and no
+ *             stream-K work, the single CTA of width 64 or 128 and the split-K
+ *             clusters of 2 CTAs (width 64, 128 or 256), of 4 CTAs (width 64 or
+ *             128) and of 8 CTAs (width 128) without a bias or activation, and
+ *             the single CTA and the 2-CTA cluster of width 64 or 128 with one.
+ *             With any N, beta == 0, no bias or activation and no stream-K
+ *             work: the single CTA of width 64 or 128.  Both kernels compute
+ *             the same result bit for bit.  Other values: GEMM_ERR_INVALID_ARG. */
 enum { GEMM_ORDER_AUTO = 0, GEMM_ORDER_GROUPED = 1, GEMM_ORDER_HILBERT = 2 };
 
 typedef struct {

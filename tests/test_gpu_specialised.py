@@ -133,11 +133,18 @@ def test_specialised_beta(_lib, a_col, b_col, out_dtype):
 
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
 @pytest.mark.parametrize("mode", [{"cta_group": 2, "bn": 256},
-                                  {"cta_group": 2, "bn": 256, "stream_k": 2}], ids=["dp", "streamk"])
+                                  {"cta_group": 2, "bn": 256, "stream_k": 2},
+                                  {"cta_group": 1, "bn": 64}, {"cta_group": 1, "bn": 128},
+                                  {"cta_group": 1, "split_k": 2, "bn": 128},
+                                  {"cta_group": 1, "split_k": 2, "bn": 64}],
+                         ids=["dp", "streamk", "cta1-bn64", "cta1-bn128", "splitk2-bn128",
+                              "splitk2-bn64"])
 def test_specialised_fused_epilogue(_lib, a_col, b_col, mode):
-    """The CTA pair's fused-epilogue instances (bias per column or row, with and
-    without ReLU): exact on integers and identical to the general kernel."""
-    M, N, K = (520, 776, 456) if "stream_k" not in mode else (1032, 1288, 1000)
+    """The fused-epilogue instances (bias per column or row, with and without
+    ReLU) of the CTA pair, the single CTA and the 2-way split-K cluster: exact on
+    integers and identical to the general kernel."""
+    M, N, K = ((1032, 1288, 1000) if "stream_k" in mode else
+               (120, 776, 1096) if "split_k" in mode else (520, 776, 456))
     A, B = operands(M, N, K, "bf16", a_col, b_col, dist="int", seed=M + 3, pad=True)
     rng = np.random.default_rng(N)
     for kind in ("col", "row"):
