@@ -453,7 +453,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
     if (sk_mode == 2 || worth) {
       const int64_t dp = (waves > 0 ? waves - 1 : 0) * units;
       const int64_t sk = (p->num_tiles - dp) * int64_t(p->groups);
-      if (sk >= units && sk < (int64_t(1) << 40)) {
+      if (sk >= units && sk < (int64_t(1) << 31)) {   // the kernel's 32-bit stream-K range
         p->dp_tiles = static_cast<int32_t>(dp);
         p->sk_iters = sk;
       }
@@ -654,6 +654,7 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   ka.groups = p.groups;
   ka.dp_tiles = p.dp_tiles;
   ka.sk_iters = p.sk_iters;
+  ka.fd_groups = make_fastdiv(static_cast<uint32_t>(p.groups));
   ka.tile_split = p.tile_split;
   ka.owner_groups = p.owner_groups;
   ka.bias = bias;
@@ -904,8 +905,9 @@ int32_t gemm_work_items(int32_t unit, int32_t units, int32_t dp_tiles, int64_t s
                         int32_t groups, int32_t* items, int32_t max_items) {
   if (unit < 0 || units <= 0 || unit >= units || groups <= 0 || dp_tiles < 0 || sk_iters < 0)
     return 0;
+  if (sk_iters >= (int64_t(1) << 31)) return 0;
   WorkIter wi;
-  wi.init(unit, units, dp_tiles, sk_iters, groups);
+  wi.init(unit, units, dp_tiles, sk_iters, groups, make_fastdiv(static_cast<uint32_t>(groups)));
   WorkItem w;
   int32_t n = 0;
   while (wi.next(&w)) {
@@ -925,7 +927,7 @@ int32_t gemm_split_tile_item(int32_t unit, int32_t tile_split, int32_t owner_gro
       groups - owner_groups < tile_split - 1 || item == nullptr)
     return 0;
   WorkIter wi;
-  wi.init(unit, 0, 0, 0, groups, tile_split, owner_groups);
+  wi.init(unit, 1, 0, 0, groups, make_fastdiv(static_cast<uint32_t>(groups)), tile_split, owner_groups);
   WorkItem w;
   if (!wi.next(&w)) return 0;
   item[0] = w.tile;

@@ -143,43 +143,51 @@ GEMM_HD uint64_t make_sdesc_sw128(uint32_t smem_addr, uint32_t lbo_bytes, uint32
 // ------------------------------------------------------------- work split
 //
 // A launch's work is a list of tiles, each a sequence of `groups` k-groups (ring
-// stages).  Data-parallel phase: unit u (a CTA, or a CTA pair) takes whole tiles
-// u, u + units, ... below dp_tiles.  Stream-K phase: the remaining tiles' k-groups
-// form one iteration space of sk_iters = (num_tiles - dp_tiles) * groups entries,
-// split evenly: unit u takes [u * sk_iters / units, (u + 1) * sk_iters / units),
-// walked tile by tile.  The unit holding a tile's first k-groups owns the tile
-// (for it that is its last segment); every later unit touching the tile leaves
-// its share as a partial sum in its first (or only) segment, so partials are
-// ready long before their owner needs them and no unit waits on a chain.
+// stages).  Data-parallel tiles: unit u (a CTA, or a CTA pair) takes whole tiles
+// u, u + units, ... below dp_tiles.  Stream-K tiles: the remaining tiles'
+// k-groups form one iteration space of sk_iters = (num_tiles - dp_tiles) *
+// groups entries, split evenly: unit u takes [u * sk_iters / units,
+// (u + 1) * sk_iters / units), walked tile by tile.  A unit walks its stream-K
+// share first and its data-parallel tiles after it, so the stream-K fix-ups
+// (below) run while data-parallel mainloops keep the tensor cores busy, and the
+// launch ends on plain tiles.  The unit holding a tile's first k-groups owns
+// the tile (for it that is the last segment of its stream-K share); every later
+// unit touching the tile leaves its share as a partial sum in its first (or
+// only) segment, so partials are ready long before their owner needs them and
+// no unit waits on a chain.
 struct WorkItem {
   int tile, g0, g1;   // tile index and k-group range [g0, g1)
 };
 
-// Split-tile schedule (tile_split = s >= 2, instead of the two phases above):
+// Split-tile schedule (tile_split = s >= 2, instead of the two kinds above):
 // unit u works on tile u / s alone.  Part u % s = 0 takes k-groups
 // [0, owner_groups) and owns the tile; parts 1 .. s-1 split the remaining
 // k-groups evenly and leave partial sums.  The owner's share is the larger one,
 // so the other parts finish (and publish) while it is still accumulating.
+//
+// The stream-K range is worked out without 64-bit divisions (slow on the
+// device, and on the producer's path to its first copy): sk_iters < 2^31 (the
+// planner's limit), and with sk_iters = q * units + r, u * sk_iters / units =
+// u * q + (u * r) / units, all 32-bit; a position i is split into tile and
+// k-group by fastdiv (fg: make_fastdiv of groups).
 struct WorkIter {
-  int units, dp_tiles, groups, next_dp, unit;
-  long long i, hi, sk_iters;
+  int units, dp_tiles, groups, next_dp;
+  long long i, hi;
+  FastDiv fg;
   int st_tile, st_g0, st_g1;   // split-tile: the unit's one item (st_tile < 0: taken)
-  bool sk_ready;               // the stream-K range [i, hi) has been worked out
-  GEMM_HD void init(int unit_, int units_, int dp_tiles_, long long sk_iters_, int groups_,
-                    int tile_split = 0, int owner_groups = 0) {
+  GEMM_HD void init(int unit, int units_, int dp_tiles_, long long sk_iters, int groups_,
+                    const FastDiv& fg_, int tile_split = 0, int owner_groups = 0) {
     units = units_;
     dp_tiles = dp_tiles_;
     groups = groups_;
-    next_dp = unit_;
-    unit = unit_;
-    sk_iters = sk_iters_;
+    next_dp = unit;
+    fg = fg_;
     i = hi = 0;
-    sk_ready = false;
     st_tile = -1;
     st_g0 = st_g1 = 0;
     if (tile_split > 1) {
-      const int part = unit_ % tile_split;
-      st_tile = unit_ / tile_split;
+      const int part = unit % tile_split;
+      st_tile = unit / tile_split;
       if (part == 0) {
         st_g1 = owner_groups;
       } else {
@@ -188,7 +196,13 @@ struct WorkIter {
         st_g1 = owner_groups + (part * rest) / np;
       }
       dp_tiles = 0;
-      sk_iters = 0;
+    } else if (sk_iters != 0) {
+      const uint32_t u = static_cast<uint32_t>(units_);
+      const uint32_t q = static_cast<uint32_t>(sk_iters) / u;
+      const uint32_t r = static_cast<uint32_t>(sk_iters) - q * u;
+      const uint32_t ur = static_cast<uint32_t>(unit) * r;
+      i = static_cast<long long>(unit) * q + ur / u;
+      hi = static_cast<long long>(unit + 1) * q + (ur + r) / u;
     }
   }
   GEMM_HD bool next(WorkItem* w) {
@@ -199,30 +213,22 @@ struct WorkIter {
       st_tile = -1;
       return true;
     }
+    if (i < hi) {   // the stream-K share first
+      const int t = static_cast<int>(fastdiv(static_cast<uint32_t>(i), fg.mul, fg.shift));
+      const int g0 = static_cast<int>(i - static_cast<long long>(t) * groups);
+      const long long left = hi - i;
+      const int g1 = left < groups - g0 ? g0 + static_cast<int>(left) : groups;
+      w->tile = dp_tiles + t;
+      w->g0 = g0;
+      w->g1 = g1;
+      i += g1 - g0;
+      return true;
+    }
     if (next_dp < dp_tiles) {
       w->tile = next_dp;
       w->g0 = 0;
       w->g1 = groups;
       next_dp += units;
-      return true;
-    }
-    if (sk_iters != 0 && !sk_ready) {
-      // The unit's stream-K range, worked out only once its data-parallel tiles
-      // are handed out: 64-bit divisions are slow on the device, and the first
-      // item of a unit with data-parallel tiles must not wait for them.
-      i = (static_cast<long long>(unit) * sk_iters) / units;
-      hi = (static_cast<long long>(unit + 1) * sk_iters) / units;
-      sk_ready = true;
-    }
-    if (i < hi) {
-      const long long t = i / groups;
-      const int g0 = static_cast<int>(i - t * groups);
-      const long long left = hi - i;
-      const int g1 = left < groups - g0 ? g0 + static_cast<int>(left) : groups;
-      w->tile = dp_tiles + static_cast<int>(t);
-      w->g0 = g0;
-      w->g1 = g1;
-      i += g1 - g0;
       return true;
     }
     return false;
@@ -263,7 +269,8 @@ struct KernelArgs {
   // with M < BM: the rows of smem beyond them only feed accumulator rows >= M,
   // which are never stored).
   int a_box_rows;
-  long long sk_iters;
+  long long sk_iters;    // < 2^31
+  FastDiv fd_groups;     // make_fastdiv(groups), for WorkIter
   unsigned long long timeout_ns;
   int* status;           // device status word (0 = ok)
   // Tile order: NULL = grouped (tile_coord), else (m block, n block) of tile t

@@ -655,8 +655,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   };
   auto work_begin = [&](WorkIter& wi) {
-    wi.init(unit0, unit_stride, args.dp_tiles, args.sk_iters, args.groups, args.tile_split,
-            args.owner_groups);
+    wi.init(unit0, unit_stride, args.dp_tiles, args.sk_iters, args.groups, args.fd_groups,
+            args.tile_split, args.owner_groups);
   };
   uint32_t producer_iters = 0;  // ring iterations armed (producer thread only)
   // Start-up.  The lanes of warp 0 initialise the barriers (one each) while
@@ -1027,12 +1027,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     float tb[BN / 32] = {};   // the current tile's column bias (see the tile loop)
     float trb = 0.0f;         // ... or this thread's row bias
     // Write one finished tile: TMEM -> registers (+ the later units' partial
-    // sums, already summed in unit order in the TMEM buffer at t_part, when ADD)
-    // -> alpha * acc + beta * C (C read here when rc) -> output.  hold: the
+    // sums when ADD: already summed in unit order in the TMEM buffer at t_part
+    // when part_tmem, else loaded here from the scratch slots of units oc0 ..
+    // oc0 + ncontrib - 1, whose flags are up, and summed in the same order) ->
+    // alpha * acc + beta * C (C read here when rc) -> output.  hold: the
     // accumulator is not handed back here (the caller first writes the next
     // item's initial value into it).  Returns false if a wait gave up.
     auto store_tile = [&](auto add_tag, auto fused_tag, uint32_t t_row, uint32_t t_part, int nb,
-                          int row0, int buf, bool rc, bool hold) -> bool {
+                          int row0, int buf, bool rc, bool hold, bool part_tmem, int oc0,
+                          int ncontrib) -> bool {
       constexpr bool ADD = decltype(add_tag)::value;
       constexpr bool FUSED = decltype(fused_tag)::value;   // bias / activation
 #pragma unroll 1
@@ -1051,7 +1054,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t v0[32], v1[32];
         tmem_ld_32x32b_x32(t_row, v0, pc);
         if (CHUNK == 64) tmem_ld_32x32b_x32(t_row, v1, pc + 32);
-        if (ADD) {
+        if (ADD && part_tmem) {
           uint32_t p0[32], p1[32];
           tmem_ld_32x32b_x32(t_part, p0, pc);
           if (CHUNK == 64) tmem_ld_32x32b_x32(t_part, p1, pc + 32);
@@ -1060,6 +1063,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 32; ++i) {
             v0[i] = __float_as_uint(__uint_as_float(v0[i]) + __uint_as_float(p0[i]));
             if (CHUNK == 64) v1[i] = __float_as_uint(__uint_as_float(v1[i]) + __uint_as_float(p1[i]));
+          }
+        } else if (ADD) {
+          tmem_ld_wait();
+          // this chunk's columns of the partials (slot layout [quarter][BN/4
+          // pieces][32 rows][16 B]: 512 contiguous bytes per piece), 16 columns
+          // at a time (few registers: the next tile's mainloop hides this
+          // epilogue), summed in unit order and then added
+          const float4* base = reinterpret_cast<const float4*>(args.ws) +
+                               static_cast<size_t>(quarter) * BN * EPI_ROWS / 4 + lane;
+#pragma unroll
+          for (int h = 0; h < CHUNK / 16; ++h) {
+            float4 sp[4];
+#pragma unroll 1
+            for (int k = 0; k < ncontrib; ++k) {
+              const float4* src = base + static_cast<size_t>((oc0 + k) * UNIT_CTAS + rank) * (BM * BN / 4) +
+                                  static_cast<size_t>(pc / 4 + 4 * h) * EPI_ROWS;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float4 f = __ldcg(src + j * EPI_ROWS);
+                if (k == 0) {
+                  sp[j] = f;
+                } else {
+                  sp[j].x += f.x;
+                  sp[j].y += f.y;
+                  sp[j].z += f.z;
+                  sp[j].w += f.w;
+                }
+              }
+            }
+            uint32_t* vv = h < 2 ? v0 + 16 * h : v1 + 16 * (h - 2);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              vv[4 * j] = __float_as_uint(__uint_as_float(vv[4 * j]) + sp[j].x);
+              vv[4 * j + 1] = __float_as_uint(__uint_as_float(vv[4 * j + 1]) + sp[j].y);
+              vv[4 * j + 2] = __float_as_uint(__uint_as_float(vv[4 * j + 2]) + sp[j].z);
+              vv[4 * j + 3] = __float_as_uint(__uint_as_float(vv[4 * j + 3]) + sp[j].w);
+            }
           }
         } else {
           tmem_ld_wait();
@@ -1179,28 +1219,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // A work item holding its tile's first k-groups but not all of them owns
       // the tile: the units after it hold the later k-groups and leave partial
-      // sums.  It is always its unit's last item (the last segment of a
-      // stream-K unit, or the only item of a split-tile unit), so the other
-      // accumulator buffer is free: the partials are summed into it while this
-      // item's MMAs run, and the chunk loop adds them from there.
+      // sums, summed in unit order and added to this item's accumulator.  When
+      // the item is its unit's last (no data-parallel tiles follow, or a
+      // split-tile unit), the other accumulator buffer is free: the partials
+      // are summed into it while this item's MMAs run, and the chunk loop adds
+      // them from there.  Otherwise the chunk loop loads them itself, in an
+      // epilogue that the next tile's mainloop hides.
       const uint32_t t_part = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                               static_cast<uint32_t>((buf ^ 1) * BN);
-      int ncontrib = 0;
+      int ncontrib = 0, oc0 = 0;
+      bool part_tmem = false;
       if (!SPLITK && w.g0 == 0 && w.g1 < args.groups) {
-        int c0, c1;
-        owner_contributors(args, unit0, unit_stride, w, &c0, &c1);
-        ncontrib = c1 - c0;
-        if (h1) {   // not the unit's last item: the work split is broken
-          if (lane == 0) {
-            record_error(args.status, SITE_STREAMK_FLAG);
-            *abort_flag = 1;
+        int c1;
+        owner_contributors(args, unit0, unit_stride, w, &oc0, &c1);
+        ncontrib = c1 - oc0;
+        if (ncontrib > 0 && !h1) {
+          if (!preload_partials(oc0, ncontrib, t_part)) {
+            ok = false;
+            break;
           }
-          ok = false;
-          break;
-        }
-        if (ncontrib > 0 && !preload_partials(c0, ncontrib, t_part)) {
-          ok = false;
-          break;
+          part_tmem = true;
         }
       }
       if (!wait_warp<PAIR>(&tfull[buf], aph, abort_flag, args, SITE_EPI_TMEM_FULL)) {
@@ -1295,15 +1333,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         continue;
       }
+      if (ncontrib > 0 && !part_tmem) {   // the partials the chunk loop will load
+        bool got = true;
+        for (int k = 0; k < ncontrib && got; ++k)
+          got = wait_flag_warp(args.ws_flags + (oc0 + k) * UNIT_CTAS + rank);
+        if (!got) {
+          ok = false;
+          break;
+        }
+      }
       // one specialised chunk loop per case, chosen once per tile
       const BoolC<false> no;
       const BoolC<true> yes;
       if (ncontrib == 0)
-        ok = args.epi ? store_tile(no, yes, t_row, 0u, nb, row0, buf, rc, hold)
-                      : store_tile(no, no, t_row, 0u, nb, row0, buf, rc, hold);
+        ok = args.epi ? store_tile(no, yes, t_row, 0u, nb, row0, buf, rc, hold, false, 0, 0)
+                      : store_tile(no, no, t_row, 0u, nb, row0, buf, rc, hold, false, 0, 0);
       else
-        ok = args.epi ? store_tile(yes, yes, t_row, t_part, nb, row0, buf, rc, hold)
-                      : store_tile(yes, no, t_row, t_part, nb, row0, buf, rc, hold);
+        ok = args.epi ? store_tile(yes, yes, t_row, t_part, nb, row0, buf, rc, hold, part_tmem, oc0, ncontrib)
+                      : store_tile(yes, no, t_row, t_part, nb, row0, buf, rc, hold, part_tmem, oc0, ncontrib);
       if (ok && hold) {
         preload_c(w2, buf);
         release_acc(buf);

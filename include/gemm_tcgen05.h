@@ -318,10 +318,11 @@ int32_t gemm_tile_order(int order, int32_t m_tiles, int32_t n_tiles, int32_t gro
                         int32_t* m_blk, int32_t* n_blk, int32_t max_tiles);
 
 /* The work split of one unit (a CTA, or a CTA pair) for a plan, computed on the
- * host exactly as the kernel walks it: whole tiles unit, unit + units, ... below
- * dp_tiles, then the unit's even share of the sk_iters stream-K iterations, tile
- * by tile.  Writes up to max_items (tile, first k-group, end k-group) triples to
- * items[3*i .. 3*i+2] and returns the number of items the unit has. */
+ * host exactly as the kernel walks it: the unit's even share of the sk_iters
+ * stream-K iterations (sk_iters < 2^31), tile by tile, then the whole tiles
+ * unit, unit + units, ... below dp_tiles.  Writes up to max_items (tile, first
+ * k-group, end k-group) triples to items[3*i .. 3*i+2] and returns the number of
+ * items the unit has (0 for invalid arguments). */
 int32_t gemm_work_items(int32_t unit, int32_t units, int32_t dp_tiles, int64_t sk_iters,
                         int32_t groups, int32_t* items, int32_t max_items);
 
