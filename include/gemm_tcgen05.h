@@ -115,7 +115,8 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *             with split_k 2; one tile per cluster, so grid is ignored).
  *   stream_k  1: off; 2: on.  Stream-K runs all but the last whole wave of
  *             tiles data-parallel and splits the remaining tiles' k-groups evenly
- *             over all CTAs (or CTA pairs); a tile's partial sums are added by the
+ *             over all CTAs (or CTA pairs), each doing its stream-K share before
+ *             its data-parallel tiles; a tile's partial sums are added by the
  *             CTA that finishes it, in a fixed order, through a scratch buffer the
  *             library keeps per device and stream.  Ignored with split_k > 1.
  *             3: split-tile.  Every tile's k-groups are split over split_k CTAs
