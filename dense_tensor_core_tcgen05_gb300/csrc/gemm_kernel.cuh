@@ -1024,6 +1024,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       return true;
     };
 
+    // Owner whose item is not its unit's last, with one contributor (flag up):
+    // that unit's partial of this warp's 32 rows added onto the accumulator in
+    // TMEM at t_acc, GR 32-column groups per round (the same loads as
+    // preload_partials), so the tile is then stored like a whole one.  The
+    // sum is acc + partial, as the chunk loop's would be.
+    auto add_partial = [&](int c0, uint32_t t_acc) {
+      constexpr int GR = BN / 32 < 4 ? BN / 32 : 4;
+      const float4* src = reinterpret_cast<const float4*>(
+          args.ws + static_cast<size_t>(c0 * UNIT_CTAS + rank) * BM * BN +
+          static_cast<size_t>(quarter) * BN * EPI_ROWS) + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; c += GR) {
+        float4 v[8 * GR];
+#pragma unroll
+        for (int j = 0; j < 8 * GR; ++j) v[j] = __ldcg(src + static_cast<size_t>(c * 8 + j) * EPI_ROWS);
+#pragma unroll
+        for (int q = 0; q < GR; ++q) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_acc, r, (c + q) * 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 f = v[8 * q + j];
+            r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + f.x);
+            r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + f.y);
+            r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + f.z);
+            r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + f.w);
+          }
+          tmem_st_32x32b_x32(t_acc, r, (c + q) * 32);
+        }
+      }
+      tmem_st_wait();   // stored before the chunk loop reads the accumulator
+    };
+
     float tb[BN / 32] = {};   // the current tile's column bias (see the tile loop)
     float trb = 0.0f;         // ... or this thread's row bias
     // Write one finished tile: TMEM -> registers (+ the later units' partial
@@ -1340,6 +1374,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!got) {
           ok = false;
           break;
+        }
+        if (ncontrib == 1) {   // one contributor: added in TMEM, in batched loads
+          add_partial(oc0, t_row);
+          ncontrib = 0;
         }
       }
       // one specialised chunk loop per case, chosen once per tile
