@@ -730,6 +730,34 @@ gemm_status_t run_gemm(int64_t M, int64_t N, int64_t K, float alpha, const void*
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// Rows of C per panel of gemm_host's pipeline; M itself means one panel (the
+// copies and the GEMM in sequence).  A problem that moves at least 64 MiB over
+// the host link and has at least 2048 rows is cut into about 8 panels, each a
+// multiple of 256 rows (the CTA pair's tile height), so that one panel's copies
+// overlap the GEMMs of the panels before it and the copy-out of those after.
+int64_t host_panel_rows(int64_t M, int64_t link_bytes) {
+  if (link_bytes < (int64_t(64) << 20) || M < 2048) return M;
+  const int64_t rows = ceil_div(ceil_div(M, 8), 256) * 256;
+  return rows < M ? rows : M;
+}
+
+// One row panel [r0, r0 + rows) of a stored matrix (rows x cols elements of
+// esz bytes in the caller's view, leading dimension ld) between host and
+// device.  col_major: the matrix is stored column by column, so the panel is a
+// band of every stored column.
+cudaError_t copy_rows(void* dst, const void* src, int64_t ld, int64_t esz, int64_t r0, int64_t rows,
+                      int64_t cols, bool col_major, cudaMemcpyKind kind, cudaStream_t st) {
+  const size_t pitch = static_cast<size_t>(ld * esz);
+  const int64_t off = col_major ? r0 * esz : r0 * ld * esz;
+  char* d = static_cast<char*>(dst) + off;
+  const char* h = static_cast<const char*>(src) + off;
+  if (col_major)
+    return cudaMemcpy2DAsync(d, pitch, h, pitch, static_cast<size_t>(rows * esz),
+                             static_cast<size_t>(cols), kind, st);
+  return cudaMemcpy2DAsync(d, pitch, h, pitch, static_cast<size_t>(cols * esz),
+                           static_cast<size_t>(rows), kind, st);
+}
+
 }  // namespace
 
 namespace gemm_tc {
@@ -797,28 +825,74 @@ gemm_status_t gemm_host(int64_t M, int64_t N, int64_t K, float alpha, const void
   if (s != GEMM_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream_v);
   const bool a_col = (layout & GEMM_A_COL) != 0, b_col = (layout & GEMM_B_COL) != 0;
-  const size_t osz = static_cast<size_t>(out_size(out_dtype));
-  if (K > 0) {
-    const int64_t a_rows = a_col ? K : M, a_cols = a_col ? M : K;
-    const int64_t b_rows = b_col ? N : K, b_cols = b_col ? K : N;
-    const int64_t isz = in_size(in_dtype);
-    if (cudaMemcpy2DAsync(dA, lda * isz, hA, lda * isz, a_cols * isz, a_rows,
-                          cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpy2DAsync(dB, ldb * isz, hB, ldb * isz, b_cols * isz, b_rows,
-                          cudaMemcpyHostToDevice, st) != cudaSuccess)
+  const int64_t osz = out_size(out_dtype), isz = in_size(in_dtype);
+  const bool read_c = beta != 0.0f;
+  // B's stored extent: K rows of N (row-major) or N rows of K (column-major)
+  const int64_t b_rows = b_col ? N : K, b_cols = b_col ? K : N;
+  const int64_t link = (K > 0 ? (M + N) * K * isz : 0) + M * N * osz * (read_c ? 2 : 1);
+  const int64_t pr = K > 0 ? host_panel_rows(M, link) : M;
+  if (pr >= M) {
+    // one panel: copies in, GEMM, copy out, in order on the caller's stream
+    if (K > 0 && (copy_rows(dA, hA, lda, isz, 0, M, K, a_col, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+                  cudaMemcpy2DAsync(dB, ldb * isz, hB, ldb * isz, b_cols * isz, b_rows,
+                                    cudaMemcpyHostToDevice, st) != cudaSuccess))
       return GEMM_ERR_CUDA;
+    if (read_c && copy_rows(dC, hC, ldc, osz, 0, M, N, false, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    s = run_gemm(M, N, K, alpha, dA, lda, dB, ldb, beta, dC, ldc, in_dtype, out_dtype, layout,
+                 stream_v, nullptr);
+    if (s != GEMM_OK) return s;
+    if (copy_rows(hC, dC, ldc, osz, 0, M, N, false, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    return GEMM_OK;
   }
-  if (beta != 0.0f &&
-      cudaMemcpy2DAsync(dC, ldc * osz, hC, ldc * osz, N * osz, M, cudaMemcpyHostToDevice, st) !=
-          cudaSuccess)
-    return GEMM_ERR_CUDA;
-  s = run_gemm(M, N, K, alpha, dA, lda, dB, ldb, beta, dC, ldc, in_dtype, out_dtype, layout,
-               stream_v, nullptr);
-  if (s != GEMM_OK) return s;
-  if (cudaMemcpy2DAsync(hC, ldc * osz, dC, ldc * osz, N * osz, M, cudaMemcpyDeviceToHost, st) !=
-      cudaSuccess)
-    return GEMM_ERR_CUDA;
-  return GEMM_OK;
+  // Row panels.  A copy-in stream carries B, then each panel's rows of A (and
+  // of C when beta != 0); the caller's stream runs each panel's GEMM once its
+  // rows are in; a copy-out stream returns each panel's rows of C once its GEMM
+  // is done.  Events order the three; the caller's stream finally waits for the
+  // copy-out stream, so synchronising it covers the whole call.  The internal
+  // streams and events are released once their work completes.
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  std::vector<cudaEvent_t> evs;
+  evs.reserve(static_cast<size_t>(2 * ceil_div(M, pr) + 3));
+  auto mark = [&](cudaStream_t on, cudaStream_t waiter) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+    evs.push_back(e);
+    return cudaEventRecord(e, on) == cudaSuccess && cudaStreamWaitEvent(waiter, e, 0) == cudaSuccess;
+  };
+  bool ok = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) == cudaSuccess &&
+            mark(st, s_in) &&   // after whatever the caller queued before
+            cudaMemcpy2DAsync(dB, ldb * isz, hB, ldb * isz, b_cols * isz, b_rows,
+                              cudaMemcpyHostToDevice, s_in) == cudaSuccess;
+  gemm_status_t result = ok ? GEMM_OK : GEMM_ERR_CUDA;
+  for (int64_t r0 = 0; ok && r0 < M; r0 += pr) {
+    const int64_t rows = std::min(pr, M - r0);
+    ok = copy_rows(dA, hA, lda, isz, r0, rows, K, a_col, cudaMemcpyHostToDevice, s_in) == cudaSuccess &&
+         (!read_c || copy_rows(dC, hC, ldc, osz, r0, rows, N, false, cudaMemcpyHostToDevice, s_in) ==
+                         cudaSuccess) &&
+         mark(s_in, st);
+    if (!ok) {
+      result = GEMM_ERR_CUDA;
+      break;
+    }
+    const void* a_panel = static_cast<const char*>(dA) + (a_col ? r0 * isz : r0 * lda * isz);
+    void* c_panel = static_cast<char*>(dC) + r0 * ldc * osz;
+    result = run_gemm(rows, N, K, alpha, a_panel, lda, dB, ldb, beta, c_panel, ldc, in_dtype,
+                      out_dtype, layout, stream_v, nullptr);
+    ok = result == GEMM_OK && mark(st, s_out) &&
+         copy_rows(hC, dC, ldc, osz, r0, rows, N, false, cudaMemcpyDeviceToHost, s_out) == cudaSuccess;
+    if (!ok && result == GEMM_OK) result = GEMM_ERR_CUDA;
+  }
+  // the caller's stream waits for both internal streams, also after a failure
+  // (work already queued on them still touches the caller's buffers)
+  if (s_in && !mark(s_in, st) && result == GEMM_OK) result = GEMM_ERR_CUDA;
+  if (s_out && !mark(s_out, st) && result == GEMM_OK) result = GEMM_ERR_CUDA;
+  for (cudaEvent_t e : evs) cudaEventDestroy(e);
+  if (s_in) cudaStreamDestroy(s_in);
+  if (s_out) cudaStreamDestroy(s_out);
+  return result;
 }
 
 const char* gemm_status_string(gemm_status_t status) {

@@ -246,11 +246,21 @@ gemm_status_t gemm_ex_noalloc(int64_t M, int64_t N, int64_t K, float alpha, cons
  *
  * hA, hB, hC are host pointers (pinned memory gives asynchronous copies);
  * dA, dB, dC are caller-owned device buffers of at least the same extents
- * (rows * ld elements of each stored array), used as staging.  On `stream`
- * the call enqueues: copy hA -> dA and hB -> dB, copy hC -> dC when beta != 0,
- * the GEMM on the device buffers, and copy dC -> hC.  It returns without
- * synchronising; hC holds the result after the caller synchronises `stream`.
- * Same argument rules and errors as gemm() (pointer checks apply to both sets).
+ * (rows * ld elements of each stored array), used as staging.  The call
+ * enqueues copy hA -> dA and hB -> dB, copy hC -> dC when beta != 0, the GEMM
+ * on the device buffers, and copy dC -> hC, all ordered after the work already
+ * queued on `stream`.  It returns without synchronising; hC holds the result
+ * after the caller synchronises `stream`.
+ *   A problem that moves at least 64 MiB over the host link and has M >= 2048
+ * is pipelined by row panels of C (about 8, each a multiple of 256 rows): B is
+ * copied whole, then each panel's rows of A (and C) on an internal copy-in
+ * stream, each panel's GEMM runs on `stream` once its rows are in, and its
+ * rows of C return on an internal copy-out stream, so that copies in both
+ * directions overlap the GEMMs; `stream` finally waits for both internal
+ * streams.  Smaller problems run the four steps in order on `stream`.  Each
+ * panel is a GEMM of its own (its plan may differ from the whole problem's).
+ * Same argument rules and errors as gemm() (pointer checks apply to both sets);
+ * GEMM_ERR_CUDA if a copy, stream or event call fails.
  */
 gemm_status_t gemm_host(int64_t M, int64_t N, int64_t K, float alpha, const void* hA, int64_t lda,
                         const void* hB, int64_t ldb, float beta, void* hC, int64_t ldc,

@@ -426,6 +426,35 @@ def test_host_entry_point_e2e(_lib):
                          a_col=False, b_col=True, exact=True)
 
 
+@pytest.mark.parametrize("a_col,b_col,beta", [(False, True, 0.5), (True, False, 0.0)])
+def test_host_entry_point_pipelined(_lib, a_col, b_col, beta):
+    """gemm_host on a problem large enough for its row-panel pipeline (5 panels,
+    the last one ragged; copies on internal streams overlapping the panels'
+    GEMMs): every element exact against the oracle, C read when beta != 0."""
+    g = _lib
+    M, N, K = 2148, 4096, 4096
+    A, B = operands(M, N, K, "bf16", a_col, b_col, dist="int", seed=23, pad=True)
+    C = si.matrix("int", 91, M, N, "f32")
+    hA = torch.from_numpy(A.view(np.int16).copy()).pin_memory()
+    hB = torch.from_numpy(B.view(np.int16).copy()).pin_memory()
+    init = C.view(np.float32) if beta != 0.0 else np.full((M, N), np.nan, np.float32)
+    hC = torch.from_numpy(np.ascontiguousarray(init)).pin_memory()
+    dA = torch.empty(A.shape, dtype=torch.bfloat16, device="cuda")
+    dB = torch.empty(B.shape, dtype=torch.bfloat16, device="cuda")
+    dC = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    layout = (g.GEMM_A_COL if a_col else 0) | (g.GEMM_B_COL if b_col else 0)
+    s = g.gemm_host(M, N, K, 1.0, hA.data_ptr(), A.shape[1], hB.data_ptr(), B.shape[1], beta,
+                    hC.data_ptr(), N, g.GEMM_BF16, g.GEMM_F32, layout, dA.data_ptr(),
+                    dB.data_ptr(), dC.data_ptr(), st)
+    assert s == g.GEMM_OK
+    assert g.gemm_sync_status(st)[0] == g.GEMM_OK
+    out = hC.numpy().view(np.uint32)
+    check_against_oracle(out, A, B, M=M, N=N, K=K, in_dtype="bf16", out_dtype="f32",
+                         a_col=a_col, b_col=b_col, beta=beta, C=C if beta != 0.0 else None,
+                         exact=True)
+
+
 def test_device_checks_on_gpu(_lib):
     g = _lib
     a = torch.ones(64, 64, device="cuda", dtype=torch.float16)
