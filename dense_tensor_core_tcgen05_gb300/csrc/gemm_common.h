@@ -147,14 +147,18 @@ GEMM_HD uint64_t make_sdesc_sw128(uint32_t smem_addr, uint32_t lbo_bytes, uint32
 // u, u + units, ... below dp_tiles.  Stream-K tiles: the remaining tiles'
 // k-groups form one iteration space of sk_iters = (num_tiles - dp_tiles) *
 // groups entries, split evenly: unit u takes [u * sk_iters / units,
-// (u + 1) * sk_iters / units), walked tile by tile.  A unit walks its stream-K
-// share first and its data-parallel tiles after it, so the stream-K fix-ups
-// (below) run while data-parallel mainloops keep the tensor cores busy, and the
-// launch ends on plain tiles.  The unit holding a tile's first k-groups owns
-// the tile (for it that is the last segment of its stream-K share); every later
-// unit touching the tile leaves its share as a partial sum in its first (or
-// only) segment, so partials are ready long before their owner needs them and
-// no unit waits on a chain.
+// (u + 1) * sk_iters / units), walked tile by tile from its top down.  A unit
+// walks its stream-K share first and its data-parallel tiles after it, so the
+// stream-K fix-ups (below) run while data-parallel mainloops keep the tensor
+// cores busy, and the launch ends on plain tiles.  The unit holding a tile's
+// last k-groups owns the tile (for it that is the last segment of its stream-K
+// share); every earlier unit touching the tile leaves its share as a partial
+// sum in its first (or only) segment, so partials are ready long before their
+// owner needs them and no unit waits on a chain.  Walking down, the first
+// segment of every unit whose share spans tiles starts at k-group 0 of a tile,
+// as the first tiles of a data-parallel launch do: the neighbouring units'
+// first copies share operand panels in L2 rather than all coming from DRAM at
+// once.
 struct WorkItem {
   int tile, g0, g1;   // tile index and k-group range [g0, g1)
 };
@@ -213,15 +217,14 @@ struct WorkIter {
       st_tile = -1;
       return true;
     }
-    if (i < hi) {   // the stream-K share first
-      const int t = static_cast<int>(fastdiv(static_cast<uint32_t>(i), fg.mul, fg.shift));
-      const int g0 = static_cast<int>(i - static_cast<long long>(t) * groups);
-      const long long left = hi - i;
-      const int g1 = left < groups - g0 ? g0 + static_cast<int>(left) : groups;
+    if (i < hi) {   // the stream-K share first, from its last tile down
+      const int t = static_cast<int>(fastdiv(static_cast<uint32_t>(hi - 1), fg.mul, fg.shift));
+      const long long start = static_cast<long long>(t) * groups;
+      const long long lo = i > start ? i : start;
       w->tile = dp_tiles + t;
-      w->g0 = g0;
-      w->g1 = g1;
-      i += g1 - g0;
+      w->g0 = static_cast<int>(lo - start);
+      w->g1 = static_cast<int>(hi - start);
+      hi = lo;
       return true;
     }
     if (next_dp < dp_tiles) {
@@ -304,23 +307,35 @@ struct KernelArgs {
   int epi;               // 1 when bias_kind or act is set (selects the fused epilogue)
 };
 
+// Whether work item w finishes its tile: a whole tile, or the owner's segment
+// (the last k-groups for stream-K, the first for a split-tile part), which adds
+// the other units' partial sums and stores the output.  Every other item leaves
+// a partial sum.
+GEMM_HD bool item_finishes(const KernelArgs& a, const WorkItem& w) {
+  return a.tile_split > 1 ? w.g0 == 0 : w.g1 >= a.groups;
+}
+
 // Whether work item number `tl` of a unit (item `w`) starts from an accumulator
-// holding beta * C rather than zero (see KernelArgs::pre_c).  The MMA issuer and
-// the epilogue warps evaluate it on the same item sequence.
+// holding beta * C rather than zero (see KernelArgs::pre_c): only an item that
+// finishes its tile takes the C term.  The MMA issuer and the epilogue warps
+// evaluate it on the same item sequence.
 GEMM_HD bool item_preloads_c(const KernelArgs& a, uint32_t tl, const WorkItem& w) {
-  return a.pre_c && a.read_c && tl >= 2 && w.g0 == 0;
+  return a.pre_c && a.read_c && tl >= 2 && item_finishes(a, w);
 }
 
 // Units whose partial sums the owner of work item w (unit `unit` of `units`;
-// w holds its tile's first k-groups but not all of them) adds: [*c0, *c1).
+// w finishes its tile but does not hold all of its k-groups) adds, in unit
+// order: [*c0, *c1).  Stream-K: the units before it, down to the one holding
+// the tile's first k-group; split-tile: the tile's other parts, after it.
 GEMM_HD void owner_contributors(const KernelArgs& a, int unit, int units, const WorkItem& w,
                                 int* c0, int* c1) {
-  *c0 = unit + 1;
   if (a.tile_split > 1) {
+    *c0 = unit + 1;
     *c1 = unit + a.tile_split;
   } else {
     const long long base = static_cast<long long>(w.tile - a.dp_tiles) * a.groups;
-    *c1 = sk_unit_of(base + a.groups - 1, units, a.sk_iters) + 1;
+    *c0 = sk_unit_of(base, units, a.sk_iters);
+    *c1 = unit;
   }
 }
 

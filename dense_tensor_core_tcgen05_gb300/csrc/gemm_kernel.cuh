@@ -1251,9 +1251,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           trb = rr < args.M ? __ldg(args.bias + rr) : 0.0f;
         }
       }
-      // A work item holding its tile's first k-groups but not all of them owns
-      // the tile: the units after it hold the later k-groups and leave partial
-      // sums, summed in unit order and added to this item's accumulator.  When
+      // A work item that finishes its tile without holding all of its k-groups
+      // owns the tile: the other units touching it leave partial sums, summed
+      // in unit order and added to this item's accumulator.  When
       // the item is its unit's last (no data-parallel tiles follow, or a
       // split-tile unit), the other accumulator buffer is free: the partials
       // are summed into it while this item's MMAs run, and the chunk loop adds
@@ -1263,7 +1263,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                               static_cast<uint32_t>((buf ^ 1) * BN);
       int ncontrib = 0, oc0 = 0;
       bool part_tmem = false;
-      if (!SPLITK && w.g0 == 0 && w.g1 < args.groups) {
+      if (!SPLITK && item_finishes(args, w) && (w.g0 > 0 || w.g1 < args.groups)) {
         int c1;
         owner_contributors(args, unit0, unit_stride, w, &oc0, &c1);
         ncontrib = c1 - oc0;
@@ -1317,8 +1317,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (EARLY) push_rows();
         continue;   // one tile per split-K cluster; phase 2 follows
       }
-      if (w.g0 > 0) {
-        // Stream-K segment that does not hold its tile's first k-groups: publish
+      if (!item_finishes(args, w)) {
+        // Stream-K segment (or split-tile part) that does not finish its tile: publish
         // the fp32 partial sum in this CTA's scratch slot, hand the accumulator
         // back, then release the CTA's flag with the launch epoch.  Such a
         // segment is the first (or only) one of its unit, so it is published

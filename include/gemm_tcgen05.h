@@ -115,10 +115,11 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *             with split_k 2; one tile per cluster, so grid is ignored).
  *   stream_k  1: off; 2: on.  Stream-K runs all but the last whole wave of
  *             tiles data-parallel and splits the remaining tiles' k-groups evenly
- *             over all CTAs (or CTA pairs), each doing its stream-K share before
- *             its data-parallel tiles; a tile's partial sums are added by the
- *             CTA that finishes it, in a fixed order, through a scratch buffer the
- *             library keeps per device and stream.  Ignored with split_k > 1.
+ *             over all CTAs (or CTA pairs), each doing its stream-K share (from
+ *             its last tile down) before its data-parallel tiles; a tile's
+ *             partial sums are added by the CTA holding its last k-groups, in a
+ *             fixed order, through a scratch buffer the library keeps per device
+ *             and stream.  Ignored with split_k > 1.
  *             3: split-tile.  Every tile's k-groups are split over split_k CTAs
  *             (2 to 16; 0 means 2) of one-CTA tiles (bn 64, 128 or 256; 0 means
  *             128) without a cluster: the first CTA takes the first and larger
@@ -330,8 +331,8 @@ int32_t gemm_tile_order(int order, int32_t m_tiles, int32_t n_tiles, int32_t gro
 
 /* The work split of one unit (a CTA, or a CTA pair) for a plan, computed on the
  * host exactly as the kernel walks it: the unit's even share of the sk_iters
- * stream-K iterations (sk_iters < 2^31), tile by tile, then the whole tiles
- * unit, unit + units, ... below dp_tiles.  Writes up to max_items (tile, first
+ * stream-K iterations (sk_iters < 2^31), tile by tile from the share's last
+ * tile down, then the whole tiles unit, unit + units, ... below dp_tiles.  Writes up to max_items (tile, first
  * k-group, end k-group) triples to items[3*i .. 3*i+2] and returns the number of
  * items the unit has (0 for invalid arguments). */
 int32_t gemm_work_items(int32_t unit, int32_t units, int32_t dp_tiles, int64_t sk_iters,

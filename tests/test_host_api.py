@@ -222,9 +222,10 @@ def test_stream_k_split_covers_every_k_group_once(g, units, num_tiles, groups, w
                 assert (t, k) not in seen
                 seen[(t, k)] = u
     assert len(seen) == num_tiles * groups
-    # the units touching a split tile are consecutive, in k order; the lowest one
-    # (holding k-group 0) owns the tile and its share is that unit's last item,
-    # while every other unit's share is its first item
+    # the units touching a split tile are consecutive, in k order; the highest
+    # one (holding the last k-group) owns the tile and its share is that unit's
+    # last stream-K item, while every other unit's share is its first item; so a
+    # unit whose share spans tiles starts at k-group 0 of its first tile
     for t in range(dp, num_tiles):
         owners = [seen[(t, k)] for k in range(groups)]
         assert owners == sorted(owners)
@@ -233,10 +234,17 @@ def test_stream_k_split_covers_every_k_group_once(g, units, num_tiles, groups, w
             items = [it for it in g.gemm_work_items(u, units, dp, sk, groups) if it[0] >= dp]
             share = [it for it in items if it[0] == t]
             assert len(share) == 1
-            if u == owners[0] and len(set(owners)) > 1:
-                assert share[0] == items[-1] and share[0][1] == 0
-            elif u != owners[0]:
+            if u == owners[-1] and len(set(owners)) > 1:
+                assert share[0] == items[-1] and share[0][2] == groups
+            elif u != owners[-1]:
                 assert share[0] == items[0]
+            if u == owners[0]:
+                assert share[0][1] == 0
+    for u in range(units):
+        items = [it for it in g.gemm_work_items(u, units, dp, sk, groups) if it[0] >= dp]
+        if len(items) > 1:
+            assert items[0][1] == 0
+            assert [it[0] for it in items] == sorted((it[0] for it in items), reverse=True)
 
 
 def test_plan_overrides_and_errors(g):
