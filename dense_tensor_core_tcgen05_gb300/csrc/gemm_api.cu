@@ -426,12 +426,13 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   if (pair) grid = std::max(2, grid & ~1);
   // Work split: k-groups per tile, then stream-K for the last wave(s).  All but
   // the last whole wave stay data-parallel; the rest of the tiles' k-groups are
-  // shared evenly by all units.  Chosen automatically only when the last wave
-  // would leave at least half of the units idle and the run is 2 to 5 waves
-  // long: a GEMM this size runs at the GPU's power limit, so idle units in a
-  // short tail mostly let the busy ones clock higher, and with one wave (or
-  // many) the partial-sum traffic costs more than the tail saves (measured on
-  // GB300: 2048^3 and 3072^2 x 4096 slower with stream-K, 4096^3 faster).
+  // shared evenly by all units.  Chosen automatically when the run is at least
+  // 2 waves long and the last wave would leave at least a quarter of the units
+  // idle: with less than 2 waves every tile is split and the partial-sum
+  // traffic costs more than the tail saves, and an almost full last wave has
+  // little to balance (measured on GB300, same runs, us: 4096^3 76.5 / 78.6
+  // data-parallel, 6144^2 x 4096 164.5 / 172.7, 8192^3 615.6 / 619.1 with
+  // stream-K; 2048^3 27.3 / 21.1 and 3072^2 x 4096 51.8 / 47.8 without).
   const int ko = ko_for(bn, pair);
   p->groups = static_cast<int32_t>(ceil_div(kb, ko));
   p->dp_tiles = p->num_tiles;
@@ -449,7 +450,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_d
   } else if (split == 1 && sk_mode != 1 && grid <= kMaxSkCtas && grid <= num_sms) {
     const int64_t units = grid / per_unit;
     const int64_t waves = p->num_tiles / units, rem = p->num_tiles % units;
-    const bool worth = rem != 0 && 2 * rem <= units && waves >= 2 && waves <= 5 && p->groups >= 4;
+    const bool worth = rem != 0 && 4 * rem <= 3 * units && waves >= 2 && p->groups >= 4;
     if (sk_mode == 2 || worth) {
       const int64_t dp = (waves > 0 ? waves - 1 : 0) * units;
       const int64_t sk = (p->num_tiles - dp) * int64_t(p->groups);

@@ -55,7 +55,8 @@ cudaError_t launch_gemm_f8_f16(int bn, bool pair, int split, const OperandMaps& 
 // set 1, the 256-wide CTA pair (with a stream-K tail, sk, or with a C read,
 // readc, or neither), the 2-way split-K clusters of width 128 and 64 and the
 // single 64-wide CTA; set 2, the CTA pair with the fused epilogue (epi; with or
-// without a stream-K tail) and the other single-panel choices (the single
+// without a stream-K tail) or with both a stream-K tail and a C read, and the
+// other single-panel choices (the single
 // 128-wide CTA, 4-way clusters of width 64 and 128, 8-way clusters of width 128,
 // 2-way clusters of width 256); set 3, the single CTA of width 64 or 128 when N times the output size is
 // not a multiple of 16 bytes (the ragged right edge, stored element by element,
@@ -73,7 +74,7 @@ constexpr int spec_set(int bn, bool pair, int split, bool sk, bool readc, bool e
   if (pair) {
     if (bn != 256 || split != 1) return 0;
     if (epi) return readc ? 0 : 2;
-    return (sk && readc) ? 0 : 1;
+    return (sk && readc) ? 2 : 1;
   }
   if (sk || readc || epi) return 0;
   if ((split == 2 && (bn == 128 || bn == 64)) || (split == 1 && bn == 64)) return 1;

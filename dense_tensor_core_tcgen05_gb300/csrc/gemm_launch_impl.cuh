@@ -113,6 +113,8 @@ cudaError_t launch_spec_layout(int bn, bool pair, int split, bool sk, bool readc
 #endif
 #if GEMM_SPEC_SET == 0 || GEMM_SPEC_SET == 2
   if (pair) {
+    if (!epi)   // stream-K reading C
+      return launch_inst<256, true, 1, spec_bits(LAYOUT, true, true)>(m, args, grid, stream, dev);
     constexpr int E = spec_bits(LAYOUT, false, false, true);
     if (sk) return launch_inst<256, true, 1, spec_bits(LAYOUT, true, false, true)>(m, args, grid, stream, dev);
     return launch_inst<256, true, 1, E>(m, args, grid, stream, dev);

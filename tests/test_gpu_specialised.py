@@ -113,11 +113,13 @@ def test_specialised_fp8(_lib, fmt, case):
 
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
-def test_specialised_beta(_lib, a_col, b_col, out_dtype):
-    """The CTA pair's C-reading instances: beta * C exact on integers, and the
-    same bits as the general kernel."""
-    M, N, K = 520, 776, 456
-    cfg = {"cta_group": 2, "bn": 256}
+@pytest.mark.parametrize("streamk", [False, True], ids=["dp", "streamk"])
+def test_specialised_beta(_lib, a_col, b_col, out_dtype, streamk):
+    """The CTA pair's C-reading instances (data-parallel, and with a stream-K
+    tail, where only the item finishing a tile takes beta * C): exact on
+    integers, and the same bits as the general kernel."""
+    M, N, K = (1032, 1288, 1000) if streamk else (520, 776, 456)
+    cfg = {"cta_group": 2, "bn": 256, "stream_k": 2} if streamk else {"cta_group": 2, "bn": 256}
     A, B = operands(M, N, K, "bf16", a_col, b_col, dist="int", seed=N + K, pad=True)
     C = si.matrix("int", 77, M, pad8(N), out_dtype)
     for beta in (1.0, -2.0):

@@ -119,11 +119,18 @@ def test_no_cpu_fallback_without_device(g):
     # 104 tiles stream-K
     ((4096, 4096, 4096, 1, 1), 0, dict(cta_group=2, bn=256, num_tiles=256, grid=152,
                                        dp_tiles=152, sk_iters=104 * 32)),
-    # 1.89 waves (last one 89% full) and 13.5 waves: data-parallel
+    # 1.89 waves (under 2): data-parallel
     ((3072, 3072, 4096, 1, 1), 0, dict(cta_group=2, bn=256, num_tiles=144, grid=152,
                                        dp_tiles=144, sk_iters=0)),
+    # 13.47 waves, the last one 47% full: 12 data-parallel waves, the remaining
+    # 112 tiles stream-K
     ((8192, 8192, 8192, 1, 2), 2, dict(cta_group=2, bn=256, num_tiles=1024, grid=152, b_mn=0,
-                                       dp_tiles=1024, sk_iters=0)),
+                                       dp_tiles=912, sk_iters=112 * 64)),
+    # 7.58 waves, the last one 58% full: stream-K; 6.96 waves (the last one 96%
+    # full, less than a quarter idle): data-parallel
+    ((6144, 6144, 4096, 1, 1), 2, dict(cta_group=2, num_tiles=576, dp_tiles=6 * 76,
+                                       sk_iters=(576 - 6 * 76) * 32)),
+    ((5888, 5888, 4096, 1, 1), 2, dict(cta_group=2, num_tiles=529, dp_tiles=529, sk_iters=0)),
     # a single 128-row panel with long K: 128-wide tiles, K split over 2-CTA clusters
     ((128, 8192, 8192, 1, 1), 2, dict(cta_group=1, bm=128, bn=128, num_tiles=64, grid=128,
                                       k_blocks=128, stages=3, split_k=2)),
