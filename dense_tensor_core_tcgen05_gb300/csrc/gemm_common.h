@@ -154,13 +154,19 @@ GEMM_HD uint64_t make_sdesc_sw128(uint32_t smem_addr, uint32_t lbo_bytes, uint32
 // last k-groups owns the tile (for it that is the last segment of its stream-K
 // share); every earlier unit touching the tile leaves its share as a partial
 // sum in its first (or only) segment, so partials are ready long before their
-// owner needs them and no unit waits on a chain.  Walking down, the first
+// owner needs them and no unit waits on a chain.  A unit's data-parallel tiles
+// alternate the direction of their k loop (up, down, up, ...): the units run
+// their data-parallel rounds side by side, so each round starts with the
+// k-blocks the previous round loaded last, which are the ones still in L2
+// (the rows of A are shared by the rounds of one group of the grouped order).
+// Walking its stream-K share down, the first
 // segment of every unit whose share spans tiles starts at k-group 0 of a tile,
 // as the first tiles of a data-parallel launch do: the neighbouring units'
 // first copies share operand panels in L2 rather than all coming from DRAM at
 // once.
 struct WorkItem {
   int tile, g0, g1;   // tile index and k-group range [g0, g1)
+  int down;           // 1: the k-groups are walked from g1 - 1 down to g0
 };
 
 // Split-tile schedule (tile_split = s >= 2, instead of the two kinds above):
@@ -175,7 +181,7 @@ struct WorkItem {
 // u * q + (u * r) / units, all 32-bit; a position i is split into tile and
 // k-group by fastdiv (fg: make_fastdiv of groups).
 struct WorkIter {
-  int units, dp_tiles, groups, next_dp;
+  int units, dp_tiles, groups, next_dp, dp_round;
   long long i, hi;
   FastDiv fg;
   int st_tile, st_g0, st_g1;   // split-tile: the unit's one item (st_tile < 0: taken)
@@ -185,6 +191,7 @@ struct WorkIter {
     dp_tiles = dp_tiles_;
     groups = groups_;
     next_dp = unit;
+    dp_round = 0;
     fg = fg_;
     i = hi = 0;
     st_tile = -1;
@@ -214,6 +221,7 @@ struct WorkIter {
       w->tile = st_tile;
       w->g0 = st_g0;
       w->g1 = st_g1;
+      w->down = 0;
       st_tile = -1;
       return true;
     }
@@ -224,6 +232,7 @@ struct WorkIter {
       w->tile = dp_tiles + t;
       w->g0 = static_cast<int>(lo - start);
       w->g1 = static_cast<int>(hi - start);
+      w->down = 0;
       hi = lo;
       return true;
     }
@@ -231,7 +240,9 @@ struct WorkIter {
       w->tile = next_dp;
       w->g0 = 0;
       w->g1 = groups;
+      w->down = dp_round & 1;
       next_dp += units;
+      ++dp_round;
       return true;
     }
     return false;

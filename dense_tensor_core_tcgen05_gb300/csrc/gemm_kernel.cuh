@@ -753,7 +753,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         kb_range(w, &kb_begin, &kb_end);
         const int a_row = mb * TILE_M + static_cast<int>(rank) * BM;
         const int b_col = nb * BN + static_cast<int>(rank) * L::B_COLS;
-        for (int kb0 = kb_begin; kb0 < kb_end; kb0 += KO, ++it) {
+        const int steps = (kb_end - kb_begin + KO - 1) / KO;
+        const bool down = !SPLITK && w.down;
+        for (int q = 0; q < steps; ++q, ++it) {
+          const int kb0 = kb_begin + (down ? steps - 1 - q : q) * KO;
           const int nkb = kb_end - kb0 < KO ? kb_end - kb0 : KO;
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -896,8 +899,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        int si = 0;
-        for (int kb0 = kb_begin; kb0 < kb_end; kb0 += KO, ++it, ++si) {
+        const int steps = (kb_end - kb_begin + KO - 1) / KO;
+        const bool down = !SPLITK && w.down;
+        for (int si = 0; si < steps; ++si, ++it) {
+          const int kb0 = kb_begin + (down ? steps - 1 - si : si) * KO;
           const int nkb = kb_end - kb0 < KO ? kb_end - kb0 : KO;
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
