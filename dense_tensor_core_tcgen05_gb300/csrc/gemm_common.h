@@ -297,7 +297,7 @@ struct KernelArgs {
   int read_c;            // beta != 0
   // 1: beta * C is written into a tile's TMEM accumulator before its first MMA
   // (alpha == 1 only, so the accumulator then holds alpha*AB + beta*C), for every
-  // work item after a unit's first two that holds its tile's first k-groups.
+  // work item after a unit's first two that finishes its tile (item_preloads_c).
   int pre_c;
   int inject_skip;       // debug: the producer leaves ring iteration (inject_skip - 1) unarmed
   int num_tiles;

@@ -1022,7 +1022,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     };
-    // Owner of a tile whose later k-groups other units hold: once their flags
+    // Owner of a tile whose other k-groups other units hold: once their flags
     // are up, sum their partials of this warp's 32 rows (unit order c0, c0+1,
     // ...) into the TMEM accumulator buffer at t_part, which the unit no longer
     // uses (the owner item is the unit's last), while the item's own MMAs are
@@ -1113,7 +1113,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     float tb[BN / 32] = {};   // the current tile's column bias (see the tile loop)
     float trb = 0.0f;         // ... or this thread's row bias
-    // Write one finished tile: TMEM -> registers (+ the later units' partial
+    // Write one finished tile: TMEM -> registers (+ the other units' partial
     // sums when ADD: already summed in unit order in the TMEM buffer at t_part
     // when part_tmem, else loaded here from the scratch slots of units oc0 ..
     // oc0 + ncontrib - 1, whose flags are up, and summed in the same order) ->
