@@ -104,6 +104,13 @@ def test_no_cpu_fallback_without_device(g):
         pytest.skip("a device is present")
     s = g.gemm(128, 128, 128, 1.0, ALIGNED, 128, ALIGNED, 128, 0.0, ALIGNED, 128, 0, 2, 0, 0)
     assert s == g.GEMM_ERR_CUDA
+    # the host entry point too, on its single-panel path and on its row-panel
+    # pipeline (>= 64 MiB over the link, M >= 2048): its first copy or stream
+    # call fails before any buffer is touched, and the error comes back
+    for M, N, K in ((128, 128, 128), (4096, 4096, 4096)):
+        s = g.gemm_host(M, N, K, 1.0, ALIGNED, K, ALIGNED, N, 0.5, ALIGNED, N, 0, 2, 0,
+                        ALIGNED, ALIGNED, ALIGNED, 0)
+        assert s == g.GEMM_ERR_CUDA, (M, s)
     with pytest.raises(ValueError):
         g.matmul(torch.ones(4, 4, dtype=torch.float16), torch.ones(4, 4, dtype=torch.float16),
                  torch.ones(4, 4))
