@@ -494,6 +494,50 @@ def test_split_tile_plans(g):
         g.GEMM_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("units,num_tiles,groups,waves_dp", [
+    (76, 256, 16, 2), (76, 1024, 64, 12), (76, 64, 16, 0), (152, 60, 5, 0), (7, 23, 9, 2),
+    (5, 3, 4, 0), (76, 576, 32, 6), (3, 2, 40, 0), (64, 200, 3, 1)])
+def test_stream_k_schedule_has_no_wait_cycle(g, units, num_tiles, groups, waves_dp):
+    """Each unit runs its items in order (the MMA issuer and the epilogue walk the
+    same list, with two accumulator buffers); an item that finishes a split tile
+    waits until every other unit's segment of that tile is published.  Simulated
+    on the host from the kernel's own walk: every unit must get through its list,
+    i.e. no owner waits (directly or through its unit's earlier items) on a
+    segment that itself waits on that owner."""
+    dp = waves_dp * units
+    sk = (num_tiles - dp) * groups
+    items = {u: [tuple(it) for it in g.gemm_work_items(u, units, dp, sk, groups)]
+             for u in range(units)}
+    holders = {}
+    for u, its in items.items():
+        for t, g0, g1 in its:
+            if t >= dp:
+                holders.setdefault(t, []).append((u, g0, g1))
+    done = {u: 0 for u in range(units)}   # items finished per unit
+    published = set()                                # (unit, tile) segments published
+    progress = True
+    while progress:
+        progress = False
+        for u in range(units):
+            while done[u] < len(items[u]):
+                t, g0, g1 = items[u][done[u]]
+                whole = g0 == 0 and g1 == groups
+                if t >= dp and not whole and g1 == groups:
+                    # the owner: every other holder's segment must be out
+                    if any((v, t) not in published for v, _, _ in holders[t] if v != u):
+                        break
+                if t >= dp and g1 < groups:
+                    published.add((u, t))
+                done[u] += 1
+                progress = True
+    stuck = [u for u in range(units) if done[u] < len(items[u])]
+    assert not stuck, f"units {stuck[:8]} wait forever"
+    # and the kernel's contributor list is exactly the other holders, in unit order
+    for t, hs in holders.items():
+        us = sorted(v for v, _, _ in hs)
+        assert us == list(range(us[0], us[-1] + 1))
+
+
 @pytest.mark.parametrize("parts,groups", [(2, 64), (2, 2), (3, 7), (4, 64), (8, 33), (16, 16)])
 def test_split_tile_items_cover_each_tile_once(g, parts, groups):
     """Every k-group of a tile is held by exactly one of its parts; the first part
