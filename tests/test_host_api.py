@@ -163,6 +163,29 @@ def test_plan(g, shape, layout, expect):
     assert d["grid"] % d["cta_group"] == 0
 
 
+@pytest.mark.parametrize("M,N,expect_sk", [
+    (2816, 4864, True),    # 209 pair tiles: 2 waves + 57 (a quarter of 76 units idle)
+    (3584, 3840, False),   # 210: 2 waves + 58 (fewer than a quarter idle)
+    (2048, 4864, False),   # 152: exactly 2 waves, nothing to balance
+    (2816, 3584, True),    # 154: 2 waves + 2
+    (2048, 2048, False),   # 64: under 2 waves (every tile would be split)
+])
+def test_stream_k_rule_boundaries(g, M, N, expect_sk):
+    """The planner's automatic stream-K tail: at least 2 waves of tiles and a last
+    wave that leaves at least a quarter of the units idle; then all but the last
+    whole wave stay data-parallel."""
+    s, p = g.gemm_plan(M, N, 4096, 1, 1, 2, 152, {"cta_group": 2, "bn": 256})
+    assert s == 0
+    d = p.as_dict()
+    units = d["grid"] // 2
+    if expect_sk:
+        waves = d["num_tiles"] // units
+        assert d["sk_iters"] > 0 and d["dp_tiles"] == (waves - 1) * units, d
+        assert d["sk_iters"] == (d["num_tiles"] - d["dp_tiles"]) * d["groups"]
+    else:
+        assert d["sk_iters"] == 0 and d["dp_tiles"] == d["num_tiles"], d
+
+
 def test_plan_prefers_pairs_only_with_more_than_one_panel(g):
     for M in (1, 64, 128):
         s, p = g.gemm_plan(M, 4096, 4096, 1, 1, 0, 152)
