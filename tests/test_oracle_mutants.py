@@ -11,6 +11,7 @@ import shutil
 import pytest
 
 import test_oracle_epilogue_pins as EP
+import test_oracle_fp8_pins as F8
 import test_oracle_pins as P
 
 ORACLE_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
@@ -44,6 +45,17 @@ MUTANTS = [
     ("fp16 subnormal scale", "return s | (uint16_t)ldexp(ay, 24);",
      "return s | (uint16_t)ldexp(ay, 23);"),
     ("scale term without |a|", "scl[j] += aa * fabs(b);", "scl[j] += fabs(b);"),
+    ("E4M3 exponent bias off by one", "v = ldexp((double)(8 + m), e - 10);",
+     "v = ldexp((double)(8 + m), e - 11);"),
+    ("E4M3 subnormals scaled as normals", "v = ldexp((double)m, -9);",
+     "v = ldexp((double)(8 + m), -10);"),
+    ("E4M3 with an infinity", "else if (e == 15 && m == 7)\n        v = NAN;",
+     "else if (e == 15 && m == 7)\n        v = INFINITY;"),
+    ("E5M2 infinity read as NaN",
+     "/* m/4 * 2^(1-15) */\n    else if (e == 31)\n        v = m ? NAN : INFINITY;",
+     "/* m/4 * 2^(1-15) */\n    else if (e == 31)\n        v = NAN;"),
+    ("E5M2 mantissa with three bits", "int s = (b >> 7) & 1, e = (b >> 2) & 0x1F, m = b & 0x3;",
+     "int s = (b >> 7) & 1, e = (b >> 2) & 0x1F, m = b & 0x7;"),
 ]
 
 # the pins, as (test module, function, keyword arguments)
@@ -67,6 +79,9 @@ PINS = [
     (EP, "test_brute_force_dyadic_exact_bias_relu", dict(seed=1)),
     (EP, "test_brute_force_dyadic_exact_bias_relu", dict(seed=2)),
     (EP, "test_brute_force_dyadic_exact_bias_relu", dict(seed=3)),
+    (F8, "test_decode_all_fp8_patterns", dict(fmt="e4m3")),
+    (F8, "test_decode_all_fp8_patterns", dict(fmt="e5m2")),
+    (F8, "test_fp8_gemm_brute_force_exact", dict(seed=0)),
 ]
 
 
