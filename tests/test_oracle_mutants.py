@@ -45,6 +45,14 @@ MUTANTS = [
     ("fp16 subnormal scale", "return s | (uint16_t)ldexp(ay, 24);",
      "return s | (uint16_t)ldexp(ay, 23);"),
     ("scale term without |a|", "scl[j] += aa * fabs(b);", "scl[j] += fabs(b);"),
+    ("ties rounded away from zero", "r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;",
+     "r = fl + 1.0;"),
+    ("rounding by truncation", "if (d > 0.5)\n        r = fl + 1.0;",
+     "if (d > 2.0)\n        r = fl + 1.0;"),
+    ("no overflow to infinity", "if (y > maxf) return copysign(INFINITY, x);",
+     "if (y > maxf) return copysign(maxf, x);"),
+    ("subnormal quantum not fixed", "if (E < emin) E = emin;        /* subnormal range: fixed quantum */",
+     "/* subnormal range not special-cased */"),
     ("E4M3 exponent bias off by one", "v = ldexp((double)(8 + m), e - 10);",
      "v = ldexp((double)(8 + m), e - 11);"),
     ("E4M3 subnormals scaled as normals", "v = ldexp((double)m, -9);",
