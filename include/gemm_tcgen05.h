@@ -145,8 +145,8 @@ gemm_status_t gemm(int64_t M, int64_t N, int64_t K, float alpha, const void* A, 
  *             specialised for its layout when the plan's configuration has
  *             one.  With N times the output element size a multiple of 16
  *             bytes: the 256-wide CTA pair (beta == 0 with or without stream-K
- *             work, with or without a bias or activation; beta != 0 without
- *             stream-K work, bias or activation); with beta == 0 and no
+ *             work, with or without a bias or activation; beta != 0 with or
+ *             without stream-K work, without a bias or activation); with beta == 0 and no
  *             stream-K work, the single CTA of width 64 or 128 and the split-K
  *             clusters of 2 CTAs (width 64, 128 or 256), of 4 CTAs (width 64 or
  *             128) and of 8 CTAs (width 128) without a bias or activation, and
